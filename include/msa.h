@@ -1,0 +1,203 @@
+/*
+ * msa.h — C ABI of libmsa: MInference-style dynamic sparse prefill attention
+ * on one GB300 (sm_103a).
+ *
+ * The method (PaperTrace 2.1.2 "MInference: 按 head 模式加速长上下文 Prefill",
+ * §1.1, eq.(1)-(2)): each attention head h of one layer restricts the causal
+ * softmax of query row i to a candidate set N_h(i) ⊆ {j <= i} and computes
+ *   o_hi = Σ_{j in N_h(i)} exp(s_hij) v_hj / Σ_{t in N_h(i)} exp(s_hit),
+ *   s_hij = scale * q_hi . k_hj.
+ * Which set a head uses comes from a per-head config table (same page, §1.1
+ * and §3.1): A-shape (eq.(3)), Vertical-Slash (eq.(5)) or Block-Sparse
+ * (eq.(6)).  Vertical-Slash and Block-Sparse sets are built per request from a
+ * cheap proxy (§3.1, §6.2; "LLM模型之MInference" blog §2.3.2).
+ *
+ * Conventions shared by every call:
+ *  - Q, O: [B, Hq, n, d_h] bf16; K, V: [B, Hkv, n, d_h] bf16; all contiguous
+ *    device memory with 16-byte-aligned base addresses.  LSE: [B, Hq, n] fp32
+ *    (natural log of the softmax denominator; -inf for an empty set).
+ *  - GQA: query head h reads KV head h / (Hq / Hkv) (same page §5.1, "head
+ *    dispatch and GQA mapping"); K/V are never repeated in memory.
+ *  - d_h ∈ {64, 128}; Vertical-Slash and Block-Sparse blocks are 64 rows.
+ *  - `heads` (host array of n_heads distinct query-head indices in [0, Hq))
+ *    selects the heads a call works on; index arrays are laid out by "slot"
+ *    = b * n_heads + position in `heads`.
+ *  - Every buffer, including the workspace, is allocated and owned by the
+ *    caller; the library keeps no allocation between calls.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Arguments are validated on the host before anything
+ *    is launched: a bad argument returns an error and launches nothing.
+ *    Faults detected on the device (a bounded wait that timed out, an index
+ *    out of range) are recorded in a device error word that
+ *    msa_poll_device_status() reads; outputs of a failed call are undefined.
+ *  - No call synchronises with the host (no device-to-host copy on the path).
+ */
+#ifndef MSA_H
+#define MSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MSA_API __attribute__((visibility("default")))
+#else
+#define MSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1,         /* bad pointer, shape, head list or budget */
+  MSA_ERR_UNSUPPORTED = 2,         /* valid request outside the supported set (d_h, block) */
+  MSA_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes below the matching *_workspace() size */
+  MSA_ERR_CUDA = 4,                /* a CUDA runtime call failed */
+  MSA_ERR_DEVICE_TIMEOUT = 5,      /* a kernel's bounded wait gave up (reported by the poll) */
+  MSA_ERR_INDEX = 6                /* an index entry out of range (reported by the poll) */
+} msa_status;
+
+typedef enum { MSA_ASHAPE = 0, MSA_VS = 1, MSA_BLOCK = 2 } msa_pattern;
+
+/* Problem shape.  scale <= 0 selects 1/sqrt(d_h) (eq.(1)). */
+typedef struct {
+  int32_t B, Hq, Hkv, n, d_h;
+  float scale;
+} msa_shape;
+
+/* One head's entry of the layer x head config table (MInference page §1.1:
+ * best_pattern per layer and head with its budgets; §6.3: pattern type,
+ * vertical / slash counts, block count, window, initial tokens, block size). */
+typedef struct {
+  int32_t pattern;    /* msa_pattern */
+  int32_t sink;       /* A-shape: g initial tokens */
+  int32_t window;     /* A-shape: w local window (>= 1) */
+  int32_t last_q;     /* Vertical-Slash: proxy rows, the last last_q queries */
+  int32_t n_vertical; /* Vertical-Slash: v columns kept */
+  int32_t n_slash;    /* Vertical-Slash: s diagonal offsets kept */
+  int32_t block;      /* Vertical-Slash / Block-Sparse block size (64) */
+  int32_t topk;       /* Block-Sparse: k_b key blocks per query block (>= 1) */
+} msa_head_cfg;
+
+/* Vertical-Slash index of a set of heads (device buffers owned by the caller).
+ * For slot s (see conventions), with v_cap = min(n_vertical, n) and
+ * s_cap = min(n_slash, n) and words = ceil(n / 32):
+ *   vertical[s * v_cap + t]   column indices C_h, ascending (t < vertical_cnt[s])
+ *   slash[s * s_cap + t]      diagonal offsets D_h (δ = i - j), descending
+ *   vertical_bits[s * words]  bit j set iff j ∈ C_h
+ *   slash_bits[s * words]     bit δ set iff δ ∈ D_h
+ * (MInference blog §2.3.3: verticals sorted ascending, slashes descending.) */
+typedef struct {
+  int32_t* vertical;
+  int32_t* vertical_cnt;
+  int32_t* slash;
+  int32_t* slash_cnt;
+  uint32_t* vertical_bits;
+  uint32_t* slash_bits;
+  int32_t v_cap;
+  int32_t s_cap;
+} msa_vs_index;
+
+/* Status as text (static storage). */
+MSA_API const char* msa_status_string(msa_status s);
+
+/* Workspace bytes msa_build_vs_index needs for n_heads heads with budgets cfg
+ * (0 on invalid arguments). */
+MSA_API size_t msa_vs_index_workspace(const msa_shape* shape, const msa_head_cfg* cfg, int32_t n_heads);
+
+/* Workspace bytes msa_build_block_index needs (0 on invalid arguments). */
+MSA_API size_t msa_block_index_workspace(const msa_shape* shape, int32_t block, int32_t n_heads);
+
+/* Workspace bytes msa_prefill_layer needs for this table (Hq entries); it
+ * holds the per-request indices and the index builders' scratch. */
+MSA_API size_t msa_layer_workspace(const msa_shape* shape, const msa_head_cfg* table);
+
+/* Online Vertical-Slash index (MInference page §2.1 and §6.2; blog §2.3.2
+ * Vertical-Slash steps 1-3).  For each listed head h, with the last
+ * L = min(last_q, n) query rows R:
+ *   Ã_ij = softmax over j <= i of scale * q_i.k_j       (i in R)
+ *   c_j = Σ_{i in R} Ã_ij,  r_δ = Σ_{i in R, i >= δ} Ã_{i,i-δ}
+ *   C_h = top-v of c, D_h = top-s of r (ties to the lower index).
+ * Scores are fp32 from bf16 tensor-core products.  Writes `out` (layout
+ * above).  q: [B,Hq,n,d_h], k: [B,Hkv,n,d_h].  Requires ws_bytes >=
+ * msa_vs_index_workspace(shape, cfg, n_heads). */
+MSA_API msa_status msa_build_vs_index(const msa_shape* shape, const void* q, const void* k, const int32_t* heads,
+                              int32_t n_heads, const msa_head_cfg* cfg, const msa_vs_index* out, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* Online Block-Sparse index (MInference page eq.(6) and §2.1 last paragraph;
+ * blog §2.3.2 Block-Sparse steps 1-3): Q̄_u, K̄_v = means of the real tokens
+ * of each 64-row block, r_uv = Q̄_u . K̄_v, and
+ *   J_u = {u} ∪ top_{k_b - 1} { v < u } by r_uv   (ties to the lower v),
+ * i.e. the causal diagonal block is always kept and counts toward k_b.
+ * block_idx: [B, n_heads, N_b, topk] int32, ascending, -1 padded;
+ * block_cnt: [B, n_heads, N_b] int32 = min(topk, u + 1).  N_b = ceil(n/64). */
+MSA_API msa_status msa_build_block_index(const msa_shape* shape, const void* q, const void* k, const int32_t* heads,
+                                 int32_t n_heads, int32_t block, int32_t topk, int32_t* block_idx,
+                                 int32_t* block_cnt, void* ws, size_t ws_bytes, void* stream);
+
+/* A-shape attention (MInference page eq.(3)): N_A(i) = {0..min(g-1,i)} ∪
+ * {max(0,i-w+1)..i}, exact (each key once).  o: [B,Hq,n,d_h] (only the listed
+ * heads are written); lse nullable; edges nullable: if given, [B*Hq] int64
+ * device counters to which each head's attended-edge count E_h is ADDED. */
+MSA_API msa_status msa_attn_ashape(const msa_shape* shape, const void* q, const void* k, const void* v,
+                           const int32_t* heads, int32_t n_heads, int32_t sink, int32_t window, void* o,
+                           float* lse, int64_t* edges, void* stream);
+
+/* Vertical-Slash attention over the physical set of row i in query block
+ * u = [a, e] (MInference page §2.1 "1x64 verticals, 64x64 slash tiles" and
+ * §4.1 "verticals as points, slashes as intervals"):
+ *   N(i) = ( ∪_{δ in D_h} [a-δ, e-δ]  ∪  C_h ) ∩ [0, i].
+ * index: as written by msa_build_vs_index for the same `heads`. */
+MSA_API msa_status msa_attn_vs(const msa_shape* shape, const void* q, const void* k, const void* v, const int32_t* heads,
+                       int32_t n_heads, int32_t block, const msa_vs_index* index, void* o, float* lse,
+                       int64_t* edges, void* stream);
+
+/* Block-Sparse attention (MInference page eq.(6)): row i of block u attends
+ * the keys of blocks v in J_u with j <= i (the diagonal block is causal).
+ * block_idx / block_cnt: as written by msa_build_block_index. */
+MSA_API msa_status msa_attn_block(const msa_shape* shape, const void* q, const void* k, const void* v,
+                          const int32_t* heads, int32_t n_heads, int32_t block, int32_t topk,
+                          const int32_t* block_idx, const int32_t* block_cnt, void* o, float* lse,
+                          int64_t* edges, void* stream);
+
+/* One layer's sparse prefill attention dispatched per head from the table
+ * (MInference page §5.1 "head dispatch": each head reads its pattern, VS and
+ * BS heads build their index online, then every head's sparse kernel runs).
+ * table: host array of Hq entries.  All indices are built in `ws` and the
+ * three patterns run in one attention launch ordered longest-work-first, with
+ * no host synchronisation between index and attention. */
+MSA_API msa_status msa_prefill_layer(const msa_shape* shape, const void* q, const void* k, const void* v,
+                             const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/* Pointers into a msa_prefill_layer workspace: where that call left the
+ * Vertical-Slash index (slot = b * n_vs + rank of the head among the table's
+ * VS heads) and the Block-Sparse index (likewise among BS heads).  Any
+ * output pointer may be NULL.  Valid until the workspace is reused. */
+MSA_API msa_status msa_layer_indices(const msa_shape* shape, const msa_head_cfg* table, void* ws, msa_vs_index* vs,
+                             int32_t** block_idx, int32_t** block_cnt);
+
+/* Expand the compact Vertical-Slash index of one slot into the explicit
+ * per-query-block form of the MInference blog §2.3.3 (block count / block
+ * ranges, column count / column indices) for blocks u_begin .. u_begin +
+ * u_count - 1: merged inclusive key ranges ∪_{δ} [a-δ, e-δ] ∩ [0, e] and the
+ * verticals c <= e not inside a range, ascending.  Device outputs:
+ *   range_cnt[u_count], ranges[u_count][range_cap][2], col_cnt[u_count],
+ *   cols[u_count][col_cap].  Entries beyond a cap are dropped and the count
+ *   still reports the full number. */
+MSA_API msa_status msa_vs_expand(const msa_shape* shape, const msa_vs_index* index, int32_t slot, int32_t u_begin,
+                         int32_t u_count, int32_t range_cap, int32_t col_cap, int32_t* range_cnt,
+                         int32_t* ranges, int32_t* col_cnt, int32_t* cols, void* stream);
+
+/* Synchronise `stream`, read and clear the device error word of the current
+ * device.  Returns MSA_OK, MSA_ERR_DEVICE_TIMEOUT, MSA_ERR_INDEX or
+ * MSA_ERR_CUDA. */
+MSA_API msa_status msa_poll_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H */

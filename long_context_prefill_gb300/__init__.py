@@ -1,0 +1,328 @@
+"""Python binding of libmsa (MInference-style dynamic sparse prefill attention
+on sm_103a).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  There is no fallback:
+if ``libmsa.so`` is missing or cannot be loaded, every call raises.
+
+Function names mirror the C ABI in ``include/msa.h`` without the ``msa_``
+prefix.  Tensors: Q/O [B,Hq,n,d] bf16, K/V [B,Hkv,n,d] bf16 (contiguous, on
+the current CUDA device); ``heads`` is a list of query-head indices.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmsa.so")
+
+MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE_TOO_SMALL = 0, 1, 2, 3
+MSA_ERR_CUDA, MSA_ERR_DEVICE_TIMEOUT, MSA_ERR_INDEX = 4, 5, 6
+ASHAPE, VS, BLOCK = 0, 1, 2
+PATTERNS = {"ashape": ASHAPE, "vs": VS, "block": BLOCK}
+
+EXPORTS = ("msa_status_string", "msa_vs_index_workspace", "msa_block_index_workspace", "msa_layer_workspace",
+           "msa_build_vs_index", "msa_build_block_index", "msa_attn_ashape", "msa_attn_vs", "msa_attn_block",
+           "msa_prefill_layer", "msa_layer_indices", "msa_vs_expand", "msa_poll_device_status")
+
+
+class MsaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("n", ctypes.c_int32),
+                ("d_h", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+class HeadCfg(ctypes.Structure):
+    _fields_ = [("pattern", ctypes.c_int32), ("sink", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("last_q", ctypes.c_int32), ("n_vertical", ctypes.c_int32), ("n_slash", ctypes.c_int32),
+                ("block", ctypes.c_int32), ("topk", ctypes.c_int32)]
+
+
+class VSIndexC(ctypes.Structure):
+    _fields_ = [("vertical", ctypes.c_void_p), ("vertical_cnt", ctypes.c_void_p), ("slash", ctypes.c_void_p),
+                ("slash_cnt", ctypes.c_void_p), ("vertical_bits", ctypes.c_void_p), ("slash_bits", ctypes.c_void_p),
+                ("v_cap", ctypes.c_int32), ("s_cap", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str = LIB_PATH):
+    """Load libmsa.so (raises if it is missing: there is no CPU fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"libmsa.so not built ({path}); run __graft_entry__.build()")
+            lib = ctypes.CDLL(path)
+            P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+            st = ctypes.c_int
+            lib.msa_status_string.restype = ctypes.c_char_p
+            lib.msa_status_string.argtypes = [st]
+            lib.msa_vs_index_workspace.restype = sz
+            lib.msa_vs_index_workspace.argtypes = [P, P, i32]
+            lib.msa_block_index_workspace.restype = sz
+            lib.msa_block_index_workspace.argtypes = [P, i32, i32]
+            lib.msa_layer_workspace.restype = sz
+            lib.msa_layer_workspace.argtypes = [P, P]
+            lib.msa_build_vs_index.restype = st
+            lib.msa_build_vs_index.argtypes = [P, P, P, P, i32, P, P, P, sz, P]
+            lib.msa_build_block_index.restype = st
+            lib.msa_build_block_index.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, sz, P]
+            lib.msa_attn_ashape.restype = st
+            lib.msa_attn_ashape.argtypes = [P, P, P, P, P, i32, i32, i32, P, P, P, P]
+            lib.msa_attn_vs.restype = st
+            lib.msa_attn_vs.argtypes = [P, P, P, P, P, i32, i32, P, P, P, P, P]
+            lib.msa_attn_block.restype = st
+            lib.msa_attn_block.argtypes = [P, P, P, P, P, i32, i32, i32, P, P, P, P, P, P]
+            lib.msa_prefill_layer.restype = st
+            lib.msa_prefill_layer.argtypes = [P, P, P, P, P, P, P, P, P, sz, P]
+            lib.msa_layer_indices.restype = st
+            lib.msa_layer_indices.argtypes = [P, P, P, P, P, P]
+            lib.msa_vs_expand.restype = st
+            lib.msa_vs_expand.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P]
+            lib.msa_poll_device_status.restype = st
+            lib.msa_poll_device_status.argtypes = [P]
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().msa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != MSA_OK:
+        raise MsaError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _heads(heads):
+    arr = (ctypes.c_int32 * len(heads))(*[int(h) for h in heads])
+    return arr, len(heads)
+
+
+def make_shape(q: torch.Tensor, k: torch.Tensor, scale: float | None = None) -> Shape:
+    B, Hq, n, d = q.shape
+    return Shape(B, Hq, k.shape[1], n, d, float(scale) if scale else 0.0)
+
+
+def head_cfg(entry: dict) -> HeadCfg:
+    """A config-table entry from a dict: pattern 'ashape' | 'vs' | 'block' plus its budgets."""
+    pat = entry["pattern"]
+    pat = PATTERNS[pat] if isinstance(pat, str) else int(pat)
+    return HeadCfg(pat, int(entry.get("sink", 0)), int(entry.get("window", 1)), int(entry.get("last_q", 64)),
+                   int(entry.get("n_vertical", 0)), int(entry.get("n_slash", 0)), int(entry.get("block", 64)),
+                   int(entry.get("topk", 1)))
+
+
+def table_array(table):
+    arr = (HeadCfg * len(table))()
+    for h, e in enumerate(table):
+        arr[h] = head_cfg(e)
+    return arr
+
+
+def _out_like(q, o):
+    return torch.empty_like(q) if o is None else o
+
+
+# ----------------------------------------------------------------- attention
+def attn_ashape(q, k, v, heads, sink, window, o=None, lse=None, edges=None, scale=None, stream=None):
+    """A-shape heads (sink g, window w); returns o."""
+    lib = load()
+    o = _out_like(q, o)
+    sh = make_shape(q, k, scale)
+    hp, nh = _heads(heads)
+    _check(lib.msa_attn_ashape(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), hp, nh, int(sink), int(window), _ptr(o),
+                               _ptr(lse), _ptr(edges), _stream(stream)), "msa_attn_ashape")
+    return o
+
+
+class VSIndex:
+    """Device buffers of a Vertical-Slash index (see msa_vs_index in msa.h)."""
+
+    def __init__(self, slots: int, n: int, n_vertical: int, n_slash: int, device):
+        self.v_cap = max(min(int(n_vertical), n), 0)
+        self.s_cap = max(min(int(n_slash), n), 0)
+        words = (n + 31) // 32
+        self.vertical = torch.empty(slots, max(self.v_cap, 1), dtype=torch.int32, device=device)
+        self.vertical_cnt = torch.empty(slots, dtype=torch.int32, device=device)
+        self.slash = torch.empty(slots, max(self.s_cap, 1), dtype=torch.int32, device=device)
+        self.slash_cnt = torch.empty(slots, dtype=torch.int32, device=device)
+        self.vertical_bits = torch.zeros(slots, words, dtype=torch.int32, device=device)
+        self.slash_bits = torch.zeros(slots, words, dtype=torch.int32, device=device)
+
+    def c(self) -> VSIndexC:
+        return VSIndexC(self.vertical.data_ptr(), self.vertical_cnt.data_ptr(), self.slash.data_ptr(),
+                        self.slash_cnt.data_ptr(), self.vertical_bits.data_ptr(), self.slash_bits.data_ptr(),
+                        self.v_cap, self.s_cap)
+
+    @staticmethod
+    def from_c(c: VSIndexC, slots: int, n: int):
+        """Non-owning view of an index that lives in a layer workspace."""
+        ix = VSIndex.__new__(VSIndex)
+        ix.v_cap, ix.s_cap = c.v_cap, c.s_cap
+        words = (n + 31) // 32
+        ix.vertical = _view_i32(c.vertical, slots * max(c.v_cap, 1)).view(slots, max(c.v_cap, 1))
+        ix.vertical_cnt = _view_i32(c.vertical_cnt, slots)
+        ix.slash = _view_i32(c.slash, slots * max(c.s_cap, 1)).view(slots, max(c.s_cap, 1))
+        ix.slash_cnt = _view_i32(c.slash_cnt, slots)
+        ix.vertical_bits = _view_i32(c.vertical_bits, slots * words).view(slots, words)
+        ix.slash_bits = _view_i32(c.slash_bits, slots * words).view(slots, words)
+        return ix
+
+
+_views = {}
+
+
+def _view_i32(ptr: int, count: int) -> torch.Tensor:
+    """A torch int32 view of `count` elements at device address `ptr` (inside a live workspace)."""
+    key = (ptr, count)
+    base = _views.get("ws")
+    if base is None:
+        raise RuntimeError("no workspace registered for index views")
+    off = ptr - base.data_ptr()
+    assert off % 4 == 0 and 0 <= off and off + 4 * count <= base.numel()
+    return base[off:off + 4 * count].view(torch.int32)
+
+
+def attn_vs(q, k, v, heads, index: VSIndex, o=None, lse=None, edges=None, scale=None, stream=None):
+    lib = load()
+    o = _out_like(q, o)
+    sh = make_shape(q, k, scale)
+    hp, nh = _heads(heads)
+    ic = index.c()
+    _check(lib.msa_attn_vs(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), hp, nh, 64, ctypes.byref(ic), _ptr(o),
+                           _ptr(lse), _ptr(edges), _stream(stream)), "msa_attn_vs")
+    return o
+
+
+def attn_block(q, k, v, heads, topk, block_idx, block_cnt, o=None, lse=None, edges=None, scale=None, stream=None):
+    lib = load()
+    o = _out_like(q, o)
+    sh = make_shape(q, k, scale)
+    hp, nh = _heads(heads)
+    _check(lib.msa_attn_block(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), hp, nh, 64, int(topk), _ptr(block_idx),
+                              _ptr(block_cnt), _ptr(o), _ptr(lse), _ptr(edges), _stream(stream)), "msa_attn_block")
+    return o
+
+
+# ----------------------------------------------------------------- indices
+def build_vs_index(q, k, heads, last_q, n_vertical, n_slash, index: VSIndex | None = None, scale=None, stream=None):
+    lib = load()
+    sh = make_shape(q, k, scale)
+    hp, nh = _heads(heads)
+    cfg = HeadCfg(VS, 0, 1, int(last_q), int(n_vertical), int(n_slash), 64, 1)
+    if index is None:
+        index = VSIndex(q.shape[0] * nh, q.shape[2], n_vertical, n_slash, q.device)
+    ws_bytes = lib.msa_vs_index_workspace(ctypes.byref(sh), ctypes.byref(cfg), nh)
+    ws = torch.empty(max(int(ws_bytes), 1), dtype=torch.uint8, device=q.device)
+    ic = index.c()
+    _check(lib.msa_build_vs_index(ctypes.byref(sh), _ptr(q), _ptr(k), hp, nh, ctypes.byref(cfg), ctypes.byref(ic),
+                                  _ptr(ws), int(ws_bytes), _stream(stream)), "msa_build_vs_index")
+    index._ws = ws  # keep the scratch alive until the stream has used it
+    return index
+
+
+def build_block_index(q, k, heads, topk, block_idx=None, block_cnt=None, scale=None, stream=None):
+    lib = load()
+    sh = make_shape(q, k, scale)
+    hp, nh = _heads(heads)
+    B, n = q.shape[0], q.shape[2]
+    nb = (n + 63) // 64
+    if block_idx is None:
+        block_idx = torch.empty(B, nh, nb, int(topk), dtype=torch.int32, device=q.device)
+    if block_cnt is None:
+        block_cnt = torch.empty(B, nh, nb, dtype=torch.int32, device=q.device)
+    ws_bytes = lib.msa_block_index_workspace(ctypes.byref(sh), 64, nh)
+    ws = torch.empty(max(int(ws_bytes), 1), dtype=torch.uint8, device=q.device)
+    _check(lib.msa_build_block_index(ctypes.byref(sh), _ptr(q), _ptr(k), hp, nh, 64, int(topk), _ptr(block_idx),
+                                     _ptr(block_cnt), _ptr(ws), int(ws_bytes), _stream(stream)),
+           "msa_build_block_index")
+    block_idx._ws = ws
+    return block_idx, block_cnt
+
+
+def vs_expand(q_shape, index: VSIndex, slot, u_begin, u_count, range_cap, col_cap, stream=None):
+    """Explicit per-block ranges and columns of one slot (device tensors)."""
+    lib = load()
+    B, Hq, n, d = q_shape
+    sh = Shape(B, Hq, 1, n, d, 0.0)
+    dev = index.vertical.device
+    rc = torch.empty(u_count, dtype=torch.int32, device=dev)
+    rg = torch.empty(u_count, max(range_cap, 1), 2, dtype=torch.int32, device=dev)
+    cc = torch.empty(u_count, dtype=torch.int32, device=dev)
+    cl = torch.empty(u_count, max(col_cap, 1), dtype=torch.int32, device=dev)
+    ic = index.c()
+    _check(lib.msa_vs_expand(ctypes.byref(sh), ctypes.byref(ic), int(slot), int(u_begin), int(u_count), int(range_cap),
+                             int(col_cap), _ptr(rc), _ptr(rg), _ptr(cc), _ptr(cl), _stream(stream)), "msa_vs_expand")
+    return rc, rg, cc, cl
+
+
+# ----------------------------------------------------------------- layer
+class Layer:
+    """One layer's config table plus its workspace; call() runs msa_prefill_layer."""
+
+    def __init__(self, table, B, Hq, Hkv, n, d, device, scale=None):
+        self.table = list(table)
+        assert len(self.table) == Hq
+        self.tarr = table_array(self.table)
+        self.shape = Shape(B, Hq, Hkv, n, d, float(scale) if scale else 0.0)
+        lib = load()
+        self.ws_bytes = int(lib.msa_layer_workspace(ctypes.byref(self.shape), self.tarr))
+        if self.ws_bytes == 0:
+            raise MsaError(MSA_ERR_INVALID_ARG, "msa_layer_workspace")
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, q, k, v, o=None, lse=None, edges=None, stream=None):
+        lib = load()
+        o = _out_like(q, o)
+        _check(lib.msa_prefill_layer(ctypes.byref(self.shape), _ptr(q), _ptr(k), _ptr(v), self.tarr, _ptr(o), _ptr(lse),
+                                     _ptr(edges), _ptr(self.ws), self.ws_bytes, _stream(stream)), "msa_prefill_layer")
+        return o
+
+    def indices(self):
+        """(VSIndex view, block_idx, block_cnt) left in the workspace by the last call."""
+        lib = load()
+        vc = VSIndexC()
+        bi = ctypes.c_void_p()
+        bc = ctypes.c_void_p()
+        _check(lib.msa_layer_indices(ctypes.byref(self.shape), self.tarr, _ptr(self.ws), ctypes.byref(vc),
+                                     ctypes.byref(bi), ctypes.byref(bc)), "msa_layer_indices")
+        _views["ws"] = self.ws
+        B, n = self.shape.B, self.shape.n
+        nvs = sum(1 for e in self.table if head_cfg(e).pattern == VS)
+        nbs = [e for e in self.table if head_cfg(e).pattern == BLOCK]
+        vs = VSIndex.from_c(vc, B * nvs, n) if nvs else None
+        blk = cnt = None
+        if nbs:
+            nb = (n + 63) // 64
+            topk = head_cfg(nbs[0]).topk
+            blk = _view_i32(bi.value, B * len(nbs) * nb * topk).view(B, len(nbs), nb, topk)
+            cnt = _view_i32(bc.value, B * len(nbs) * nb).view(B, len(nbs), nb)
+        return vs, blk, cnt
+
+
+def poll_device_status(stream=None) -> int:
+    """Synchronise the stream and read/clear the device error word (status code)."""
+    return int(load().msa_poll_device_status(_stream(stream)))

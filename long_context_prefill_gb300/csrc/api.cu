@@ -1,0 +1,295 @@
+// Host side of libmsa: argument validation, TMA tensor maps, work-unit
+// construction and the exported C entry points declared in include/msa.h.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "internal.h"
+
+namespace msa {
+
+__device__ int g_device_error = 0;
+
+int* device_error_word() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+  return reinterpret_cast<int*>(p);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool make_bf16_map(CUtensorMap* map, const void* base, int64_t BH, int64_t n, int64_t d, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)(d * 2), (cuuint64_t)(n * d * 2)};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ validation
+msa_status check_shape(const msa_shape* s) {
+  if (!s) return MSA_ERR_INVALID_ARG;
+  if (s->B < 1 || s->Hq < 1 || s->Hkv < 1 || s->n < 1 || s->d_h < 1) return MSA_ERR_INVALID_ARG;
+  if (s->Hq % s->Hkv != 0) return MSA_ERR_INVALID_ARG;
+  if (!(s->scale == s->scale) || isinf(s->scale)) return MSA_ERR_INVALID_ARG;
+  if (s->d_h != 64 && s->d_h != 128) return MSA_ERR_UNSUPPORTED;
+  if (s->n > (1 << 28)) return MSA_ERR_UNSUPPORTED;
+  if ((int64_t)s->B * s->Hq > (1 << 24)) return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+static msa_status check_ptr(const void* p, bool required) {
+  if (!p) return required ? MSA_ERR_INVALID_ARG : MSA_OK;
+  if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return MSA_ERR_INVALID_ARG;
+  return MSA_OK;
+}
+
+static msa_status check_ptr4(const void* p, bool required) {
+  if (!p) return required ? MSA_ERR_INVALID_ARG : MSA_OK;
+  if (reinterpret_cast<uintptr_t>(p) % 4 != 0) return MSA_ERR_INVALID_ARG;
+  return MSA_OK;
+}
+
+msa_status check_heads(const int32_t* heads, int32_t n_heads, int32_t Hq) {
+  if (!heads || n_heads < 1 || n_heads > Hq) return MSA_ERR_INVALID_ARG;
+  std::vector<char> seen((size_t)Hq, 0);
+  for (int32_t x = 0; x < n_heads; ++x) {
+    if (heads[x] < 0 || heads[x] >= Hq || seen[(size_t)heads[x]]) return MSA_ERR_INVALID_ARG;
+    seen[(size_t)heads[x]] = 1;
+  }
+  return MSA_OK;
+}
+
+float effective_scale(const msa_shape& s) { return s.scale > 0.f ? s.scale : 1.0f / sqrtf((float)s.d_h); }
+
+#define MSA_TRY(x)                       \
+  do {                                   \
+    msa_status st__ = (x);               \
+    if (st__ != MSA_OK) return st__;     \
+  } while (0)
+
+static msa_status check_qkv(const msa_shape* s, const void* q, const void* k, const void* v) {
+  MSA_TRY(check_shape(s));
+  MSA_TRY(check_ptr(q, true));
+  MSA_TRY(check_ptr(k, true));
+  if (v) MSA_TRY(check_ptr(v, true));
+  return MSA_OK;
+}
+
+// ------------------------------------------------------------------ units
+void ashape_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t sink, int32_t window,
+                  std::vector<Unit>& out) {
+  const int g = s.Hq / s.Hkv;
+  for (int b = 0; b < s.B; ++b)
+    for (int x = 0; x < nh; ++x) {
+      Unit u;
+      memset(&u, 0, sizeof(u));
+      u.pattern = kUnitAshape;
+      u.kvh = b * s.Hkv + heads[x] / g;
+      u.qh[0] = u.qh[1] = b * s.Hq + heads[x];
+      u.row_off[0] = 0;
+      u.row_off[1] = 64;
+      u.sink = sink;
+      u.window = window;
+      out.push_back(u);
+    }
+}
+
+void vs_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t slot_base_per_batch,
+              int32_t slots_per_batch, std::vector<Unit>& out) {
+  const int g = s.Hq / s.Hkv;
+  for (int b = 0; b < s.B; ++b)
+    for (int x = 0; x < nh; ++x) {
+      Unit u;
+      memset(&u, 0, sizeof(u));
+      u.pattern = kUnitVS;
+      u.kvh = b * s.Hkv + heads[x] / g;
+      u.qh[0] = u.qh[1] = b * s.Hq + heads[x];
+      u.row_off[0] = 0;
+      u.row_off[1] = 64;
+      u.slot[0] = u.slot[1] = b * slots_per_batch + slot_base_per_batch + x;
+      out.push_back(u);
+    }
+}
+
+// Block-Sparse units: two heads of one KV group at the same query block share
+// the K/V blocks they both selected, so such heads are paired (one unit per
+// parity of the query block); a head left alone takes two consecutive blocks.
+void block_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t slots_per_batch,
+                 std::vector<Unit>& out) {
+  const int g = s.Hq / s.Hkv;
+  for (int b = 0; b < s.B; ++b) {
+    for (int kv = 0; kv < s.Hkv; ++kv) {
+      std::vector<int> pos;
+      for (int x = 0; x < nh; ++x)
+        if (heads[x] / g == kv) pos.push_back(x);
+      size_t p = 0;
+      for (; p + 1 < pos.size(); p += 2)
+        for (int par = 0; par < 2; ++par) {
+          Unit u;
+          memset(&u, 0, sizeof(u));
+          u.pattern = kUnitBlock;
+          u.kvh = b * s.Hkv + kv;
+          for (int h = 0; h < 2; ++h) {
+            u.qh[h] = b * s.Hq + heads[pos[p + h]];
+            u.slot[h] = b * slots_per_batch + pos[p + h];
+            u.row_off[h] = 64 * par;
+          }
+          out.push_back(u);
+        }
+      if (p < pos.size()) {
+        Unit u;
+        memset(&u, 0, sizeof(u));
+        u.pattern = kUnitBlock;
+        u.kvh = b * s.Hkv + kv;
+        for (int h = 0; h < 2; ++h) {
+          u.qh[h] = b * s.Hq + heads[pos[p]];
+          u.slot[h] = b * slots_per_batch + pos[p];
+          u.row_off[h] = 64 * h;
+        }
+        out.push_back(u);
+      }
+    }
+  }
+}
+
+msa_status attention(const msa_shape& s, const void* q, const void* k, const void* v, void* o, float* lse,
+                     int64_t* edges, const std::vector<Unit>& units, const AttnArgs& idx, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  if (!make_bf16_map(&tq, q, (int64_t)s.B * s.Hq, s.n, s.d_h, 64) ||
+      !make_bf16_map(&tk, k, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64) ||
+      !make_bf16_map(&tv, v, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64))
+    return MSA_ERR_CUDA;
+  AttnArgs a = idx;
+  a.n = s.n;
+  a.d = s.d_h;
+  a.T = ceil_div(s.n, 128);
+  a.scale_log2 = effective_scale(s) * 1.4426950408889634f;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.edges = reinterpret_cast<unsigned long long*>(edges);
+  a.err = device_error_word();
+  if (!a.err) return MSA_ERR_CUDA;
+  return launch_attention(tq, tk, tv, a, units.data(), (int)units.size(), stream);
+}
+
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+const char* msa_status_string(msa_status s) {
+  switch (s) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID_ARG: return "invalid argument";
+    case MSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MSA_ERR_CUDA: return "CUDA runtime error";
+    case MSA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MSA_ERR_INDEX: return "index entry out of range";
+  }
+  return "unknown status";
+}
+
+msa_status msa_attn_ashape(const msa_shape* shape, const void* q, const void* k, const void* v,
+                           const int32_t* heads, int32_t n_heads, int32_t sink, int32_t window, void* o,
+                           float* lse, int64_t* edges, void* stream) {
+  MSA_TRY(check_qkv(shape, q, k, v));
+  MSA_TRY(check_ptr(o, true));
+  MSA_TRY(check_ptr4(lse, false));
+  MSA_TRY(check_ptr(edges, false));
+  MSA_TRY(check_heads(heads, n_heads, shape->Hq));
+  if (sink < 0 || window < 1) return MSA_ERR_INVALID_ARG;
+  std::vector<Unit> units;
+  ashape_units(*shape, heads, n_heads, sink, window, units);
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  return attention(*shape, q, k, v, o, lse, edges, units, a, (cudaStream_t)stream);
+}
+
+msa_status msa_attn_vs(const msa_shape* shape, const void* q, const void* k, const void* v, const int32_t* heads,
+                       int32_t n_heads, int32_t block, const msa_vs_index* index, void* o, float* lse,
+                       int64_t* edges, void* stream) {
+  MSA_TRY(check_qkv(shape, q, k, v));
+  MSA_TRY(check_ptr(o, true));
+  MSA_TRY(check_ptr4(lse, false));
+  MSA_TRY(check_ptr(edges, false));
+  MSA_TRY(check_heads(heads, n_heads, shape->Hq));
+  if (block != 64) return MSA_ERR_UNSUPPORTED;
+  if (!index) return MSA_ERR_INVALID_ARG;
+  MSA_TRY(check_ptr4(index->vertical_bits, true));
+  MSA_TRY(check_ptr4(index->slash_bits, true));
+  std::vector<Unit> units;
+  vs_units(*shape, heads, n_heads, 0, n_heads, units);
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.vs_dbits = index->slash_bits;
+  a.vs_cbits = index->vertical_bits;
+  a.vs_words = ceil_div(shape->n, 32);
+  return attention(*shape, q, k, v, o, lse, edges, units, a, (cudaStream_t)stream);
+}
+
+msa_status msa_attn_block(const msa_shape* shape, const void* q, const void* k, const void* v,
+                          const int32_t* heads, int32_t n_heads, int32_t block, int32_t topk,
+                          const int32_t* block_idx, const int32_t* block_cnt, void* o, float* lse,
+                          int64_t* edges, void* stream) {
+  MSA_TRY(check_qkv(shape, q, k, v));
+  MSA_TRY(check_ptr(o, true));
+  MSA_TRY(check_ptr4(lse, false));
+  MSA_TRY(check_ptr(edges, false));
+  MSA_TRY(check_heads(heads, n_heads, shape->Hq));
+  if (block != 64) return MSA_ERR_UNSUPPORTED;
+  if (topk < 1) return MSA_ERR_INVALID_ARG;
+  MSA_TRY(check_ptr4(block_idx, true));
+  MSA_TRY(check_ptr4(block_cnt, true));
+  std::vector<Unit> units;
+  block_units(*shape, heads, n_heads, n_heads, units);
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.bs_idx = block_idx;
+  a.bs_cnt = block_cnt;
+  a.bs_topk = topk;
+  a.bs_nb = ceil_div(shape->n, 64);
+  return attention(*shape, q, k, v, o, lse, edges, units, a, (cudaStream_t)stream);
+}
+
+msa_status msa_poll_device_status(void* stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MSA_ERR_CUDA;
+  int* w = device_error_word();
+  if (!w) return MSA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MSA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MSA_ERR_CUDA;
+  }
+  if (v == kErrTimeout) return MSA_ERR_DEVICE_TIMEOUT;
+  if (v == kErrIndex) return MSA_ERR_INDEX;
+  return MSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,757 @@
+// Sparse causal attention engine for sm_103a (A-shape, Vertical-Slash and
+// Block-Sparse heads in one kernel).
+//
+// What it computes (MInference page, eq.(1)-(2) restricted to N_h(i), with
+// the online-softmax merge of eq.(7)-(8)): for every query row i of a work
+// item, o_i = Σ_{j in N(i)} e^{s_ij} v_j / Σ_{j in N(i)} e^{s_ij}.
+//
+// One CTA processes one item: 128 query rows (two 64-row halves) of one KV
+// group against a stream of 128-key tiles that a pattern iterator generates:
+//   warp 4     producer: builds each tile's descriptor (key segments and
+//              per-half validity masks), TMA-loads Q once and K/V per tile
+//              (two 64-row segments per tile, any start row), or gathers
+//              single columns with vector loads (Vertical-Slash columns);
+//   warp 5     MMA issuer (one thread): S = Q K^T into TMEM (double
+//              buffered), then O += P V into a TMEM accumulator;
+//   warps 0-3  softmax: thread r owns query row r (TMEM lane r); masks S
+//              (causal, pattern, sequence end) before the max, keeps the
+//              running max/denominator, writes P (bf16) to shared memory for
+//              the PV MMA, rescales O in TMEM only when the max grows by more
+//              than 2^8, and writes the normalised output.
+// Every (i, j) pair enters the softmax at most once: tiles partition the keys
+// of an item, and masks drop what lies outside N(i) (MInference page §3.2 and
+// §5.1 "boundary masks": set to -inf before the max).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace msa {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kStages = 2;
+constexpr int kDescSlots = 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct TileDesc {
+  int32_t seg[2];   // range tiles: first key of each 64-key segment
+  int32_t kind;     // 0 = range, 1 = gather
+  int32_t rule;     // A-shape row rule: bit0 keeps j < sink, bit1 keeps j > i - window
+  uint32_t mask[2][4];  // per half: bit k = key k of the tile may be attended
+  int32_t gidx[128];    // gather tiles: key of column k (-1 = empty)
+};
+
+enum {
+  kBarQ = 0,
+  kBarKFull = 1,
+  kBarKEmpty = kBarKFull + kStages,
+  kBarVFull = kBarKEmpty + kStages,
+  kBarVEmpty = kBarVFull + kStages,
+  kBarSFull = kBarVEmpty + kStages,
+  kBarSEmpty = kBarSFull + 2,
+  kBarPFull = kBarSEmpty + 2,
+  kBarPEmpty = kBarPFull + 1,
+  kBarDFull = kBarPEmpty + 1,
+  kBarDEmpty = kBarDFull + kDescSlots,
+  kNumBars = kBarDEmpty + kDescSlots
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kTile = 128 * D * 2;  // 128 rows of d_h bf16
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTile;
+  static constexpr int kV = kK + kStages * kTile;
+  static constexpr int kP = kV + kStages * kTile;
+  static constexpr int kDesc = kP + 128 * 128 * 2;
+  static constexpr int kStage = kDesc + kDescSlots * (int)sizeof(TileDesc);  // gather staging (256 ints)
+  static constexpr int kBars = kStage + 256 * 4;
+  static constexpr int kMisc = kBars + kNumBars * 8;
+  static constexpr int kTotal = kMisc + 64;
+  // > 113 KB keeps one CTA per SM, so the 512-column TMEM allocation never waits.
+  static constexpr int kAlloc = (kTotal + 1024) > 120 * 1024 ? (kTotal + 1024) : 120 * 1024;
+};
+
+__device__ __forceinline__ void set_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint64_t low_mask64(int c) {  // bits [0, c), c clamped to [0, 64]
+  c = c < 0 ? 0 : (c > 64 ? 64 : c);
+  return c >= 64 ? ~0ull : ((1ull << c) - 1ull);
+}
+
+// Any bit of `bits` (an n-bit map) set in [lo, hi] ∩ [0, n)?
+__device__ __forceinline__ bool bits_any(const uint32_t* bits, int n, int lo, int hi) {
+  lo = lo < 0 ? 0 : lo;
+  hi = hi > n - 1 ? n - 1 : hi;
+  if (lo > hi) return false;
+  const int w0 = lo >> 5, w1 = hi >> 5;
+  for (int w = w0; w <= w1; ++w) {
+    uint32_t x = __ldg(bits + w);
+    if (w == w0) x &= 0xFFFFFFFFu << (lo & 31);
+    if (w == w1) x &= 0xFFFFFFFFu >> (31 - (hi & 31));
+    if (x) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ int bits_count(const uint32_t* bits, int n, int lo, int hi) {
+  lo = lo < 0 ? 0 : lo;
+  hi = hi > n - 1 ? n - 1 : hi;
+  if (lo > hi) return 0;
+  const int w0 = lo >> 5, w1 = hi >> 5;
+  int c = 0;
+  for (int w = w0; w <= w1; ++w) {
+    uint32_t x = __ldg(bits + w);
+    if (w == w0) x &= 0xFFFFFFFFu << (lo & 31);
+    if (w == w1) x &= 0xFFFFFFFFu >> (31 - (hi & 31));
+    c += __popc(x);
+  }
+  return c;
+}
+
+__device__ __forceinline__ bool bit_at(const uint32_t* bits, int j) { return (__ldg(bits + (j >> 5)) >> (j & 31)) & 1u; }
+
+// ------------------------------------------------------------------ item geometry
+struct Item {
+  int row0[2];   // first query row of each half
+  int exists[2]; // half has at least one row < n
+  int e[2];      // last row of each half's query block (clipped to n-1)
+  int a0;        // 128 * t
+};
+
+__device__ __forceinline__ Item make_item(const Unit& U, int t, int n) {
+  Item it;
+  it.a0 = 128 * t;
+  for (int h = 0; h < 2; ++h) {
+    it.row0[h] = 128 * t + U.row_off[h];
+    it.exists[h] = it.row0[h] < n;
+    int e = it.row0[h] + 63;
+    it.e[h] = e < n - 1 ? e : n - 1;
+  }
+  return it;
+}
+
+// ------------------------------------------------------------------ A-shape tiles
+// MInference page eq.(3): rows i of the item attend j < g or i-w < j <= i.
+// The key ranges [0, g) and [a0-w+1, a0+127] (merged when they touch) are cut
+// into 128-key tiles; a per-tile row rule applies the exact set.
+struct AshapeIter {
+  int nr;
+  int lo[2], hi[2], rule[2], tiles[2];
+  __device__ void init(const Unit& U, const Item& it, int n) {
+    const int hi_key = min(it.a0 + 127, n - 1);
+    const int g = U.sink, w = U.window;
+    const int sw = max(0, it.a0 - w + 1);
+    if (sw <= g) {
+      nr = 1; lo[0] = 0; hi[0] = hi_key; rule[0] = 3;
+    } else {
+      nr = 2;
+      lo[0] = 0; hi[0] = min(g, n) - 1; rule[0] = 1;
+      lo[1] = sw; hi[1] = hi_key; rule[1] = 2;
+    }
+    for (int r = 0; r < 2; ++r) tiles[r] = (r < nr && hi[r] >= lo[r]) ? (hi[r] - lo[r] + 128) / 128 : 0;
+  }
+  __device__ int count() const { return tiles[0] + tiles[1]; }
+  __device__ void emit(int j, int n, TileDesc& d) const {
+    const int r = j < tiles[0] ? 0 : 1;
+    const int t0 = lo[r] + 128 * (r == 0 ? j : j - tiles[0]);
+    d.seg[0] = t0;
+    d.seg[1] = t0 + 64;
+    d.kind = 0;
+    d.rule = rule[r];
+    for (int w = 0; w < 4; ++w) {
+      const int base = t0 + 32 * w;
+      const int c = n - base;  // keys below n
+      const uint32_t m = c >= 32 ? 0xFFFFFFFFu : (c <= 0 ? 0u : ((1u << c) - 1u));
+      d.mask[0][w] = m;
+      d.mask[1][w] = m;
+    }
+  }
+};
+
+// ------------------------------------------------------------------ Block-Sparse tiles
+// MInference page eq.(6): half h (query block u_h) attends the key blocks J_{u_h}.
+// The sorted lists of both halves are merged; every pair of consecutive key
+// blocks of the union forms one 128-key tile, and each half keeps only its own
+// blocks.
+struct BlockIter {
+  const int32_t* J[2];
+  int cnt[2], u[2];
+  int p[2];
+  int total;
+  int last;  // last block emitted (lists must be strictly ascending)
+  __device__ void init(const Unit& U, const Item& it, const AttnArgs& a) {
+    for (int h = 0; h < 2; ++h) {
+      u[h] = it.row0[h] / 64;
+      if (it.exists[h]) {
+        const int64_t off = (int64_t)U.slot[h] * a.bs_nb + u[h];
+        J[h] = a.bs_idx + off * a.bs_topk;
+        int c = __ldg(a.bs_cnt + off);
+        cnt[h] = c < 0 ? 0 : (c > a.bs_topk ? a.bs_topk : c);
+      } else {
+        J[h] = nullptr;
+        cnt[h] = 0;
+      }
+    }
+    // size of the union
+    int x = 0, y = 0, m = 0;
+    while (x < cnt[0] || y < cnt[1]) {
+      const int vx = x < cnt[0] ? __ldg(J[0] + x) : 0x7FFFFFFF;
+      const int vy = y < cnt[1] ? __ldg(J[1] + y) : 0x7FFFFFFF;
+      if (vx <= vy) ++x;
+      if (vy <= vx) ++y;
+      ++m;
+    }
+    total = m;
+    p[0] = p[1] = 0;
+    last = -1;
+  }
+  __device__ int count() const { return (total + 1) / 2; }
+  // Next block of the union with its membership bits; false at the end.
+  __device__ bool next_block(int& v, int& bits) {
+    if (p[0] >= cnt[0] && p[1] >= cnt[1]) return false;
+    const int vx = p[0] < cnt[0] ? __ldg(J[0] + p[0]) : 0x7FFFFFFF;
+    const int vy = p[1] < cnt[1] ? __ldg(J[1] + p[1]) : 0x7FFFFFFF;
+    v = min(vx, vy);
+    bits = 0;
+    if (vx == v) { bits |= 1; ++p[0]; }
+    if (vy == v) { bits |= 2; ++p[1]; }
+    if (v <= last) bits = -1;  // not ascending: flagged and dropped by emit()
+    else last = v;
+    return true;
+  }
+  __device__ void emit(int n, TileDesc& d, int* err) {
+    int v0 = 0, b0 = 0, v1 = 0, b1 = 0;
+    next_block(v0, b0);
+    if (!next_block(v1, b1)) { v1 = v0; b1 = 0; }  // odd tail: reload a valid block, fully masked
+    int vs[2] = {v0, v1}, bs[2] = {b0, b1};
+    for (int s = 0; s < 2; ++s) {
+      if (bs[s] < 0) { bs[s] = 0; set_error(err, kErrIndex); }
+      // a block must be causal for the half that keeps it
+      for (int h = 0; h < 2; ++h)
+        if ((bs[s] >> h & 1) && (vs[s] < 0 || vs[s] > u[h])) { bs[s] &= ~(1 << h); set_error(err, kErrIndex); }
+      if (vs[s] < 0 || 64 * vs[s] >= n) { vs[s] = 0; bs[s] = 0; }
+    }
+    d.kind = 0;
+    d.rule = 0;
+    for (int s = 0; s < 2; ++s) {
+      d.seg[s] = 64 * vs[s];
+      for (int w = 0; w < 2; ++w) {
+        const int base = 64 * vs[s] + 32 * w;
+        const int c = n - base;
+        const uint32_t m = c >= 32 ? 0xFFFFFFFFu : (c <= 0 ? 0u : ((1u << c) - 1u));
+        d.mask[0][2 * s + w] = (bs[s] & 1) ? m : 0u;
+        d.mask[1][2 * s + w] = (bs[s] & 2) ? m : 0u;
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ Vertical-Slash tiles
+// Physical set of row i in query block [a, e] (MInference page §2.1 and §4.1):
+// keys covered by some slash tile [a-δ, e-δ] (δ in D), plus the vertical
+// columns C, restricted to j <= i.  Key j is covered by a slash tile of the
+// block iff D has an offset in [a-j, e-j].  Aligned 128-key windows that some
+// slash tile touches become range tiles whose masks include the verticals in
+// them; verticals in the other windows are gathered into column tiles.
+struct VSIter {
+  const uint32_t* dbits;
+  const uint32_t* cbits;
+  int n, M, hi_key;
+  int a[2], e[2], L[2], ex[2];
+  int m;       // window cursor
+  int staged;  // columns waiting in the staging list
+  __device__ void init(const Unit& U, const Item& it, const AttnArgs& A) {
+    n = A.n;
+    dbits = A.vs_dbits + (int64_t)U.slot[0] * A.vs_words;
+    cbits = A.vs_cbits + (int64_t)U.slot[0] * A.vs_words;
+    hi_key = min(it.a0 + 127, n - 1);
+    M = hi_key / 128 + 1;
+    for (int h = 0; h < 2; ++h) {
+      a[h] = it.row0[h];
+      e[h] = it.e[h];
+      ex[h] = it.exists[h];
+      L[h] = e[h] - a[h] + 1;
+    }
+    m = 0;
+    staged = 0;
+  }
+  __device__ bool window_has_slash(int w) const {
+    const int j0 = 128 * w;
+    for (int h = 0; h < 2; ++h) {
+      if (!ex[h]) continue;
+      const int jhi = min(j0 + 127, e[h]);
+      if (j0 > jhi) continue;
+      if (bits_any(dbits, n, a[h] - jhi, a[h] - j0 + L[h] - 1)) return true;
+    }
+    return false;
+  }
+  // Tile count: windows with slash coverage, plus the columns of the others
+  // packed 128 per tile.  Whole warp; result in every lane.
+  __device__ int count(int lane) const {
+    int P = 0, G = 0;
+    for (int w = lane; w < M; w += 32) {
+      if (window_has_slash(w)) ++P;
+      else G += bits_count(cbits, n, 128 * w, min(128 * w + 127, hi_key));
+    }
+    for (int o = 16; o; o >>= 1) {
+      P += __shfl_xor_sync(0xFFFFFFFFu, P, o);
+      G += __shfl_xor_sync(0xFFFFFFFFu, G, o);
+    }
+    return P + (G + 127) / 128;
+  }
+  __device__ void range_masks(int w, int lane, TileDesc& d) const {
+    const int j0 = 128 * w;
+    for (int h = 0; h < 2; ++h) {
+      for (int q = 0; q < 4; ++q) {
+        const int j = j0 + 32 * q + lane;
+        bool ok = false;
+        if (ex[h] && j <= e[h]) ok = bit_at(cbits, j) || bits_any(dbits, n, a[h] - j, a[h] - j + L[h] - 1);
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, ok);
+        if (lane == 0) d.mask[h][q] = b;
+      }
+    }
+    if (lane == 0) { d.seg[0] = j0; d.seg[1] = j0 + 64; d.kind = 0; d.rule = 0; }
+  }
+  __device__ void gather_tile(int lane, int* stage, TileDesc& d) {
+    const int take = staged < 128 ? staged : 128;
+    for (int k = lane; k < 128; k += 32) d.gidx[k] = k < take ? stage[k] : -1;
+    __syncwarp();
+    for (int h = 0; h < 2; ++h)
+      for (int q = 0; q < 4; ++q) {
+        const int g = d.gidx[32 * q + lane];
+        const bool ok = ex[h] && g >= 0 && g <= e[h];
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, ok);
+        if (lane == 0) d.mask[h][q] = b;
+      }
+    // shift the rest of the staging list down (rest < take, so the ranges do not overlap)
+    const int rest = staged - take;
+    for (int k = lane; k < rest; k += 32) stage[k] = stage[take + k];
+    __syncwarp();
+    staged = rest;
+    if (lane == 0) { d.kind = 1; d.rule = 0; d.seg[0] = 0; d.seg[1] = 0; }
+  }
+  // Produce the next tile into d (whole warp).
+  __device__ void emit(int lane, int* stage, TileDesc& d) {
+    for (;;) {
+      if (staged >= 128 || (m >= M && staged > 0)) { gather_tile(lane, stage, d); return; }
+      if (m >= M) {  // nothing left (cannot happen when the count was honoured): empty tile
+        if (lane == 0) { d.kind = 0; d.rule = 0; d.seg[0] = 0; d.seg[1] = 64; }
+        for (int h = 0; h < 2; ++h)
+          for (int q = 0; q < 4; ++q) if (lane == 0) d.mask[h][q] = 0u;
+        return;
+      }
+      const int w = m++;
+      if (window_has_slash(w)) { range_masks(w, lane, d); return; }
+      // stage this window's columns (ascending)
+      const int j0 = 128 * w;
+      for (int q = 0; q < 4; ++q) {
+        const int j = j0 + 32 * q + lane;
+        const bool ok = j <= hi_key && bit_at(cbits, j);
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, ok);
+        if (ok) stage[staged + __popc(b & ((1u << lane) - 1u))] = j;
+        staged += __popc(b);
+      }
+      __syncwarp();
+    }
+  }
+};
+
+// ------------------------------------------------------------------ kernel
+template <int D, bool kCount>
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const AttnArgs A,
+                       const __grid_constant__ UnitTable UT) {
+  using Ly = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::kBars);
+  TileDesc* descs = reinterpret_cast<TileDesc*>(sm + Ly::kDesc);
+  int* stage = reinterpret_cast<int*>(sm + Ly::kStage);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + Ly::kMisc);  // [0] tmem, [1] tiles, [2] abort
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item_id = blockIdx.x;
+  const int t = A.T - 1 - item_id / A.n_units;
+  const Unit& U = UT.u[item_id % A.n_units];
+  const int n = A.n;
+  const Item it = make_item(U, t, n);
+
+  AshapeIter ai;
+  BlockIter bi;
+  VSIter vi;
+
+  if (warp == 0) {
+    tmem_alloc(const_cast<uint32_t*>(&misc[0]), kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32 * kMmaWarp) {
+    mbar_init(&bars[kBarQ], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars[kBarKFull + s], 1);
+      mbar_init(&bars[kBarKEmpty + s], 1);
+      mbar_init(&bars[kBarVFull + s], 1);
+      mbar_init(&bars[kBarVEmpty + s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[kBarSFull + s], 1);
+      mbar_init(&bars[kBarSEmpty + s], 4);
+    }
+    mbar_init(&bars[kBarPFull], 4);
+    mbar_init(&bars[kBarPEmpty], 1);
+    for (int s = 0; s < kDescSlots; ++s) {
+      mbar_init(&bars[kBarDFull + s], 1);
+      mbar_init(&bars[kBarDEmpty + s], 4);
+    }
+    misc[2] = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp) {
+    int T = 0;
+    if (U.pattern == kUnitAshape) { ai.init(U, it, n); T = ai.count(); }
+    else if (U.pattern == kUnitBlock) { bi.init(U, it, A); T = bi.count(); }
+    else { vi.init(U, it, A); T = vi.count(lane); }
+    if (lane == 0) misc[1] = (uint32_t)T;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const int T = (int)misc[1];
+
+  uint8_t* sQ = sm + Ly::kQ;
+  uint8_t* sK = sm + Ly::kK;
+  uint8_t* sV = sm + Ly::kV;
+  uint8_t* sP = sm + Ly::kP;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    bool ok = true;
+    if (lane == 0 && T > 0) {  // no tile, no copy: nothing may be in flight when the CTA exits
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      mbar_arrive_expect_tx(&bars[kBarQ], Ly::kTile);
+      for (int h = 0; h < 2; ++h)
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sQ + c * 16384 + h * 8192, &tq, &bars[kBarQ], 64 * c, it.row0[h], U.qh[h]);
+    }
+    auto load_kv = [&](int j, bool is_v) -> bool {
+      const int st = j % kStages;
+      const uint32_t ph = ((j / kStages) & 1) ^ 1;
+      uint64_t* empty = &bars[(is_v ? kBarVEmpty : kBarKEmpty) + st];
+      uint64_t* full = &bars[(is_v ? kBarVFull : kBarKFull) + st];
+      if (!mbar_wait(empty, ph)) return false;
+      const TileDesc& d = descs[j % kDescSlots];
+      uint8_t* dst = (is_v ? sV : sK) + st * Ly::kTile;
+      const CUtensorMap* map = is_v ? &tv : &tk;
+      if (d.kind == 0) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, Ly::kTile);
+          for (int s = 0; s < 2; ++s)
+            for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384 + s * 8192, map, full, 64 * c, d.seg[s], U.kvh);
+        }
+      } else {
+        // gather single key rows with 16-byte loads into the swizzled layout
+        constexpr int kChunks16 = D / 8;  // 16-byte chunks per row
+        const uint8_t* gbase = reinterpret_cast<const uint8_t*>(is_v ? A.v : A.k) + (int64_t)U.kvh * n * D * 2;
+        for (int idx = lane; idx < 128 * kChunks16; idx += 32) {
+          const int r = idx / kChunks16, c16 = idx % kChunks16;
+          int key = d.gidx[r];
+          key = key < 0 ? 0 : key;  // empty columns reload key 0 (finite data, masked)
+          const uint4 val = __ldg(reinterpret_cast<const uint4*>(gbase + (int64_t)key * D * 2) + c16);
+          *reinterpret_cast<uint4*>(dst + (c16 >> 3) * 16384 + sw128_offset(r, c16 & 7)) = val;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full);
+      }
+      return true;
+    };
+    auto make_desc = [&](int j) -> bool {
+      const int slot = j % kDescSlots;
+      if (!mbar_wait(&bars[kBarDEmpty + slot], ((j / kDescSlots) & 1) ^ 1)) return false;
+      TileDesc& d = descs[slot];
+      if (U.pattern == kUnitVS) {
+        vi.emit(lane, stage, d);
+      } else if (lane == 0) {
+        if (U.pattern == kUnitAshape) ai.emit(j, n, d);
+        else bi.emit(n, d, A.err);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarDFull + slot]);
+      return true;
+    };
+    if (T > 0) ok = make_desc(0) && load_kv(0, false);
+    for (int j = 0; ok && j < T; ++j) {
+      if (misc[2]) { ok = false; break; }
+      if (j + 1 < T) ok = make_desc(j + 1) && load_kv(j + 1, false);
+      if (ok) ok = load_kv(j, true);
+    }
+    if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && T > 0) {
+      bool ok = mbar_wait(&bars[kBarQ], 0);
+      const uint32_t q0 = smem_u32(sQ), p0 = smem_u32(sP);
+      constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
+      auto pv = [&](int j) -> bool {
+        const int st = j % kStages;
+        if (!mbar_wait(&bars[kBarPFull], j & 1)) return false;
+        if (!mbar_wait(&bars[kBarVFull + st], (j / kStages) & 1)) return false;
+        tc_fence_after();
+        const uint32_t v0 = smem_u32(sV + st * Ly::kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc_sw128(p0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(v0 + kk * 2048, 16384, 1024);
+          mma_bf16_ss(tmem + 256, ad, bd, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars[kBarVEmpty + st]);
+        mma_commit(&bars[kBarPEmpty]);
+        return true;
+      };
+      for (int j = 0; ok && j < T; ++j) {
+        if (misc[2]) { ok = false; break; }
+        const int st = j % kStages, sb = j & 1;
+        ok = mbar_wait(&bars[kBarKFull + st], (j / kStages) & 1) &&
+             mbar_wait(&bars[kBarSEmpty + sb], ((j >> 1) & 1) ^ 1);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t k0 = smem_u32(sK + st * Ly::kTile);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + 128 * sb, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024), id_qk,
+                      kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[kBarSFull + sb]);
+        mma_commit(&bars[kBarKEmpty + st]);
+        if (j > 0) ok = pv(j - 1);
+      }
+      if (ok) ok = pv(T - 1);
+      if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int r = threadIdx.x;  // 0..127 = TMEM lane = tile row
+    const int h = r >> 6;
+    const int i = it.row0[h] + (r & 63);
+    const bool row_ok = i < n;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float c2 = A.scale_log2;
+    const int g = U.sink, wnd = U.window;
+    float m_used = -INFINITY, l = 0.f;
+    unsigned long long count = 0;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      if (misc[2]) { ok = false; break; }
+      // ---- tile descriptor -> validity words for this row
+      const int slot = j % kDescSlots;
+      if (!mbar_wait(&bars[kBarDFull + slot], (j / kDescSlots) & 1)) { ok = false; break; }
+      const TileDesc& d = descs[slot];
+      uint64_t vw0, vw1;
+      if (!row_ok) {
+        vw0 = vw1 = 0ull;
+      } else if (d.kind == 0) {
+        uint64_t v[2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const int base = d.seg[s];
+          uint64_t m64 = ((uint64_t)d.mask[h][2 * s + 1] << 32) | d.mask[h][2 * s];
+          m64 &= low_mask64(i - base + 1);  // causal: j <= i
+          if (d.rule) {
+            uint64_t keep = 0;
+            if (d.rule & 1) keep |= low_mask64(g - base);             // j < g
+            if (d.rule & 2) keep |= ~low_mask64(i - wnd + 1 - base);  // j > i - w
+            m64 &= keep;
+          }
+          v[s] = m64;
+        }
+        vw0 = v[0];
+        vw1 = v[1];
+      } else {
+        uint64_t v[2] = {0ull, 0ull};
+        for (int k = 0; k < 128; ++k) {
+          const int gj = d.gidx[k];
+          const bool bit = ((d.mask[h][k >> 5] >> (k & 31)) & 1u) && gj >= 0 && gj <= i;
+          v[k >> 6] |= (uint64_t)bit << (k & 63);
+        }
+        vw0 = v[0];
+        vw1 = v[1];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarDEmpty + slot]);
+      if (kCount) count += __popcll(vw0) + __popcll(vw1);
+
+      // ---- S tile from TMEM
+      const int sb = j & 1;
+      if (!mbar_wait(&bars[kBarSFull + sb], (j >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      float sv[128];
+      {
+        uint32_t* u = reinterpret_cast<uint32_t*>(sv);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + 128 * sb + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(u + 32 * c));
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarSEmpty + sb]);
+
+      // ---- mask, max
+      if (~vw0 | ~vw1) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) sv[k] = ((vw0 >> k) & 1ull) ? sv[k] : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 64; ++k) sv[64 + k] = ((vw1 >> k) & 1ull) ? sv[64 + k] : -INFINITY;
+      }
+      float mt = sv[0];
+#pragma unroll
+      for (int k = 1; k < 128; ++k) mt = fmaxf(mt, sv[k]);
+      const float m_new = fmaxf(m_used, mt * c2);
+      const bool need = m_new > m_used + kRescaleThreshold;
+      const bool any = __any_sync(0xFFFFFFFFu, need);
+      float alpha = 1.f;
+      if (any && m_new != -INFINITY) {
+        alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_new);
+        m_used = m_new;
+      }
+      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+      float rs = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        const float p0 = ex2(fmaf(sv[2 * k], c2, -mref));
+        const float p1 = ex2(fmaf(sv[2 * k + 1], c2, -mref));
+        rs += p0 + p1;
+        pk[k] = pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + rs;
+
+      // ---- PV(j-1) must be done before P is overwritten or O is rescaled
+      if (j > 0 && !mbar_wait(&bars[kBarPEmpty], (j - 1) & 1)) { ok = false; break; }
+      if (any && j > 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_base + 256 + 32 * c, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+          tmem_st32(tmem + lane_base + 256 + 32 * c, o);
+        }
+        tmem_st_wait();
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const int k = 32 * c + 4 * cc;
+          const uint32_t addr = smem_u32(sP + c * 16384 + sw128_offset(r, cc));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[k]), "r"(pk[k + 1]),
+                       "r"(pk[k + 2]), "r"(pk[k + 3])
+                       : "memory");
+        }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarPFull]);
+    }
+    if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
+
+    // ---- epilogue: O / l, LSE
+    const int qh = U.qh[h];
+    if (ok && T > 0) {
+      if (!mbar_wait(&bars[kBarPEmpty], (T - 1) & 1)) { ok = false; misc[2] = 1; set_error(A.err, kErrTimeout); }
+      tc_fence_after();
+    }
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(A.o) + ((int64_t)qh * n + i) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      if (ok && T > 0) {
+        tmem_ld32(tmem + lane_base + 256 + 32 * c, o);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) o[x] = 0u;
+      }
+      if (row_ok) {
+        uint32_t pkd[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          pkd[x] = pack_bf16x2(__uint_as_float(o[2 * x]) * inv_l, __uint_as_float(o[2 * x + 1]) * inv_l);
+        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) dst[x] = make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
+      }
+    }
+    if (row_ok && A.lse) A.lse[(int64_t)qh * n + i] = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    if (kCount && A.edges) {
+      unsigned long long c = count;
+      for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+      if (lane == 0 && c) atomicAdd(A.edges + qh, c);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, bool kCount>
+msa_status launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
+                       const UnitTable& ut, cudaStream_t stream) {
+  auto kern = sparse_attn_kernel<D, kCount>;
+  const int smem = Layout<D>::kAlloc;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  const int64_t items = (int64_t)a.T * a.n_units;
+  if (items <= 0) return MSA_OK;
+  if (items > 0x7FFFFFFF) return MSA_ERR_UNSUPPORTED;
+  kern<<<(unsigned)items, kThreads, smem, stream>>>(tq, tk, tv, a, ut);
+  return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+}  // namespace
+
+msa_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const AttnArgs& args, const Unit* units, int n_units, cudaStream_t stream) {
+  for (int base = 0; base < n_units; base += kMaxUnits) {
+    UnitTable ut;
+    const int cnt = n_units - base < kMaxUnits ? n_units - base : kMaxUnits;
+    for (int x = 0; x < cnt; ++x) ut.u[x] = units[base + x];
+    AttnArgs a = args;
+    a.n_units = cnt;
+    msa_status st;
+    const bool count = args.edges != nullptr;
+    if (args.d == 128) st = count ? launch_impl<128, true>(tq, tk, tv, a, ut, stream) : launch_impl<128, false>(tq, tk, tv, a, ut, stream);
+    else st = count ? launch_impl<64, true>(tq, tk, tv, a, ut, stream) : launch_impl<64, false>(tq, tk, tv, a, ut, stream);
+    if (st != MSA_OK) return st;
+  }
+  return MSA_OK;
+}
+
+}  // namespace msa

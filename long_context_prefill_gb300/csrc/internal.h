@@ -1,0 +1,81 @@
+// Declarations shared by the library's translation units (host and device).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/msa.h"
+
+namespace msa {
+
+// ------------------------------------------------------------ device error word
+// Set (first error wins) by kernels whose bounded wait timed out or that saw an
+// out-of-range index; read and cleared by msa_poll_device_status().
+enum DeviceError : int { kErrNone = 0, kErrTimeout = 1, kErrIndex = 2 };
+int* device_error_word();  // device address of the current device's error word
+
+// ------------------------------------------------------------ attention work units
+// A work unit is a stream of 128-row query tiles ("items"), one per t in
+// [0, T).  Each item has two 64-row halves; half h covers rows
+// 128*t + row_off[h] .. +63 of query head qh[h] (batch folded into the head
+// index).  Both halves read the same KV head.
+enum UnitPattern : int32_t { kUnitAshape = 0, kUnitVS = 1, kUnitBlock = 2 };
+
+struct Unit {
+  int32_t pattern;
+  int32_t kvh;        // b * Hkv + kv head
+  int32_t qh[2];      // b * Hq + query head, per half
+  int32_t row_off[2]; // 0 or 64
+  int32_t slot[2];    // index slot per half (VS / BS)
+  int32_t sink, window;
+  int32_t pad[2];
+};
+static_assert(sizeof(Unit) == 48, "Unit layout");
+
+constexpr int kMaxUnits = 128;
+struct UnitTable {
+  Unit u[kMaxUnits];
+};
+
+struct AttnArgs {
+  int32_t n, d, T, n_units;
+  float scale_log2;  // scale * log2(e)
+  const void* k;     // bf16 [B*Hkv, n, d] (column gathers)
+  const void* v;
+  void* o;           // bf16 [B*Hq, n, d]
+  float* lse;        // [B*Hq, n] or null
+  unsigned long long* edges;  // [B*Hq] or null
+  // Vertical-Slash index (slot-indexed)
+  const uint32_t* vs_dbits;  // [slots, words] bit δ of D
+  const uint32_t* vs_cbits;  // [slots, words] bit j of C
+  int32_t vs_words;
+  // Block-Sparse index
+  const int32_t* bs_idx;  // [slots, N_b, topk]
+  const int32_t* bs_cnt;  // [slots, N_b]
+  int32_t bs_topk, bs_nb;
+  int* err;
+};
+
+// Launch the attention engine over n_units units of T items each.
+msa_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const AttnArgs& args, const Unit* units, int n_units, cudaStream_t stream);
+
+// ------------------------------------------------------------ TMA tensor maps
+// 3-D bf16 map over [BH, n, d] with a box of 64 columns x box_rows rows and
+// 128-byte swizzle.  Returns false if the driver rejects it.
+bool make_bf16_map(CUtensorMap* map, const void* base, int64_t BH, int64_t n, int64_t d, int box_rows);
+
+// ------------------------------------------------------------ index builders
+msa_status run_vs_index(const msa_shape& s, const void* q, const void* k, const int32_t* heads, int32_t n_heads,
+                        const msa_head_cfg& cfg, const msa_vs_index& out, void* ws, size_t ws_bytes,
+                        cudaStream_t stream);
+size_t vs_index_ws_bytes(const msa_shape& s, const msa_head_cfg& cfg, int32_t n_heads);
+
+msa_status run_block_index(const msa_shape& s, const void* q, const void* k, const int32_t* heads,
+                           int32_t n_heads, int32_t topk, int32_t* block_idx, int32_t* block_cnt, void* ws,
+                           size_t ws_bytes, cudaStream_t stream);
+size_t block_index_ws_bytes(const msa_shape& s, int32_t n_heads);
+
+inline int32_t ceil_div(int64_t a, int64_t b) { return (int32_t)((a + b - 1) / b); }
+
+}  // namespace msa

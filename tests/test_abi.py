@@ -1,0 +1,119 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol msa.h
+declares, and rejects bad arguments on the host before any launch (these
+calls return before touching the GPU, so they run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import long_context_prefill_gb300 as msa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from long_context_prefill_gb300 import build
+    build.build()
+    return msa.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "msa.h")).read()
+    return sorted(set(re.findall(r"MSA_API\s+[\w\s\*]+?\b(msa_\w+)\s*\(", src)))
+
+
+def test_header_declares_every_binding_export():
+    assert declared_functions() == sorted(msa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert msa.status_string(code)
+    assert msa.status_string(0) == "ok"
+
+
+def _shape(**kw):
+    base = dict(B=1, Hq=4, Hkv=2, n=256, d_h=128, scale=0.0)
+    base.update(kw)
+    return msa.Shape(**base)
+
+
+FAKE = ctypes.c_void_p(0x10000)  # 16-byte aligned, never dereferenced: validation fails first or no launch
+
+
+def _heads(hs):
+    return (ctypes.c_int32 * len(hs))(*hs), len(hs)
+
+
+@pytest.mark.parametrize("shape_kw,code", [
+    (dict(Hq=3, Hkv=2), msa.MSA_ERR_INVALID_ARG),   # Hq % Hkv != 0
+    (dict(n=0), msa.MSA_ERR_INVALID_ARG),
+    (dict(d_h=96), msa.MSA_ERR_UNSUPPORTED),
+    (dict(B=0), msa.MSA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), msa.MSA_ERR_INVALID_ARG),
+])
+def test_bad_shapes_rejected(lib, shape_kw, code):
+    sh = _shape(**shape_kw)
+    hp, nh = _heads([0])
+    st = lib.msa_attn_ashape(ctypes.byref(sh), FAKE, FAKE, FAKE, hp, nh, 4, 16, FAKE, None, None, None)
+    assert st == code
+
+
+def test_bad_heads_and_budgets_rejected(lib):
+    sh = _shape()
+    for hs in ([4], [-1], [0, 0], []):
+        hp, nh = _heads(hs) if hs else (None, 0)
+        assert lib.msa_attn_ashape(ctypes.byref(sh), FAKE, FAKE, FAKE, hp, nh, 4, 16, FAKE, None, None,
+                                   None) == msa.MSA_ERR_INVALID_ARG
+    hp, nh = _heads([1])
+    assert lib.msa_attn_ashape(ctypes.byref(sh), FAKE, FAKE, FAKE, hp, nh, -1, 16, FAKE, None, None,
+                               None) == msa.MSA_ERR_INVALID_ARG
+    assert lib.msa_attn_ashape(ctypes.byref(sh), FAKE, FAKE, FAKE, hp, nh, 4, 0, FAKE, None, None,
+                               None) == msa.MSA_ERR_INVALID_ARG
+    # misaligned tensor
+    assert lib.msa_attn_ashape(ctypes.byref(sh), ctypes.c_void_p(0x10008), FAKE, FAKE, hp, nh, 4, 16, FAKE, None,
+                               None, None) == msa.MSA_ERR_INVALID_ARG
+    assert lib.msa_attn_block(ctypes.byref(sh), FAKE, FAKE, FAKE, hp, nh, 64, 0, FAKE, FAKE, FAKE, None, None,
+                              None) == msa.MSA_ERR_INVALID_ARG
+    assert lib.msa_attn_block(ctypes.byref(sh), FAKE, FAKE, FAKE, hp, nh, 32, 4, FAKE, FAKE, FAKE, None, None,
+                              None) == msa.MSA_ERR_UNSUPPORTED
+    cfg = msa.HeadCfg(msa.VS, 0, 1, 0, 10, 10, 64, 1)  # last_q = 0
+    ix = msa.VSIndexC()
+    assert lib.msa_build_vs_index(ctypes.byref(sh), FAKE, FAKE, hp, nh, ctypes.byref(cfg), ctypes.byref(ix), FAKE,
+                                  1 << 20, None) == msa.MSA_ERR_INVALID_ARG
+
+
+def test_layer_workspace_and_table_validation(lib):
+    sh = _shape()
+    table = msa.table_array([dict(pattern="ashape", sink=4, window=64), dict(pattern="vs", last_q=64, n_vertical=10,
+                                                                              n_slash=20),
+                             dict(pattern="block", topk=3), dict(pattern="vs", last_q=64, n_vertical=10, n_slash=20)])
+    ws = lib.msa_layer_workspace(ctypes.byref(sh), table)
+    assert ws > 0
+    bad = msa.table_array([dict(pattern="ashape", sink=4, window=0)] * 4)
+    assert lib.msa_layer_workspace(ctypes.byref(sh), bad) == 0
+    mixed_vs = msa.table_array([dict(pattern="vs", last_q=64, n_vertical=10, n_slash=20),
+                                dict(pattern="vs", last_q=64, n_vertical=11, n_slash=20)] * 2)
+    assert lib.msa_layer_workspace(ctypes.byref(sh), mixed_vs) == 0
+    # workspace too small is reported before anything runs
+    st = lib.msa_prefill_layer(ctypes.byref(sh), FAKE, FAKE, FAKE, table, FAKE, None, None, FAKE, 16, None)
+    assert st == msa.MSA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    import importlib
+    mod = importlib.import_module("long_context_prefill_gb300")
+    saved = mod._lib
+    try:
+        mod._lib = None
+        with pytest.raises(RuntimeError):
+            mod.load(str(tmp_path / "nope.so"))
+    finally:
+        mod._lib = saved

@@ -1,0 +1,139 @@
+"""GPU parity of the three sparse attention kernels with a fixed index (the
+MInference page's first test layer, §5.2: fixed index, kernel vs plain masked
+attention).  The oracle evaluates eq.(2) over each row's set in fp64; the
+kernels run through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import compare_rows, f32, head_qkv, pack_bits, scale_of
+
+pytestmark = pytest.mark.gpu
+
+
+def _ashape_case(msa, B, Hq, Hkv, n, d, heads, sink, window, seed, rows=None):
+    q, k, v = synth.random_qkv(B, Hq, Hkv, n, d, seed, device="cuda")
+    o = torch.zeros_like(q)
+    lse = torch.full((B, Hq, n), 7.0, device="cuda")
+    edges = torch.zeros(B * Hq, dtype=torch.int64, device="cuda")
+    msa.attn_ashape(q, k, v, heads, sink, window, o=o, lse=lse, edges=edges)
+    assert msa.poll_device_status() == 0
+    rows = np.arange(n) if rows is None else rows
+    cfg = dict(pattern=oracle.ASHAPE, sink=sink, window=window)
+    for b in range(B):
+        for h in heads:
+            qn, kn, vn = head_qkv(q, k, v, b, h, Hq, Hkv)
+            ro, rl, _ = oracle.head_rows(cfg, qn, kn, vn, rows, scale_of(d))
+            compare_rows(f32(o[b, h])[rows], f32(lse[b, h])[rows], ro, rl, f"ashape b{b} h{h}")
+            assert int(edges[b * Hq + h]) == oracle.head_edges(cfg, n)
+    untouched = [h for h in range(Hq) if h not in heads]
+    for h in untouched:
+        assert torch.all(o[:, h] == 0) and torch.all(lse[:, h] == 7.0)
+
+
+def test_ashape_tiny_head(cuda_lib):
+    """The tiny workload's A-shape head (sink 64, window 512, d=64), all rows."""
+    w = synth.make_workload("tiny", device="cuda")
+    q, k, v = w["q"], w["k"], w["v"]
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 2, 2048, device="cuda")
+    cuda_lib.attn_ashape(q, k, v, [0], 64, 512, o=o, lse=lse)
+    assert cuda_lib.poll_device_status() == 0
+    qn, kn, vn = head_qkv(q, k, v, 0, 0, 2, 1)
+    ro, rl, _ = oracle.head_rows(dict(pattern=oracle.ASHAPE, sink=64, window=512), qn, kn, vn, np.arange(2048), 0.125)
+    compare_rows(f32(o[0, 0]), f32(lse[0, 0]), ro, rl, "tiny ashape")
+
+
+@pytest.mark.parametrize("n,d,sink,window", [
+    (1000, 128, 128, 300),   # ragged tail, window not a tile multiple
+    (777, 64, 0, 1),         # no sink, diagonal only
+    (300, 128, 5, 1000),     # budgets cover every key: dense causal
+    (1024, 128, 200, 129),   # sink wider than a tile
+    (65, 128, 3, 17),        # a single partial tile
+])
+def test_ashape_shapes(cuda_lib, n, d, sink, window):
+    _ashape_case(cuda_lib, 1, 4, 2, n, d, [0, 3], sink, window, seed=n + d)
+
+
+def test_ashape_batch_gqa(cuda_lib):
+    _ashape_case(cuda_lib, 2, 4, 1, 513, 128, [1, 2], 64, 256, seed=7)
+
+
+def _bs_index_host(q, k, b, heads, Hq, Hkv, topk):
+    J, C = [], []
+    for h in heads:
+        qn, kn, _ = head_qkv(q, k, k, b, h, Hq, Hkv)
+        Jh, ch = oracle.bs_index(qn, kn, 64, topk)
+        J.append(Jh)
+        C.append(ch)
+    return np.stack(J), np.stack(C)
+
+
+@pytest.mark.parametrize("heads,Hkv", [([0, 1], 1), ([2], 2), ([0, 1, 3], 2)])
+def test_block_with_oracle_index(cuda_lib, heads, Hkv):
+    """Block-Sparse attention on the oracle's J (paired heads and single heads)."""
+    B, Hq, n, d, topk = 1, 4, 1000, 128, 4
+    q, k, v = synth.random_qkv(B, Hq, Hkv, n, d, seed=11 + len(heads), device="cuda")
+    J, C = _bs_index_host(q, k, 0, heads, Hq, Hkv, topk)
+    bidx = torch.from_numpy(J[None]).cuda()
+    bcnt = torch.from_numpy(C[None]).cuda()
+    o = torch.zeros_like(q)
+    lse = torch.empty(B, Hq, n, device="cuda")
+    edges = torch.zeros(B * Hq, dtype=torch.int64, device="cuda")
+    cuda_lib.attn_block(q, k, v, heads, topk, bidx, bcnt, o=o, lse=lse, edges=edges)
+    assert cuda_lib.poll_device_status() == 0
+    for x, h in enumerate(heads):
+        qn, kn, vn = head_qkv(q, k, v, 0, h, Hq, Hkv)
+        cfg = dict(pattern=oracle.BLOCK, block=64, topk=topk)
+        ro, rl, _ = oracle.head_rows(cfg, qn, kn, vn, np.arange(n), scale_of(d), J=J[x], cnt=C[x])
+        compare_rows(f32(o[0, h]), f32(lse[0, h]), ro, rl, f"block h{h}")
+        assert int(edges[h]) == oracle.head_edges(cfg, n, J=J[x], cnt=C[x])
+
+
+def _vs_case(msa, n, d, C, D, seed, Hq=2, Hkv=1):
+    q, k, v = synth.random_qkv(1, Hq, Hkv, n, d, seed, device="cuda")
+    index = msa.VSIndex(Hq, n, max(len(C), 1), max(len(D), 1), "cuda")
+    for h in range(Hq):
+        index.vertical_bits[h] = torch.from_numpy(pack_bits(C[h], n)).cuda()
+        index.slash_bits[h] = torch.from_numpy(pack_bits(D[h], n)).cuda()
+    o = torch.zeros_like(q)
+    lse = torch.empty(1, Hq, n, device="cuda")
+    edges = torch.zeros(Hq, dtype=torch.int64, device="cuda")
+    msa.attn_vs(q, k, v, list(range(Hq)), index, o=o, lse=lse, edges=edges)
+    assert msa.poll_device_status() == 0
+    for h in range(Hq):
+        qn, kn, vn = head_qkv(q, k, v, 0, h, Hq, Hkv)
+        cfg = dict(pattern=oracle.VS, block=64)
+        ro, rl, _ = oracle.head_rows(cfg, qn, kn, vn, np.arange(n), scale_of(d), C=C[h], D=D[h])
+        compare_rows(f32(o[0, h]), f32(lse[0, h]), ro, rl, f"vs h{h}")
+        assert int(edges[h]) == oracle.head_edges(cfg, n, C=C[h], D=D[h])
+
+
+def test_vs_with_given_index(cuda_lib):
+    rng = np.random.default_rng(3)
+    n = 1500
+    C = [np.sort(rng.choice(n, 40, replace=False)), np.array([0, 5, 700, 1499])]
+    D = [np.sort(rng.choice(n, 30, replace=False))[::-1], np.array([0, 37, 300])]
+    _vs_case(cuda_lib, n, 128, C, D, seed=5)
+
+
+def test_vs_sparse_slashes_gather_columns(cuda_lib):
+    """Few far slashes leave most 128-key windows without slash coverage, so
+    the verticals there go through the column-gather tiles."""
+    rng = np.random.default_rng(9)
+    n = 4000
+    C = [np.sort(rng.choice(n, 300, replace=False)), np.sort(rng.choice(n, 7, replace=False))]
+    D = [np.array([3000, 1000, 0]), np.array([2500])]
+    _vs_case(cuda_lib, n, 64, C, D, seed=6)
+
+
+def test_vs_empty_sets(cuda_lib):
+    """No verticals and no slashes: every row's set is empty (o = 0, lse = -inf)."""
+    _vs_case(cuda_lib, 300, 128, [np.array([], np.int64)] * 2, [np.array([], np.int64)] * 2, seed=8)
+
+
+def test_vs_dense_when_all_offsets(cuda_lib):
+    n = 700
+    _vs_case(cuda_lib, n, 128, [np.array([], np.int64)] * 2, [np.arange(n)[::-1]] * 2, seed=10)
