@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Sparse-prefill benchmark (one GPU per rank; replicas when run under torchrun).
+
+One step = one msa_prefill_layer call on each layer of the workload: the
+mixed-pattern layer at n = 32768 and the two n = 131072 layers
+(Vertical-Slash only, Block-Sparse only), seeded synthetic inputs resident in
+HBM.  Each layer call is split into its two halves (index build, attention) so
+the CUDA events give T_index and T_sparse separately.
+
+Metric: effective TFLOP/s = Σ_h 4 E_h d_h / t over the whole step (E_h =
+attended causal edges, counted by the kernel in an untimed pass), plus
+ms/layer and index-build GB/s.  The JSON line also carries the attention
+kernel's roofline, an end-to-end figure through host buffers, the clocks seen
+during the timed region and the fp64 oracle timed on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+WORKLOADS = ("mixed", "vs128k", "bs128k")
+METRIC = "sparse-prefill effective TFLOP/s (4·E·d_h) & ms/layer at 128K; index-build GB/s"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return FALLBACK_PEAKS, "fallback"
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200"], stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v for v in vis.split(",") if v.strip() != ""]
+    if ids and local_rank < len(ids) and ids[local_rank].strip().isdigit():
+        return int(ids[local_rank])
+    return local_rank
+
+
+# ----------------------------------------------------------------- workload
+def algorithmic_index_bytes(w) -> int:
+    """Bytes the online indices must move at least (read Q/K once, write and
+    read the score vectors and pooled means once, write the indices)."""
+    sh, table = w["shape"], w["table"]
+    B, Hq, Hkv, n, d = sh["B"], sh["Hq"], sh["Hkv"], sh["n"], sh["d"]
+    g = Hq // Hkv
+    vs = [h for h, e in enumerate(table) if e["pattern"] == "vs"]
+    bs = [h for h, e in enumerate(table) if e["pattern"] == "block"]
+    total = 0
+    if vs:
+        e = table[vs[0]]
+        kv = {h // g for h in vs}
+        total += B * len(kv) * n * d * 2                    # K of the groups, once
+        total += B * len(vs) * min(e["last_q"], n) * d * 2  # proxy query rows
+        total += 4 * B * len(vs) * n * 4                    # c and r written and read
+        total += B * len(vs) * (4 * (e["n_vertical"] + e["n_slash"]) + 2 * 4 * ((n + 31) // 32))
+    if bs:
+        nb = (n + 63) // 64
+        kv = {h // g for h in bs}
+        topk = table[bs[0]]["topk"]
+        total += B * (len(bs) + len(kv)) * n * d * 2        # Q of the heads, K of the groups
+        total += 2 * B * (len(bs) + len(kv)) * nb * d * 4   # pooled means written and read
+        total += B * len(bs) * nb * (topk + 1) * 4          # J and counts
+    return total
+
+
+class LayerRun:
+    def __init__(self, name, device, msa, synth):
+        self.name = name
+        self.w = synth.make_workload(name, device=device)
+        sh = self.w["shape"]
+        self.sh = sh
+        self.layer = msa.Layer(self.w["table"], sh["B"], sh["Hq"], sh["Hkv"], sh["n"], sh["d"], device)
+        self.o = torch.empty_like(self.w["q"])
+        self.lse = torch.empty(sh["B"], sh["Hq"], sh["n"], device=device)
+        edges = torch.zeros(sh["B"] * sh["Hq"], dtype=torch.int64, device=device)
+        self.layer(self.w["q"], self.w["k"], self.w["v"], o=self.o, lse=self.lse, edges=edges)
+        torch.cuda.synchronize()
+        self.edges = edges.cpu().numpy()
+        self.flops = float(4.0 * self.edges.sum() * sh["d"])
+        self.index_bytes = algorithmic_index_bytes(self.w)
+        self.bytes_in = sum(t.numel() * t.element_size() for t in (self.w["q"], self.w["k"], self.w["v"]))
+        self.bytes_out = self.o.numel() * self.o.element_size()
+
+    def index(self):
+        self.layer.index(self.w["q"], self.w["k"])
+
+    def attend(self):
+        self.layer.attend(self.w["q"], self.w["k"], self.w["v"], self.o, lse=self.lse)
+
+
+# ----------------------------------------------------------------- oracle (CPU) sample
+def oracle_sample(runs, rows_per_head=16, seed=5):
+    """Time the fp64 oracle on a bounded sample of the workload: for every layer,
+    one head of each pattern it uses (its full online index at full length,
+    then rows_per_head sampled query rows).  Returns (TFLOP/s, seconds,
+    sampled FLOPs, description)."""
+    import oracle
+    import synth
+    flops, secs = 0.0, 0.0
+    for r in runs:
+        w, sh = r.w, r.sh
+        q, k, v = w["q"], w["k"], w["v"]
+        g = sh["Hq"] // sh["Hkv"]
+        seen = set()
+        for h, e in enumerate(w["table"]):
+            if e["pattern"] in seen:
+                continue
+            seen.add(e["pattern"])
+            qn = q[0, h].float().cpu().numpy()
+            kn = k[0, h // g].float().cpu().numpy()
+            vn = v[0, h // g].float().cpu().numpy()
+            rows = synth.sample_rows(sh["n"], rows_per_head, seed + h)
+            t0 = time.perf_counter()
+            idx = {}
+            if e["pattern"] == "vs":
+                C, D, _, _ = oracle.vs_index(qn, kn, e["last_q"], e["n_vertical"], e["n_slash"], sh["scale"])
+                idx = dict(C=C, D=D)
+                cfg = dict(pattern=oracle.VS, block=64)
+            elif e["pattern"] == "block":
+                J, cnt = oracle.bs_index(qn, kn, 64, e["topk"])
+                idx = dict(J=J, cnt=cnt)
+                cfg = dict(pattern=oracle.BLOCK, block=64, topk=e["topk"])
+            else:
+                cfg = dict(pattern=oracle.ASHAPE, sink=e["sink"], window=e["window"])
+            _, _, size = oracle.head_rows(cfg, qn, kn, vn, rows, sh["scale"], **idx)
+            secs += time.perf_counter() - t0
+            flops += 4.0 * float(size.sum()) * sh["d"]
+    desc = (f"per layer ({', '.join(r.name for r in runs)}): one head of each pattern, its full online index "
+            f"at full length plus {rows_per_head}+ seeded sampled query rows (fp64, {oracle.num_threads()} threads)")
+    return flops / secs / 1e12, secs, flops, desc
+
+
+# ----------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workloads", default=",".join(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    names = [x for x in args.workloads.split(",") if x]
+
+    if args.impl == "reference":
+        return reference_arm(args, world, rank, local, names)
+
+    import long_context_prefill_gb300 as msa
+    import synth
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    msa.load()
+    runs = [LayerRun(nm, device, msa, synth) for nm in names]
+    assert msa.poll_device_status() == 0
+    step_flops = sum(r.flops for r in runs)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        for x, r in enumerate(runs):
+            if evs is not None:
+                evs[x][0].record(stream)
+            r.index()
+            if evs is not None:
+                evs[x][1].record(stream)
+            r.attend()
+            if evs is not None:
+                evs[x][2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert msa.poll_device_status() == 0
+
+    K = args.steps
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in runs] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0 = msa.kernel_launches()
+    with ClockSampler(gpu_index(local)) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for s in range(K):
+            step(events[s])
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    launches = msa.kernel_launches() - l0
+    assert msa.poll_device_status() == 0
+    ms_total = max_over_ranks(start.elapsed_time(end), world, device)
+    ms_step = ms_total / K
+    value = world * step_flops * K / (ms_total * 1e-3) / 1e12
+
+    per_layer = {}
+    attn_ms_sum, attn_flops_sum = 0.0, 0.0
+    for x, r in enumerate(runs):
+        idx_ms = statistics.mean(events[s][x][0].elapsed_time(events[s][x][1]) for s in range(K))
+        att_ms = statistics.mean(events[s][x][1].elapsed_time(events[s][x][2]) for s in range(K))
+        attn_ms_sum += att_ms
+        attn_flops_sum += r.flops
+        per_layer[r.name] = {
+            "n": r.sh["n"], "heads": r.sh["Hq"], "kv_heads": r.sh["Hkv"], "d_h": r.sh["d"],
+            "ms_per_layer": round(idx_ms + att_ms, 4), "t_index_ms": round(idx_ms, 4), "t_sparse_ms": round(att_ms, 4),
+            "edges": int(r.edges.sum()), "effective_tflops": round(r.flops / ((idx_ms + att_ms) * 1e-3) / 1e12, 2),
+            "attention_tflops": round(r.flops / (att_ms * 1e-3) / 1e12, 2),
+            "index_gbs": round(r.index_bytes / (idx_ms * 1e-3) / 1e9, 1) if idx_ms > 0 else None,
+            "index_bytes": r.index_bytes,
+            "density": round(float(r.edges.sum()) / (r.sh["Hq"] * r.sh["n"] * (r.sh["n"] + 1) / 2), 4),
+        }
+    pk, pk_src = peaks()
+    achieved = attn_flops_sum / (attn_ms_sum * 1e-3) / 1e12
+    peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    roofline = {"bound": "tensor", "kernel": "sparse_attn_kernel", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": f"{pk_src} bf16 sustained (kernel timed inside a long step)",
+                "frac_of_burst": round(achieved / float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])), 4),
+                "flops_per_launch": {r.name: r.flops for r in runs},
+                "launch_ms": {r.name: per_layer[r.name]["t_sparse_ms"] for r in runs}}
+    idx_bytes = sum(r.index_bytes for r in runs)
+    idx_ms = sum(per_layer[r.name]["t_index_ms"] for r in runs)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(runs, msa, K, world, device, stream)
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generators, planted structure)",
+        "config": {"workload": "+".join(names) + " prefill layers (B=1, Hq=32, Hkv=8, d_h=128)",
+                   "layers": per_layer, "l2": "inputs larger than L2 (129 MB) between timed iterations",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "index_gbs_total": round(idx_bytes / (idx_ms * 1e-3) / 1e9, 1),
+                   "index_frac_of_hbm": round(idx_bytes / (idx_ms * 1e-3) / 1e9 / float(pk.get("hbm_gbs", 6800.0)), 4)},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, secs, fl, desc = oracle_sample(runs)
+        import oracle
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": desc, "seconds": round(secs, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def end_to_end(runs, msa, K, world, device, stream):
+    """The same metric through host buffers: every step copies Q/K/V from
+    pinned host memory, runs msa_prefill_layer, and reads O back."""
+    host = []
+    for r in runs:
+        hq = r.w["q"].cpu().pin_memory()
+        hk = r.w["k"].cpu().pin_memory()
+        hv = r.w["v"].cpu().pin_memory()
+        ho = torch.empty(r.o.shape, dtype=r.o.dtype).pin_memory()
+        host.append((hq, hk, hv, ho))
+
+    def step():
+        for r, (hq, hk, hv, ho) in zip(runs, host):
+            r.w["q"].copy_(hq, non_blocking=True)
+            r.w["k"].copy_(hk, non_blocking=True)
+            r.w["v"].copy_(hv, non_blocking=True)
+            r.layer(r.w["q"], r.w["k"], r.w["v"], o=r.o)
+            ho.copy_(r.o, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    a.record(stream)
+    for _ in range(K):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(a.elapsed_time(b), world, device)
+    flops = sum(r.flops for r in runs)
+    return {"value": round(world * flops * K / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(sum(r.bytes_in for r in runs)),
+            "d2h_bytes_per_step": int(sum(r.bytes_out for r in runs)), "ms_per_step": round(ms / K, 4)}
+
+
+def reference_arm(args, world, rank, local, names):
+    """The oracle (fp64, host cores) on a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    import oracle
+    import synth
+
+    class HostRun:
+        def __init__(self, name):
+            self.name = name
+            self.w = synth.make_workload(name, device="cuda" if torch.cuda.is_available() else "cpu")
+            self.sh = self.w["shape"]
+
+    runs = [HostRun(nm) for nm in names]
+    for _ in range(max(args.warmup, 3)):
+        oracle_sample(runs, rows_per_head=4)
+    vals, secs_all = [], 0.0
+    desc = ""
+    flops_all = 0.0
+    for _ in range(args.steps):
+        v, secs, fl, desc = oracle_sample(runs, rows_per_head=4)
+        vals.append(v)
+        secs_all += secs
+        flops_all += fl
+    value = flops_all / secs_all / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(1e3 * secs_all / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generators, planted structure)",
+            "config": {"workload": "+".join(names) + " prefill layers (B=1, Hq=32, Hkv=8, d_h=128)",
+                       "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

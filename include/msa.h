@@ -172,6 +172,22 @@ MSA_API msa_status msa_prefill_layer(const msa_shape* shape, const void* q, cons
                              const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
                              size_t ws_bytes, void* stream);
 
+/* The two halves of msa_prefill_layer, in order (the time decomposition
+ * T = T_index + T_sparse of the MInference page eq.(13)): msa_layer_index
+ * builds every Vertical-Slash and Block-Sparse index of the table into `ws`;
+ * msa_layer_attend then runs the one attention launch that reads them.
+ * msa_prefill_layer(...) == msa_layer_index(...) followed by
+ * msa_layer_attend(...) with the same workspace and stream. */
+MSA_API msa_status msa_layer_index(const msa_shape* shape, const void* q, const void* k, const msa_head_cfg* table,
+                                   void* ws, size_t ws_bytes, void* stream);
+MSA_API msa_status msa_layer_attend(const msa_shape* shape, const void* q, const void* k, const void* v,
+                                    const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
+                                    size_t ws_bytes, void* stream);
+
+/* Number of kernels this process has launched through the library so far
+ * (all devices).  Lets a caller count the launches inside a region. */
+MSA_API uint64_t msa_kernel_launches(void);
+
 /* Pointers into a msa_prefill_layer workspace: where that call left the
  * Vertical-Slash index (slot = b * n_vs + rank of the head among the table's
  * VS heads) and the Block-Sparse index (likewise among BS heads).  Any

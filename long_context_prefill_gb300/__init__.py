@@ -27,7 +27,8 @@ PATTERNS = {"ashape": ASHAPE, "vs": VS, "block": BLOCK}
 
 EXPORTS = ("msa_status_string", "msa_vs_index_workspace", "msa_block_index_workspace", "msa_layer_workspace",
            "msa_build_vs_index", "msa_build_block_index", "msa_attn_ashape", "msa_attn_vs", "msa_attn_block",
-           "msa_prefill_layer", "msa_layer_indices", "msa_vs_expand", "msa_poll_device_status")
+           "msa_prefill_layer", "msa_layer_index", "msa_layer_attend", "msa_kernel_launches", "msa_layer_indices",
+           "msa_vs_expand", "msa_poll_device_status")
 
 
 class MsaError(RuntimeError):
@@ -87,6 +88,12 @@ def load(path: str = LIB_PATH):
             lib.msa_attn_block.argtypes = [P, P, P, P, P, i32, i32, i32, P, P, P, P, P, P]
             lib.msa_prefill_layer.restype = st
             lib.msa_prefill_layer.argtypes = [P, P, P, P, P, P, P, P, P, sz, P]
+            lib.msa_layer_index.restype = st
+            lib.msa_layer_index.argtypes = [P, P, P, P, P, sz, P]
+            lib.msa_layer_attend.restype = st
+            lib.msa_layer_attend.argtypes = [P, P, P, P, P, P, P, P, P, sz, P]
+            lib.msa_kernel_launches.restype = ctypes.c_uint64
+            lib.msa_kernel_launches.argtypes = []
             lib.msa_layer_indices.restype = st
             lib.msa_layer_indices.argtypes = [P, P, P, P, P, P]
             lib.msa_vs_expand.restype = st
@@ -301,6 +308,18 @@ class Layer:
                                      _ptr(edges), _ptr(self.ws), self.ws_bytes, _stream(stream)), "msa_prefill_layer")
         return o
 
+    def index(self, q, k, stream=None):
+        """First half of the layer (T_index): build every online index into the workspace."""
+        _check(load().msa_layer_index(ctypes.byref(self.shape), _ptr(q), _ptr(k), self.tarr, _ptr(self.ws),
+                                      self.ws_bytes, _stream(stream)), "msa_layer_index")
+
+    def attend(self, q, k, v, o, lse=None, edges=None, stream=None):
+        """Second half (T_sparse): the single attention launch over the indices in the workspace."""
+        _check(load().msa_layer_attend(ctypes.byref(self.shape), _ptr(q), _ptr(k), _ptr(v), self.tarr, _ptr(o),
+                                       _ptr(lse), _ptr(edges), _ptr(self.ws), self.ws_bytes, _stream(stream)),
+               "msa_layer_attend")
+        return o
+
     def indices(self):
         """(VSIndex view, block_idx, block_cnt) left in the workspace by the last call."""
         lib = load()
@@ -321,6 +340,11 @@ class Layer:
             blk = _view_i32(bi.value, B * len(nbs) * nb * topk).view(B, len(nbs), nb, topk)
             cnt = _view_i32(bc.value, B * len(nbs) * nb).view(B, len(nbs), nb)
         return vs, blk, cnt
+
+
+def kernel_launches() -> int:
+    """Kernels launched through the library by this process so far."""
+    return int(load().msa_kernel_launches())
 
 
 def poll_device_status(stream=None) -> int:

@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include "internal.h"
@@ -11,6 +12,10 @@
 namespace msa {
 
 __device__ int g_device_error = 0;
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+uint64_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 int* device_error_word() {
   void* p = nullptr;

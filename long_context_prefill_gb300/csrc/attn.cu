@@ -732,6 +732,7 @@ msa_status launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   if (items <= 0) return MSA_OK;
   if (items > 0x7FFFFFFF) return MSA_ERR_UNSUPPORTED;
   kern<<<(unsigned)items, kThreads, smem, stream>>>(tq, tk, tv, a, ut);
+  note_launch();
   return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 

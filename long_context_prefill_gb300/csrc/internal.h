@@ -14,6 +14,10 @@ namespace msa {
 enum DeviceError : int { kErrNone = 0, kErrTimeout = 1, kErrIndex = 2 };
 int* device_error_word();  // device address of the current device's error word
 
+// Kernel launches made through the library (process-wide counter).
+void note_launch();
+uint64_t launch_count();
+
 // ------------------------------------------------------------ attention work units
 // A work unit is a stream of 128-row query tiles ("items"), one per t in
 // [0, T).  Each item has two 64-row halves; half h covers rows

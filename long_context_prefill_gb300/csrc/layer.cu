@@ -166,43 +166,52 @@ msa_status msa_build_block_index(const msa_shape* shape, const void* q, const vo
                          (cudaStream_t)stream);
 }
 
-msa_status msa_prefill_layer(const msa_shape* shape, const void* q, const void* k, const void* v,
-                             const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
-                             size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace msa {
+
+static msa_status layer_prepare(const msa_shape* shape, const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const int64_t* edges, const msa_head_cfg* table, void* ws,
+                                size_t ws_bytes, LayerPlan& W) {
   msa_status st = check_shape(shape);
   if (st != MSA_OK) return st;
-  if (!q || !k || !v || !o || !table) return MSA_ERR_INVALID_ARG;
-  for (const void* p : {q, k, v, (const void*)o})
-    if (reinterpret_cast<uintptr_t>(p) % 16) return MSA_ERR_INVALID_ARG;
+  if (!q || !k || !table) return MSA_ERR_INVALID_ARG;
+  for (const void* p : {q, k, v, o})
+    if (p && reinterpret_cast<uintptr_t>(p) % 16) return MSA_ERR_INVALID_ARG;
   if (lse && reinterpret_cast<uintptr_t>(lse) % 4) return MSA_ERR_INVALID_ARG;
   if (edges && reinterpret_cast<uintptr_t>(edges) % 8) return MSA_ERR_INVALID_ARG;
-  const msa_shape& s = *shape;
   LayerPlan P;
-  if ((st = plan_layer(s, table, nullptr, P)) != MSA_OK) return st;
+  if ((st = plan_layer(*shape, table, nullptr, P)) != MSA_OK) return st;
   if (ws_bytes < P.total || (P.total > 256 && !ws)) return MSA_ERR_WORKSPACE_TOO_SMALL;
   void* wsa = ws ? reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~(uintptr_t)255) : nullptr;
-  LayerPlan W;
-  if ((st = plan_layer(s, table, wsa, W)) != MSA_OK) return st;
-  cudaStream_t strm = (cudaStream_t)stream;
-  // 1. online indices (no host synchronisation between the steps)
+  return plan_layer(*shape, table, wsa, W);
+}
+
+static msa_status layer_index(const msa_shape& s, const void* q, const void* k, const LayerPlan& W,
+                              cudaStream_t strm) {
+  msa_status st = MSA_OK;
   if (!W.vs_heads.empty()) {
     st = run_vs_index(s, q, k, W.vs_heads.data(), (int32_t)W.vs_heads.size(), W.vs_cfg, W.vs, W.vs_ws,
                       W.vs_ws_bytes, strm);
     if (st != MSA_OK) return st;
   }
-  if (!W.bs_heads.empty()) {
-    st = run_block_index(s, q, k, W.bs_heads.data(), (int32_t)W.bs_heads.size(), W.bs_cfg.topk, W.bs_idx,
-                         W.bs_cnt, W.bs_ws, W.bs_ws_bytes, strm);
-    if (st != MSA_OK) return st;
-  }
-  // 2. every head's sparse attention in one launch
+  if (!W.bs_heads.empty())
+    st = run_block_index(s, q, k, W.bs_heads.data(), (int32_t)W.bs_heads.size(), W.bs_cfg.topk, W.bs_idx, W.bs_cnt,
+                         W.bs_ws, W.bs_ws_bytes, strm);
+  return st;
+}
+
+static msa_status layer_attend(const msa_shape& s, const void* q, const void* k, const void* v,
+                               const msa_head_cfg* table, void* o, float* lse, int64_t* edges, const LayerPlan& W,
+                               cudaStream_t strm) {
   std::vector<Unit> units;
   for (int32_t h : W.a_heads) ashape_units(s, &h, 1, table[h].sink, table[h].window, units);
   if (!W.vs_heads.empty()) {
     const int32_t nvs = (int32_t)W.vs_heads.size();
     vs_units(s, W.vs_heads.data(), nvs, 0, nvs, units);
   }
-  if (!W.bs_heads.empty()) block_units(s, W.bs_heads.data(), (int32_t)W.bs_heads.size(), (int32_t)W.bs_heads.size(), units);
+  if (!W.bs_heads.empty())
+    block_units(s, W.bs_heads.data(), (int32_t)W.bs_heads.size(), (int32_t)W.bs_heads.size(), units);
   // heavier patterns first within each query tile: the kernel orders items by tile, then unit
   std::vector<Unit> ordered;
   for (const Unit& u : units) if (u.pattern == kUnitVS) ordered.push_back(u);
@@ -219,6 +228,44 @@ msa_status msa_prefill_layer(const msa_shape* shape, const void* q, const void* 
   a.bs_nb = W.nb;
   return attention(s, q, k, v, o, lse, edges, ordered, a, strm);
 }
+
+}  // namespace msa
+
+extern "C" {
+
+msa_status msa_layer_index(const msa_shape* shape, const void* q, const void* k, const msa_head_cfg* table,
+                           void* ws, size_t ws_bytes, void* stream) {
+  LayerPlan W;
+  msa_status st = layer_prepare(shape, q, k, nullptr, nullptr, nullptr, nullptr, table, ws, ws_bytes, W);
+  if (st != MSA_OK) return st;
+  return layer_index(*shape, q, k, W, (cudaStream_t)stream);
+}
+
+msa_status msa_layer_attend(const msa_shape* shape, const void* q, const void* k, const void* v,
+                            const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
+                            size_t ws_bytes, void* stream) {
+  if (!v || !o) return MSA_ERR_INVALID_ARG;
+  LayerPlan W;
+  msa_status st = layer_prepare(shape, q, k, v, o, lse, edges, table, ws, ws_bytes, W);
+  if (st != MSA_OK) return st;
+  return layer_attend(*shape, q, k, v, table, o, lse, edges, W, (cudaStream_t)stream);
+}
+
+msa_status msa_prefill_layer(const msa_shape* shape, const void* q, const void* k, const void* v,
+                             const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
+                             size_t ws_bytes, void* stream) {
+  if (!v || !o) return MSA_ERR_INVALID_ARG;
+  LayerPlan W;
+  msa_status st = layer_prepare(shape, q, k, v, o, lse, edges, table, ws, ws_bytes, W);
+  if (st != MSA_OK) return st;
+  cudaStream_t strm = (cudaStream_t)stream;
+  // 1. online indices, 2. every head's sparse attention in one launch; no
+  // host synchronisation in between
+  if ((st = layer_index(*shape, q, k, W, strm)) != MSA_OK) return st;
+  return layer_attend(*shape, q, k, v, table, o, lse, edges, W, strm);
+}
+
+uint64_t msa_kernel_launches(void) { return launch_count(); }
 
 msa_status msa_layer_indices(const msa_shape* shape, const msa_head_cfg* table, void* ws, msa_vs_index* vs,
                              int32_t** block_idx, int32_t** block_cnt) {

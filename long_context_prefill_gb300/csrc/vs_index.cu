@@ -1,17 +1,823 @@
-// Vertical-Slash online index (placeholder until the proxy kernels land).
+// Online Vertical-Slash index (MInference page §2.1, §3.1 and §6.2; the
+// MInference blog §2.3.2, Vertical-Slash steps 1-3, and §2.3.3 for the sort
+// orders and the per-block form).
+//
+// For each Vertical-Slash head, with R = the last L = min(last_q, n) query
+// rows and scores s_ij = scale * q_i.k_j:
+//   Ã_ij = exp(s_ij - lse_i) for j <= i, lse_i = log Σ_{j<=i} exp(s_ij)
+//   c_j  = Σ_{i in R} Ã_ij                 (vertical score)
+//   r_δ  = Σ_{i in R, i >= δ} Ã_{i,i-δ}    (slash score)
+//   C = top-v of c, D = top-s of r, ties to the lower index.
+//
+// Kernels (all on one stream, no host synchronisation):
+//   proxy_stats   pass 1, tcgen05 S = Q_R K^T over a key chunk; thread = row;
+//                 online (max, sum) per row -> partials
+//   proxy_lse     combine the partials into lse per row
+//   proxy_scores  pass 2, tcgen05 S^T = K Q_R^T; thread = key; Ã for every
+//                 (row, key); c_j summed in registers; slash sums gathered
+//                 along diagonals with warp shuffles into per-key-block bins
+//   slash_finalize  adds each diagonal's bins in a fixed order -> r
+//   topk_select   radix select (threshold), then an index-ordered compaction
+//                 that writes the sorted lists and the bitmaps
+// K is streamed once per pass per group of query heads sharing a KV head; the
+// second pass mostly hits L2.
+#include <cuda_bf16.h>
+#include <math.h>
+#include <string.h>
+
+#include <vector>
+
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace msa {
-size_t vs_index_ws_bytes(const msa_shape& s, const msa_head_cfg& cfg, int32_t n_heads) { return 256; }
+
+namespace {
+
+constexpr int kPackMaxHeads = 8;
+constexpr int kRows = 256;  // query rows per pack (Q tile in shared memory)
+constexpr int kProxyThreads = 320;  // warps 0-7 epilogue, 8 producer, 9 MMA
+constexpr int kProdWarp = 8, kMmaWarpP = 9;
+constexpr int kKStages = 3;
+
+struct Pack {
+  int32_t kvh;                  // b * Hkv + kv head
+  int32_t nh;                   // heads in this pack
+  int32_t slot[kPackMaxHeads];  // output slot per head
+  int32_t qh[kPackMaxHeads];    // b * Hq + query head
+};
+constexpr int kMaxPacks = 96;
+struct PackTable {
+  Pack p[kMaxPacks];
+};
+
+struct ProxyArgs {
+  const void* q;       // bf16 [B*Hq, n, d]
+  int32_t n, d, L, Lp; // proxy rows L, padded to Lp per head
+  int32_t nchunks;     // key chunks per pack
+  int32_t ntiles;      // 128-key tiles over n
+  float c2;            // scale * log2(e)
+  float2* part;        // [packs, nchunks, 256] (max, sum) in log2 units (pass 1 out)
+  float* lse2;         // [packs, 256] (pass 2 in)
+  float* colsum;       // [slots, n] log2 c_j
+  float* rpart;        // [slots, nkb + LB, LB + 1, 32] log2 partial slash sums
+  int32_t nkb;         // 4 * ntiles key blocks of 32
+  int* err;
+};
+
+__device__ __forceinline__ void set_err(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int D>
+struct PLayout {
+  static constexpr int kQChunk = kRows * 128;         // 256 rows x 64 columns
+  static constexpr int kQ = 0;                        // D/64 chunks
+  static constexpr int kKTile = 128 * D * 2;
+  static constexpr int kK = kQ + (D / 64) * kQChunk;
+  static constexpr int kLse = kK + kKStages * kKTile;  // 256 floats
+  static constexpr int kBars = kLse + kRows * 4;
+  static constexpr int kNumBars = 2 * kKStages + 4;
+  static constexpr int kMisc = kBars + kNumBars * 8;
+  static constexpr int kTotal = kMisc + 64;
+  static constexpr int kAlloc = kTotal + 1024;
+};
+
+// Load the pack's proxy rows into the 128-byte-swizzled Q tile:
+// row r = head * Lp + t holds q at position n - L + t (zero if t >= L).
+template <int D>
+__device__ void load_rows(uint8_t* sQ, const ProxyArgs& A, const Pack& P) {
+  constexpr int kC16 = D / 8;
+  const int n = A.n;
+  for (int idx = threadIdx.x; idx < kRows * kC16; idx += blockDim.x) {
+    const int r = idx / kC16, c16 = idx % kC16;
+    const int hh = r / A.Lp, t = r % A.Lp;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (hh < P.nh && t < A.L) {
+      const int64_t row = (int64_t)P.qh[hh] * n + (n - A.L + t);
+      val = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(A.q) + row * D * 2) + c16);
+    }
+    *reinterpret_cast<uint4*>(sQ + (c16 >> 3) * PLayout<D>::kQChunk + sw128_offset(r, c16 & 7)) = val;
+  }
+  fence_proxy_async_smem();
+}
+
+// MODE 1: statistics pass (S = Q K^T, lane = row).  MODE 2: scores pass
+// (S^T = K Q^T, lane = key).  LP: rows per head (32, 64 or 128).
+template <int D, int MODE, int LP>
+__global__ void __launch_bounds__(kProxyThreads, 1)
+    proxy_kernel(const __grid_constant__ CUtensorMap tk, const ProxyArgs A, const __grid_constant__ PackTable PT) {
+  using Ly = PLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm + Ly::kQ;
+  uint8_t* sK = sm + Ly::kK;
+  float* sLse = reinterpret_cast<float*>(sm + Ly::kLse);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::kBars);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + Ly::kMisc);
+  uint64_t* kfull = bars;
+  uint64_t* kempty = bars + kKStages;
+  uint64_t* sfull = bars + 2 * kKStages;
+  uint64_t* sempty = bars + 2 * kKStages + 2;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pack_id = blockIdx.x / A.nchunks, chunk = blockIdx.x % A.nchunks;
+  const Pack& P = PT.p[pack_id];
+  const int n = A.n;
+  const int tiles_per = (A.ntiles + A.nchunks - 1) / A.nchunks;
+  const int tile0 = chunk * tiles_per;
+  const int tile1 = min(A.ntiles, tile0 + tiles_per);
+  const int T = max(0, tile1 - tile0);
+  const int nrows = P.nh * A.Lp;              // rows holding data (<= 256)
+  const int nrt = (nrows + 127) / 128;        // MODE 1: row tiles
+
+  if (warp == 0) {
+    tmem_alloc(const_cast<uint32_t*>(&misc[0]), 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32 * kMmaWarpP) {
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], 8);
+    }
+    misc[2] = 0;
+    fence_mbar_init();
+  }
+  load_rows<D>(sQ, A, P);
+  if (MODE == 2)
+    for (int r = threadIdx.x; r < kRows; r += blockDim.x) sLse[r] = A.lse2[(int64_t)pack_id * kRows + r];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  if (warp == kProdWarp) {
+    if (lane == 0 && T > 0) {
+      tma_prefetch_desc(&tk);
+      bool ok = true;
+      for (int j = 0; j < T && ok; ++j) {
+        const int st = j % kKStages;
+        if (!mbar_wait(&kempty[st], ((j / kKStages) & 1) ^ 1)) { ok = false; break; }
+        const int k0 = (tile0 + j) * 128;
+        mbar_arrive_expect_tx(&kfull[st], Ly::kKTile);
+        uint8_t* dst = sK + st * Ly::kKTile;
+        for (int s = 0; s < 2; ++s)
+          for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384 + s * 8192, &tk, &kfull[st], 64 * c, k0 + 64 * s, P.kvh);
+      }
+      if (!ok) { misc[2] = 1; set_err(A.err, kErrTimeout); }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarpP) {
+    if (lane == 0 && T > 0) {
+      bool ok = true;
+      const uint32_t q0 = smem_u32(sQ);
+      for (int j = 0; j < T && ok; ++j) {
+        const int st = j % kKStages, sb = j & 1;
+        if (!mbar_wait(&kfull[st], (j / kKStages) & 1) || !mbar_wait(&sempty[sb], ((j >> 1) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k0 = smem_u32(sK + st * Ly::kKTile);
+        if (MODE == 1) {
+          constexpr uint32_t id = idesc_bf16_f32(128, 128, false, false);
+          for (int rt = 0; rt < nrt; ++rt)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              const uint32_t qoff = (kk >> 2) * Ly::kQChunk + rt * 16384 + (kk & 3) * 32;
+              mma_bf16_ss(tmem + sb * 256 + rt * 128, sdesc_sw128(q0 + qoff, 16, 1024), sdesc_sw128(k0 + off, 16, 1024),
+                          id, kk > 0 ? 1u : 0u);
+            }
+        } else {
+          const uint32_t id = idesc_bf16_f32(128, nrows, false, false);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * Ly::kQChunk + (kk & 3) * 32;
+            mma_bf16_ss(tmem + sb * 256, sdesc_sw128(k0 + off, 16, 1024), sdesc_sw128(q0 + qoff, 16, 1024), id,
+                        kk > 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&sfull[sb]);
+        mma_commit(&kempty[st]);
+      }
+      if (!ok) { misc[2] = 1; set_err(A.err, kErrTimeout); }
+    }
+    __syncwarp();
+  } else {
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const float c2 = A.c2;
+    bool ok = true;
+    if (MODE == 1) {
+      // ------------------------------------------------ per-row online (max, sum)
+      const int rt = warp >> 2;
+      const int r = rt * 128 + (warp & 3) * 32 + lane;
+      const int t = r % A.Lp;
+      const bool row_ok = r < nrows && t < A.L;
+      const int i = n - A.L + t;  // query position of this row
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < T; ++j) {
+        if (misc[2]) { ok = false; break; }
+        const int sb = j & 1;
+        if (!mbar_wait(&sfull[sb], (j >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (rt < nrt) {
+          float sv[128];
+          uint32_t* u = reinterpret_cast<uint32_t*>(sv);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tmem_ld32(tmem + lane_base + sb * 256 + rt * 128 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(u + 32 * c));
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sempty[sb]);
+          const int k0 = (tile0 + j) * 128;
+          const int lim = row_ok ? min(i, n - 1) - k0 + 1 : 0;  // keys k0 + k valid for k < lim
+          if (lim < 128) {
+#pragma unroll
+            for (int k = 0; k < 128; ++k) sv[k] = k < lim ? sv[k] : -INFINITY;
+          }
+          float mt = sv[0];
+#pragma unroll
+          for (int k = 1; k < 128; ++k) mt = fmaxf(mt, sv[k]);
+          const float mn = fmaxf(m, mt * c2);
+          if (mn != -INFINITY) {
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < 128; ++k) acc += ex2f(fmaf(sv[k], c2, -mn));
+            l = l * ex2f(m - mn) + acc;
+            m = mn;
+          }
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sempty[sb]);
+        }
+      }
+      if (rt * 128 < kRows)
+        A.part[((int64_t)pack_id * A.nchunks + chunk) * kRows + r] = make_float2(row_ok ? m : -INFINITY, row_ok ? l : 0.f);
+    } else {
+      // ------------------------------------------------ per-key Ã, column sums, diagonal bins
+      // Sums are kept as (max, sum of 2^(x - max)) pairs over log2
+      // probabilities x = log2 Ã, so scores far below fp32's range still
+      // rank correctly; outputs are log2 of the sums.
+      constexpr int HPH = 128 / LP;   // heads per column half
+      constexpr int LB = LP / 32;     // 32-row chunks per head
+      const int ch = warp >> 2;       // column half: rows 128ch .. 128ch+127
+      float col_log[HPH];
+      float bin_log[HPH][LB + 1];
+      for (int j = 0; j < T; ++j) {
+        if (misc[2]) { ok = false; break; }
+        const int sb = j & 1;
+        if (!mbar_wait(&sfull[sb], (j >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const int kb0 = (tile0 + j) * 128 + (warp & 3) * 32;  // first key of this warp's block
+        const int key = kb0 + lane;
+#pragma unroll
+        for (int x = 0; x < HPH; ++x) {
+          const int hh = ch * HPH + x;
+          if (hh >= P.nh) continue;  // warp-uniform
+          float cm = -INFINITY, cs = 0.f;
+          float bm[LB + 1], bsum[LB + 1];
+#pragma unroll
+          for (int m = 0; m <= LB; ++m) { bm[m] = -INFINITY; bsum[m] = 0.f; }
+#pragma unroll
+          for (int cc = 0; cc < LB; ++cc) {
+            const int r0 = hh * LP + cc * 32;  // first row of this 32-row chunk
+            uint32_t sraw[32];
+            tmem_ld32(tmem + lane_base + sb * 256 + r0, sraw);
+            tmem_ld_wait();
+            float xv[32];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int tp = 0; tp < 32; ++tp) {
+              const int t = cc * 32 + tp;
+              const bool valid = t < A.L && key <= n - A.L + t && key < n;
+              xv[tp] = valid ? fmaf(__uint_as_float(sraw[tp]), c2, -sLse[r0 + tp]) : -INFINITY;
+              mx = fmaxf(mx, xv[tp]);
+            }
+            // column: running log-sum-exp over the head's rows
+            const float nm = fmaxf(cm, mx);
+            if (nm != -INFINITY) {
+              float acc = 0.f;
+#pragma unroll
+              for (int tp = 0; tp < 32; ++tp) acc += ex2f(xv[tp] - nm);
+              cs = cs * ex2f(cm - nm) + acc;
+              cm = nm;
+            }
+            // diagonal: the slash through (row t, key) has y = key - t; lane
+            // receives y = 32*(block - cc) + lane (hi) or one block lower (lo)
+            float vsh[32];
+            float hm = -INFINITY, lm = -INFINITY;
+#pragma unroll
+            for (int tp = 0; tp < 32; ++tp) {
+              vsh[tp] = __shfl_sync(0xFFFFFFFFu, xv[tp], (lane + tp) & 31);
+              if (lane + tp < 32) hm = fmaxf(hm, vsh[tp]);
+              else lm = fmaxf(lm, vsh[tp]);
+            }
+            {
+              const float a = fmaxf(bm[cc], hm);
+              if (a != -INFINITY) { bsum[cc] *= ex2f(bm[cc] - a); bm[cc] = a; }
+              const float b = fmaxf(bm[cc + 1], lm);
+              if (b != -INFINITY) { bsum[cc + 1] *= ex2f(bm[cc + 1] - b); bm[cc + 1] = b; }
+            }
+            float hs = 0.f, ls = 0.f;
+#pragma unroll
+            for (int tp = 0; tp < 32; ++tp) {
+              const bool hi = lane + tp < 32;
+              const float e = vsh[tp] != -INFINITY ? ex2f(vsh[tp] - (hi ? bm[cc] : bm[cc + 1])) : 0.f;
+              if (hi) hs += e;
+              else ls += e;
+            }
+            bsum[cc] += hs;
+            bsum[cc + 1] += ls;
+          }
+          col_log[x] = cs > 0.f ? cm + __log2f(cs) : -INFINITY;
+#pragma unroll
+          for (int m = 0; m <= LB; ++m) bin_log[x][m] = bsum[m] > 0.f ? bm[m] + __log2f(bsum[m]) : -INFINITY;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sempty[sb]);
+        const int kb = kb0 >> 5;  // key block index
+#pragma unroll
+        for (int x = 0; x < HPH; ++x) {
+          const int hh = ch * HPH + x;
+          if (hh >= P.nh) continue;
+          const int64_t slot = P.slot[hh];
+          if (key < n) A.colsum[slot * n + key] = col_log[x];
+#pragma unroll
+          for (int m = 0; m <= LB; ++m)
+            A.rpart[((slot * (A.nkb + LB) + (kb - m + LB)) * (LB + 1) + m) * 32 + lane] = bin_log[x][m];
+        }
+      }
+    }
+    if (!ok) { misc[2] = 1; set_err(A.err, kErrTimeout); }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// lse2 per row = log2-domain log-sum-exp over the chunks' partials.
+__global__ void proxy_lse_kernel(const float2* part, int nchunks, float* lse2) {
+  const int pk = blockIdx.x, r = threadIdx.x;
+  float m = -INFINITY;
+  for (int c = 0; c < nchunks; ++c) m = fmaxf(m, part[((int64_t)pk * nchunks + c) * kRows + r].x);
+  float l = 0.f;
+  if (m != -INFINITY)
+    for (int c = 0; c < nchunks; ++c) {
+      const float2 v = part[((int64_t)pk * nchunks + c) * kRows + r];
+      if (v.x != -INFINITY) l += v.y * exp2f(v.x - m);
+    }
+  lse2[(int64_t)pk * kRows + r] = (l > 0.f) ? m + log2f(l) : INFINITY;  // +inf -> exp2(s - lse) = 0 for empty rows
+}
+
+// log2 r_δ = log-sum-exp over the bins (y = n - L - δ) of the key blocks that
+// own them, m = 0..LB in order.
+__global__ void slash_finalize_kernel(const float* rpart, int n, int L, int LB, int nkb, int slots, float* r) {
+  const int64_t total = (int64_t)slots * n;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t slot = idx / n;
+    const int d = (int)(idx % n);
+    const int y = n - L - d;
+    const int beta = (y >= 0) ? (y >> 5) : -((31 - y) >> 5);  // floor(y / 32)
+    const int ln = y - 32 * beta;
+    float v[5];
+    float mx = -INFINITY;
+    for (int m = 0; m <= LB; ++m) {
+      const int kb = beta + m;
+      v[m] = (kb < 0 || kb >= nkb) ? -INFINITY
+                                   : rpart[((slot * (nkb + LB) + (beta + LB)) * (LB + 1) + m) * 32 + ln];
+      mx = fmaxf(mx, v[m]);
+    }
+    float s = 0.f;
+    if (mx != -INFINITY)
+      for (int m = 0; m <= LB; ++m) s += v[m] != -INFINITY ? exp2f(v[m] - mx) : 0.f;
+    r[slot * n + d] = s > 0.f ? mx + log2f(s) : -INFINITY;
+  }
+}
+
+// Order-preserving map from float to unsigned (larger float -> larger key).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t b = __float_as_uint(f == 0.f ? 0.f : f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// ------------------------------------------------------------------ top-k
+constexpr int kTopkThreads = 1024;
+
+__device__ int block_excl_scan(int v, int* sh, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += y;
+    }
+    sh[lane] = w;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? sh[warp - 1] : 0) + x - v;
+  total = sh[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return before;
+}
+
+struct TopkJob {
+  const float* vals;
+  int32_t* list;   // [cap]
+  int32_t* cnt;
+  uint32_t* bits;  // [words]
+  int32_t k;
+  int32_t descending;  // write the list in descending index order
+};
+
+// Both score vectors of every slot: block 2*slot selects the verticals from
+// the column sums, block 2*slot+1 the slashes from the slash sums.
+struct TopkArgs {
+  const float* colsum;
+  const float* slashsum;
+  msa_vs_index out;
+  int32_t vk, sk;
+};
+
+__device__ __forceinline__ TopkJob topk_job(const TopkArgs& a, int n) {
+  const int slot = blockIdx.x >> 1;
+  const int words = (n + 31) / 32;
+  TopkJob J;
+  if ((blockIdx.x & 1) == 0) {
+    J.vals = a.colsum + (int64_t)slot * n;
+    J.list = a.out.vertical + (int64_t)slot * a.out.v_cap;
+    J.cnt = a.out.vertical_cnt + slot;
+    J.bits = a.out.vertical_bits + (int64_t)slot * words;
+    J.k = a.vk;
+    J.descending = 0;
+  } else {
+    J.vals = a.slashsum + (int64_t)slot * n;
+    J.list = a.out.slash + (int64_t)slot * a.out.s_cap;
+    J.cnt = a.out.slash_cnt + slot;
+    J.bits = a.out.slash_bits + (int64_t)slot * words;
+    J.k = a.sk;
+    J.descending = 1;
+  }
+  return J;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs args, int n) {
+  const TopkJob J = topk_job(args, n);
+  __shared__ int hist[2048];
+  __shared__ int sh[32];
+  __shared__ int s_digit, s_above;
+  const int words = (n + 31) / 32;
+  const int k = J.k < n ? J.k : n;
+  uint32_t prefix = 0, pmask = 0;
+  int need = k;  // how many to take among values matching the prefix
+  if (k > 0 && k < n) {
+    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+    for (int pass = 0; pass < 3; ++pass) {
+      const int sft = shifts[pass], nb = 1 << widths[pass];
+      for (int b = threadIdx.x; b < nb; b += blockDim.x) hist[b] = 0;
+      __syncthreads();
+      for (int x = threadIdx.x; x < n; x += blockDim.x) {
+        const uint32_t key = order_key(J.vals[x]);
+        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sft) & (nb - 1)], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int cum = 0, b = nb - 1;
+        for (; b > 0; --b) {
+          if (cum + hist[b] >= need) break;
+          cum += hist[b];
+        }
+        s_digit = b;
+        s_above = cum;
+      }
+      __syncthreads();
+      need -= s_above;
+      prefix |= (uint32_t)s_digit << sft;
+      pmask |= (uint32_t)(nb - 1) << sft;
+      __syncthreads();
+    }
+  }
+  // prefix = bit pattern of the k-th largest; `need` values equal to it are taken
+  const bool all = (k >= n), none = (k <= 0);
+  int base_sel = 0, base_eq = 0;
+  for (int w0 = 0; w0 < words; w0 += blockDim.x) {
+    const int w = w0 + threadIdx.x;
+    uint32_t gt = 0, eq = 0;
+    if (w < words) {
+      for (int b = 0; b < 32; ++b) {
+        const int x = w * 32 + b;
+        if (x >= n) break;
+        const uint32_t key = order_key(J.vals[x]);
+        if (all || (!none && key > prefix)) gt |= 1u << b;
+        else if (!all && !none && key == prefix) eq |= 1u << b;
+      }
+    }
+    int eq_total;
+    const int eq_before = block_excl_scan(__popc(eq), sh, eq_total) + base_eq;
+    // keep the first `need` equal values in index order
+    uint32_t take = 0;
+    int rank = eq_before;
+    for (int b = 0; b < 32; ++b)
+      if ((eq >> b) & 1u) {
+        if (rank < need) take |= 1u << b;
+        ++rank;
+      }
+    const uint32_t sel = gt | take;
+    int sel_total;
+    const int pos = block_excl_scan(__popc(sel), sh, sel_total) + base_sel;
+    if (w < words) {
+      J.bits[w] = sel;
+      int p = pos;
+      for (int b = 0; b < 32; ++b)
+        if ((sel >> b) & 1u) {
+          const int outp = J.descending ? (k - 1 - p) : p;
+          if (outp >= 0 && outp < k) J.list[outp] = w * 32 + b;
+          ++p;
+        }
+    }
+    base_sel += sel_total;
+    base_eq += eq_total;
+  }
+  if (threadIdx.x == 0) *J.cnt = base_sel < k ? base_sel : k;
+}
+
+// ------------------------------------------------------------------ per-block expansion
+// One thread per query block u: merged slash ranges [a-δ, e-δ] ∩ [0, e] in
+// ascending order (δ descending), then the verticals c <= e outside them.
+__global__ void vs_expand_kernel(const int32_t* vertical, const int32_t* vcnt_p, int vcap, const int32_t* slash,
+                                 const int32_t* scnt_p, int scap, int n,
+                                 int u_begin, int u_count, int range_cap, int col_cap, int32_t* range_cnt,
+                                 int32_t* ranges, int32_t* col_cnt, int32_t* cols) {
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= u_count) return;
+  const int u = u_begin + x;
+  const int a = 64 * u, e = min(a + 64, n) - 1;
+  const int vcnt = min(max(*vcnt_p, 0), vcap), scnt = min(max(*scnt_p, 0), scap);
+  int nr = 0, lo = 0, hi = -2;
+  bool open = false;
+  for (int t = 0; t < scnt; ++t) {  // slash list is δ-descending -> starts ascending
+    const int delta = slash[t];
+    if (delta < 0 || e - delta < 0) continue;
+    const int l0 = max(a - delta, 0), h0 = e - delta;
+    if (open && l0 <= hi + 1) {
+      hi = max(hi, h0);
+    } else {
+      if (open) {
+        if (nr < range_cap) { ranges[((int64_t)x * range_cap + nr) * 2] = lo; ranges[((int64_t)x * range_cap + nr) * 2 + 1] = hi; }
+        ++nr;
+      }
+      lo = l0; hi = h0; open = true;
+    }
+  }
+  if (open) {
+    if (nr < range_cap) { ranges[((int64_t)x * range_cap + nr) * 2] = lo; ranges[((int64_t)x * range_cap + nr) * 2 + 1] = hi; }
+    ++nr;
+  }
+  range_cnt[x] = nr;
+  // columns: both lists ascending -> one merge walk
+  int nc = 0, rp = 0;
+  for (int t = 0; t < vcnt; ++t) {
+    const int c = vertical[t];
+    if (c < 0 || c > e) continue;
+    while (rp < min(nr, range_cap) && ranges[((int64_t)x * range_cap + rp) * 2 + 1] < c) ++rp;
+    bool covered = rp < min(nr, range_cap) && ranges[((int64_t)x * range_cap + rp) * 2] <= c;
+    if (!covered && nr > range_cap) {  // ranges beyond the cap were dropped: test against the slashes directly
+      for (int s = 0; s < scnt && !covered; ++s) {
+        const int delta = slash[s];
+        covered = delta >= 0 && c >= a - delta && c <= e - delta;
+      }
+    }
+    if (!covered) {
+      if (nc < col_cap) cols[(int64_t)x * col_cap + nc] = c;
+      ++nc;
+    }
+  }
+  col_cnt[x] = nc;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+int padded_rows(int L) { return L <= 32 ? 32 : (L <= 64 ? 64 : 128); }
+
+struct VSPlan {
+  std::vector<Pack> packs;
+  int L, Lp, LB, ntiles, nkb, nchunks1, nchunks2, slots;
+  size_t off_part, off_lse, off_col, off_slash, off_rpart, total;
+};
+
+VSPlan plan_vs(const msa_shape& s, const int32_t* heads, int32_t n_heads, const msa_head_cfg& cfg, int sms) {
+  VSPlan P;
+  P.L = cfg.last_q < s.n ? cfg.last_q : s.n;
+  P.Lp = padded_rows(P.L);
+  P.LB = P.Lp / 32;
+  const int per_pack = kRows / P.Lp < kPackMaxHeads ? kRows / P.Lp : kPackMaxHeads;
+  const int g = s.Hq / s.Hkv;
+  if (heads) {
+    for (int b = 0; b < s.B; ++b)
+      for (int kv = 0; kv < s.Hkv; ++kv) {
+        Pack cur;
+        memset(&cur, 0, sizeof(cur));
+        cur.kvh = b * s.Hkv + kv;
+        for (int x = 0; x < n_heads; ++x) {
+          if (heads[x] / g != kv) continue;
+          cur.slot[cur.nh] = b * n_heads + x;
+          cur.qh[cur.nh] = b * s.Hq + heads[x];
+          if (++cur.nh == per_pack) {
+            P.packs.push_back(cur);
+            cur.nh = 0;
+          }
+        }
+        if (cur.nh) P.packs.push_back(cur);
+      }
+  }
+  P.ntiles = ceil_div(s.n, 128);
+  P.nkb = 4 * P.ntiles;
+  const int np = P.packs.empty() ? 1 : (int)P.packs.size();
+  auto chunks = [&](int target) {
+    int c = ceil_div(target, np);
+    if (c > P.ntiles) c = P.ntiles;
+    return c < 1 ? 1 : c;
+  };
+  P.nchunks1 = chunks(sms);
+  P.nchunks2 = chunks(sms);
+  P.slots = s.B * n_heads;
+  size_t off = 0;
+  P.off_part = off; off = align256(off + sizeof(float2) * (size_t)np * P.nchunks1 * kRows);
+  P.off_lse = off;  off = align256(off + sizeof(float) * (size_t)np * kRows);
+  P.off_col = off;  off = align256(off + sizeof(float) * (size_t)P.slots * s.n);
+  P.off_slash = off; off = align256(off + sizeof(float) * (size_t)P.slots * s.n);
+  P.off_rpart = off; off = align256(off + sizeof(float) * (size_t)P.slots * (P.nkb + P.LB) * (P.LB + 1) * 32);
+  P.total = off + 256;
+  return P;
+}
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) return 148;
+  return sms;
+}
+
+template <int D, int MODE, int LP>
+msa_status launch_proxy(const CUtensorMap& tk, const ProxyArgs& a, const std::vector<Pack>& packs, int nchunks,
+                        cudaStream_t stream) {
+  auto kern = proxy_kernel<D, MODE, LP>;
+  const int smem = PLayout<D>::kAlloc;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return MSA_ERR_CUDA;
+  for (size_t base = 0; base < packs.size(); base += kMaxPacks) {
+    PackTable pt;
+    memset(&pt, 0, sizeof(pt));
+    const size_t cnt = packs.size() - base < (size_t)kMaxPacks ? packs.size() - base : (size_t)kMaxPacks;
+    for (size_t x = 0; x < cnt; ++x) pt.p[x] = packs[base + x];
+    ProxyArgs aa = a;
+    aa.part = a.part + base * nchunks * kRows;
+    aa.lse2 = a.lse2 + base * kRows;
+    aa.nchunks = nchunks;
+    kern<<<(unsigned)(cnt * nchunks), kProxyThreads, smem, stream>>>(tk, aa, pt);
+    note_launch();
+    if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+  }
+  return MSA_OK;
+}
+
+template <int D>
+msa_status launch_scores(int Lp, const CUtensorMap& tk, const ProxyArgs& a, const std::vector<Pack>& packs,
+                         int nchunks, cudaStream_t stream) {
+  if (Lp == 32) return launch_proxy<D, 2, 32>(tk, a, packs, nchunks, stream);
+  if (Lp == 64) return launch_proxy<D, 2, 64>(tk, a, packs, nchunks, stream);
+  return launch_proxy<D, 2, 128>(tk, a, packs, nchunks, stream);
+}
+
+}  // namespace
+
+size_t vs_index_ws_bytes(const msa_shape& s, const msa_head_cfg& cfg, int32_t n_heads) {
+  std::vector<int32_t> heads((size_t)n_heads);
+  for (int x = 0; x < n_heads; ++x) heads[(size_t)x] = x % s.Hq;
+  // pack count is largest when every head sits in its own KV group
+  msa_shape worst = s;
+  VSPlan P = plan_vs(worst, nullptr, n_heads, cfg, 1);
+  const int packs_max = s.B * n_heads;
+  const int sms = sm_count();
+  const int nch = ceil_div(sms, 1) < P.ntiles ? sms : P.ntiles;
+  size_t total = 0;
+  total += align256(sizeof(float2) * (size_t)packs_max * (nch < 1 ? 1 : nch) * kRows);
+  total += align256(sizeof(float) * (size_t)packs_max * kRows);
+  total += align256(sizeof(float) * (size_t)s.B * n_heads * s.n) * 2;
+  total += align256(sizeof(float) * (size_t)s.B * n_heads * (P.nkb + P.LB) * (P.LB + 1) * 32);
+  return total + 1024;
+}
+
 msa_status run_vs_index(const msa_shape& s, const void* q, const void* k, const int32_t* heads, int32_t n_heads,
                         const msa_head_cfg& cfg, const msa_vs_index& out, void* ws, size_t ws_bytes,
                         cudaStream_t stream) {
-  return MSA_ERR_UNSUPPORTED;
+  if (cfg.last_q > 128) return MSA_ERR_UNSUPPORTED;
+  if (!out.vertical || !out.vertical_cnt || !out.slash || !out.slash_cnt || !out.vertical_bits || !out.slash_bits)
+    return MSA_ERR_INVALID_ARG;
+  const int vcap = cfg.n_vertical < s.n ? cfg.n_vertical : s.n;
+  const int scap = cfg.n_slash < s.n ? cfg.n_slash : s.n;
+  if (out.v_cap < vcap || out.s_cap < scap) return MSA_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < vs_index_ws_bytes(s, cfg, n_heads)) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  VSPlan P = plan_vs(s, heads, n_heads, cfg, sm_count());
+  if (P.total > ws_bytes) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~(uintptr_t)255);
+  if (P.total + 256 > ws_bytes) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap tk;
+  if (!make_bf16_map(&tk, k, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64)) return MSA_ERR_CUDA;
+  ProxyArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.n = s.n;
+  a.d = s.d_h;
+  a.L = P.L;
+  a.Lp = P.Lp;
+  a.ntiles = P.ntiles;
+  a.nkb = P.nkb;
+  const float scale = s.scale > 0.f ? s.scale : 1.0f / sqrtf((float)s.d_h);
+  a.c2 = scale * 1.4426950408889634f;
+  a.part = reinterpret_cast<float2*>(w + P.off_part);
+  a.lse2 = reinterpret_cast<float*>(w + P.off_lse);
+  a.colsum = reinterpret_cast<float*>(w + P.off_col);
+  a.rpart = reinterpret_cast<float*>(w + P.off_rpart);
+  a.err = device_error_word();
+  if (!a.err) return MSA_ERR_CUDA;
+  float* slashsum = reinterpret_cast<float*>(w + P.off_slash);
+  msa_status st;
+  // pass 1: row statistics
+  st = s.d_h == 128 ? launch_proxy<128, 1, 64>(tk, a, P.packs, P.nchunks1, stream)
+                    : launch_proxy<64, 1, 64>(tk, a, P.packs, P.nchunks1, stream);
+  if (st != MSA_OK) return st;
+  proxy_lse_kernel<<<(unsigned)P.packs.size(), kRows, 0, stream>>>(a.part, P.nchunks1, a.lse2);
+  note_launch();
+  if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+  // pass 2: probabilities, column sums and diagonal bins
+  st = s.d_h == 128 ? launch_scores<128>(P.Lp, tk, a, P.packs, P.nchunks2, stream)
+                    : launch_scores<64>(P.Lp, tk, a, P.packs, P.nchunks2, stream);
+  if (st != MSA_OK) return st;
+  {
+    const int64_t total = (int64_t)P.slots * s.n;
+    const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+    slash_finalize_kernel<<<blocks, 256, 0, stream>>>(a.rpart, s.n, P.L, P.LB, P.nkb, P.slots, slashsum);
+    note_launch();
+    if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+  }
+  // top-k for both score vectors of every slot
+  TopkArgs ta;
+  ta.colsum = a.colsum;
+  ta.slashsum = slashsum;
+  ta.out = out;
+  ta.vk = vcap;
+  ta.sk = scap;
+  topk_kernel<<<(unsigned)(P.slots * 2), kTopkThreads, 0, stream>>>(ta, s.n);
+  note_launch();
+  if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+  return MSA_OK;
 }
+
 }  // namespace msa
+
+using namespace msa;
 
 extern "C" msa_status msa_vs_expand(const msa_shape* shape, const msa_vs_index* index, int32_t slot, int32_t u_begin,
                                     int32_t u_count, int32_t range_cap, int32_t col_cap, int32_t* range_cnt,
                                     int32_t* ranges, int32_t* col_cnt, int32_t* cols, void* stream) {
-  return MSA_ERR_UNSUPPORTED;
+  if (!shape || !index || shape->n < 1 || slot < 0 || u_begin < 0 || u_count < 1 || range_cap < 0 || col_cap < 0)
+    return MSA_ERR_INVALID_ARG;
+  if (!range_cnt || !ranges || !col_cnt || !cols || !index->vertical || !index->slash || !index->vertical_cnt ||
+      !index->slash_cnt)
+    return MSA_ERR_INVALID_ARG;
+  const int nb = ceil_div(shape->n, 64);
+  if (u_begin + (int64_t)u_count > nb) return MSA_ERR_INVALID_ARG;
+  vs_expand_kernel<<<(u_count + 127) / 128, 128, 0, (cudaStream_t)stream>>>(
+      index->vertical + (int64_t)slot * index->v_cap, index->vertical_cnt + slot, index->v_cap,
+      index->slash + (int64_t)slot * index->s_cap, index->slash_cnt + slot, index->s_cap,
+      shape->n, u_begin, u_count, range_cap, col_cap, range_cnt, ranges, col_cnt, cols);
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }

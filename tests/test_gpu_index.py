@@ -1,0 +1,149 @@
+"""GPU parity of the online indices against the fp64 oracle.
+
+Index sets must match exactly; on random inputs a member may differ only if
+its oracle score lies within 1e-4 (relative) of the oracle's k-th score, for
+both the missing and the extra member (fp32 device scores vs fp64)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import f32, head_qkv, unpack_bits
+
+pytestmark = pytest.mark.gpu
+
+REL = 1e-4
+
+
+def check_set(got, want, scores, what):
+    got, want = set(int(x) for x in got), set(int(x) for x in want)
+    assert len(got) == len(want), f"{what}: {len(got)} vs {len(want)} members"
+    if got == want:
+        return 0
+    kth = min(scores[x] for x in want)
+    for x in got ^ want:
+        assert abs(scores[x] - kth) <= REL * abs(kth), f"{what}: member {x} score {scores[x]!r} vs k-th {kth!r}"
+    return len(got ^ want)
+
+
+def run_vs(msa, q, k, heads, last_q, v, s):
+    idx = msa.build_vs_index(q, k, heads, last_q, v, s)
+    assert msa.poll_device_status() == 0
+    return idx
+
+
+def check_vs_against_oracle(idx, q, k, heads, last_q, v, s, exact=False):
+    B, Hq, n, d = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / np.sqrt(d)
+    diffs = 0
+    for b in range(B):
+        for x, h in enumerate(heads):
+            slot = b * len(heads) + x
+            qn, kn, _ = head_qkv(q, k, k, b, h, Hq, Hkv)
+            C, D, c, r = oracle.vs_index(qn, kn, last_q, v, s, scale)
+            vc, sc = int(idx.vertical_cnt[slot]), int(idx.slash_cnt[slot])
+            gC = idx.vertical[slot, :vc].cpu().numpy()
+            gD = idx.slash[slot, :sc].cpu().numpy()
+            assert vc == min(v, n) and sc == min(s, n)
+            assert np.all(np.diff(gC) > 0), "verticals must be ascending"
+            assert np.all(np.diff(gD) < 0), "slashes must be descending"
+            # bitmaps agree with the lists
+            assert np.array_equal(unpack_bits(idx.vertical_bits[slot].cpu().numpy(), n), np.sort(gC))
+            assert np.array_equal(unpack_bits(idx.slash_bits[slot].cpu().numpy(), n), np.sort(gD))
+            if exact:
+                assert set(gC.tolist()) == set(C.tolist()) and set(gD.tolist()) == set(D.tolist())
+            else:
+                diffs += check_set(gC, C, c, f"vertical b{b} h{h}")
+                diffs += check_set(gD, D, r, f"slash b{b} h{h}")
+    return diffs
+
+
+def test_vs_index_tiny_planted(cuda_lib):
+    """Tiny workload head 1 (planted verticals and slashes): exact sets."""
+    w = synth.make_workload("tiny", device="cuda")
+    idx = run_vs(cuda_lib, w["q"], w["k"], [1], 64, 64, 128)
+    check_vs_against_oracle(idx, w["q"], w["k"], [1], 64, 64, 128, exact=True)
+
+
+@pytest.mark.parametrize("n,d,last_q,Hq,Hkv,heads,v,s", [
+    (1000, 128, 64, 4, 1, [0, 1, 2, 3], 40, 90),    # one pack of four heads, ragged n
+    (777, 64, 17, 4, 2, [1, 2, 3], 13, 50),         # 32-row padding, two groups
+    (1500, 128, 100, 2, 1, [0, 1], 60, 1500),       # 128-row padding, every offset kept
+    (300, 128, 64, 2, 2, [1], 400, 7),              # more verticals than keys
+    (64, 128, 64, 1, 1, [0], 5, 5),                 # a single block
+])
+def test_vs_index_random(cuda_lib, n, d, last_q, Hq, Hkv, heads, v, s):
+    q, k, _ = synth.random_qkv(1, Hq, Hkv, n, d, seed=n + last_q, device="cuda")
+    idx = run_vs(cuda_lib, q, k, heads, last_q, v, s)
+    check_vs_against_oracle(idx, q, k, heads, last_q, v, s)
+
+
+def test_vs_index_batch(cuda_lib):
+    q, k, _ = synth.random_qkv(2, 4, 2, 600, 128, seed=21, device="cuda")
+    idx = run_vs(cuda_lib, q, k, [0, 3], 64, 30, 60)
+    check_vs_against_oracle(idx, q, k, [0, 3], 64, 30, 60)
+
+
+def test_vs_expand_matches_oracle_blocks(cuda_lib):
+    """Per-block ranges and uncovered columns (integer merge) bit-exact."""
+    w = synth.make_workload("tiny", device="cuda")
+    idx = run_vs(cuda_lib, w["q"], w["k"], [1], 64, 64, 128)
+    n = 2048
+    nb = n // 64
+    rc, rg, cc, cl = cuda_lib.vs_expand(tuple(w["q"].shape), idx, 0, 0, nb, 256, 128)
+    assert cuda_lib.poll_device_status() == 0
+    C = idx.vertical[0, :int(idx.vertical_cnt[0])].cpu().numpy()
+    D = idx.slash[0, :int(idx.slash_cnt[0])].cpu().numpy()
+    rc, rg, cc, cl = (t.cpu().numpy() for t in (rc, rg, cc, cl))
+    for u in range(nb):
+        ranges, cols = oracle.vs_block_index(u, n, 64, C, D)
+        assert rc[u] == len(ranges) and cc[u] == len(cols)
+        assert np.array_equal(rg[u, :rc[u]], ranges)
+        assert np.array_equal(cl[u, :cc[u]], cols)
+
+
+def check_bs_against_oracle(J, C, q, k, heads, topk, exact=False):
+    B, Hq, n, d = q.shape
+    Hkv = k.shape[1]
+    diffs = 0
+    for b in range(B):
+        for x, h in enumerate(heads):
+            qn, kn, _ = head_qkv(q, k, k, b, h, Hq, Hkv)
+            Jo, Co = oracle.bs_index(qn, kn, 64, topk)
+            qb, kb = oracle.bs_pool(qn, 64), oracle.bs_pool(kn, 64)
+            Jg, Cg = J[b, x].cpu().numpy(), C[b, x].cpu().numpy()
+            assert np.array_equal(Cg, Co), "block counts"
+            for u in range(Jo.shape[0]):
+                g = Jg[u, :Cg[u]]
+                assert np.all(np.diff(g) > 0) and g[-1] == u
+                assert np.all(Jg[u, Cg[u]:] == -1)
+                if exact:
+                    assert np.array_equal(g, Jo[u, :Co[u]])
+                else:
+                    sc = qb[u] @ kb[:u].T if u else np.zeros(0)
+                    diffs += check_set([v for v in g if v != u], [v for v in Jo[u, :Co[u]] if v != u], sc,
+                                       f"blocks b{b} h{h} u{u}")
+    return diffs
+
+
+@pytest.mark.parametrize("n,d,Hq,Hkv,heads,topk", [
+    (1000, 128, 4, 2, [0, 1, 3], 5),
+    (4096, 64, 2, 1, [1], 17),
+    (130, 128, 1, 1, [0], 100),    # top-k beyond the block count
+    (2048, 128, 2, 2, [0, 1], 1),  # diagonal only
+])
+def test_block_index_random(cuda_lib, n, d, Hq, Hkv, heads, topk):
+    q, k, _ = synth.random_qkv(1, Hq, Hkv, n, d, seed=n + topk, device="cuda")
+    J, C = cuda_lib.build_block_index(q, k, heads, topk)
+    assert cuda_lib.poll_device_status() == 0
+    check_bs_against_oracle(J, C, q, k, heads, topk)
+
+
+def test_block_index_clustered(cuda_lib):
+    """Block-clustered workload (shared block means) at reduced length: exact."""
+    w = synth.make_workload("bs128k", device="cuda", n=8192, Hq=4, Hkv=1)
+    J, C = cuda_lib.build_block_index(w["q"], w["k"], [0, 2], 16)
+    assert cuda_lib.poll_device_status() == 0
+    check_bs_against_oracle(J, C, w["q"], w["k"], [0, 2], 16)
