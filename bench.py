@@ -166,9 +166,9 @@ def algorithmic_index_bytes(w) -> int:
 
 
 class LayerRun:
-    def __init__(self, name, device, msa, synth):
+    def __init__(self, name, device, msa, synth, n=None):
         self.name = name
-        self.w = synth.make_workload(name, device=device)
+        self.w = synth.make_workload(name, device=device, n=n)
         sh = self.w["shape"]
         self.sh = sh
         self.layer = msa.Layer(self.w["table"], sh["B"], sh["Hq"], sh["Hkv"], sh["n"], sh["d"], device)
@@ -242,6 +242,8 @@ def main():
     ap.add_argument("--workloads", default=",".join(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--n", type=int, default=None,
+                    help="override the sequence length (scaled-down runs for profiling; not a headline number)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     names = [x for x in args.workloads.split(",") if x]
@@ -255,7 +257,7 @@ def main():
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     msa.load()
-    runs = [LayerRun(nm, device, msa, synth) for nm in names]
+    runs = [LayerRun(nm, device, msa, synth, n=args.n) for nm in names]
     assert msa.poll_device_status() == 0
     step_flops = sum(r.flops for r in runs)
     stream = torch.cuda.current_stream()
@@ -331,7 +333,8 @@ def main():
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generators, planted structure)",
-        "config": {"workload": "+".join(names) + " prefill layers (B=1, Hq=32, Hkv=8, d_h=128)",
+        "config": {"workload": "+".join(names) + " prefill layers (B=1, Hq=32, Hkv=8, d_h=128)"
+                   + (f", n overridden to {args.n}" if args.n else ""),
                    "layers": per_layer, "l2": "inputs larger than L2 (129 MB) between timed iterations",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "index_gbs_total": round(idx_bytes / (idx_ms * 1e-3) / 1e9, 1),

@@ -82,11 +82,15 @@ typedef struct {
 
 /* Vertical-Slash index of a set of heads (device buffers owned by the caller).
  * For slot s (see conventions), with v_cap = min(n_vertical, n) and
- * s_cap = min(n_slash, n) and words = ceil(n / 32):
+ * s_cap = min(n_slash, n), words = ceil(n / 32), cover_words = ceil((n + 63) / 32):
  *   vertical[s * v_cap + t]   column indices C_h, ascending (t < vertical_cnt[s])
  *   slash[s * s_cap + t]      diagonal offsets D_h (δ = i - j), descending
  *   vertical_bits[s * words]  bit j set iff j ∈ C_h
  *   slash_bits[s * words]     bit δ set iff δ ∈ D_h
+ *   slash_cover[s * cover_words]  bit z set iff D_h has an offset in
+ *       [n-1-z, n+62-z]; for a full 64-row query block [a, a+63], key j is
+ *       covered by one of the block's slash tiles iff bit n-1-a+j is set
+ *       (the per-tile masks the attention kernel reads with a few word loads)
  * (MInference blog §2.3.3: verticals sorted ascending, slashes descending.) */
 typedef struct {
   int32_t* vertical;
@@ -95,6 +99,7 @@ typedef struct {
   int32_t* slash_cnt;
   uint32_t* vertical_bits;
   uint32_t* slash_bits;
+  uint32_t* slash_cover;
   int32_t v_cap;
   int32_t s_cap;
 } msa_vs_index;

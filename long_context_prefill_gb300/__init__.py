@@ -51,7 +51,7 @@ class HeadCfg(ctypes.Structure):
 class VSIndexC(ctypes.Structure):
     _fields_ = [("vertical", ctypes.c_void_p), ("vertical_cnt", ctypes.c_void_p), ("slash", ctypes.c_void_p),
                 ("slash_cnt", ctypes.c_void_p), ("vertical_bits", ctypes.c_void_p), ("slash_bits", ctypes.c_void_p),
-                ("v_cap", ctypes.c_int32), ("s_cap", ctypes.c_int32)]
+                ("slash_cover", ctypes.c_void_p), ("v_cap", ctypes.c_int32), ("s_cap", ctypes.c_int32)]
 
 
 _lib = None
@@ -178,11 +178,12 @@ class VSIndex:
         self.slash_cnt = torch.empty(slots, dtype=torch.int32, device=device)
         self.vertical_bits = torch.zeros(slots, words, dtype=torch.int32, device=device)
         self.slash_bits = torch.zeros(slots, words, dtype=torch.int32, device=device)
+        self.slash_cover = torch.zeros(slots, (n + 63 + 31) // 32, dtype=torch.int32, device=device)
 
     def c(self) -> VSIndexC:
         return VSIndexC(self.vertical.data_ptr(), self.vertical_cnt.data_ptr(), self.slash.data_ptr(),
                         self.slash_cnt.data_ptr(), self.vertical_bits.data_ptr(), self.slash_bits.data_ptr(),
-                        self.v_cap, self.s_cap)
+                        self.slash_cover.data_ptr(), self.v_cap, self.s_cap)
 
     @staticmethod
     def from_c(c: VSIndexC, slots: int, n: int):
@@ -196,6 +197,8 @@ class VSIndex:
         ix.slash_cnt = _view_i32(c.slash_cnt, slots)
         ix.vertical_bits = _view_i32(c.vertical_bits, slots * words).view(slots, words)
         ix.slash_bits = _view_i32(c.slash_bits, slots * words).view(slots, words)
+        cw = (n + 63 + 31) // 32
+        ix.slash_cover = _view_i32(c.slash_cover, slots * cw).view(slots, cw)
         return ix
 
 

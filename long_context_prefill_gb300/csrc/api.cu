@@ -191,6 +191,7 @@ msa_status attention(const msa_shape& s, const void* q, const void* k, const voi
   a.d = s.d_h;
   a.T = ceil_div(s.n, 128);
   a.scale_log2 = effective_scale(s) * 1.4426950408889634f;
+  a.q = q;
   a.k = k;
   a.v = v;
   a.o = o;
@@ -248,13 +249,16 @@ msa_status msa_attn_vs(const msa_shape* shape, const void* q, const void* k, con
   if (!index) return MSA_ERR_INVALID_ARG;
   MSA_TRY(check_ptr4(index->vertical_bits, true));
   MSA_TRY(check_ptr4(index->slash_bits, true));
+  MSA_TRY(check_ptr4(index->slash_cover, true));
   std::vector<Unit> units;
   vs_units(*shape, heads, n_heads, 0, n_heads, units);
   AttnArgs a;
   memset(&a, 0, sizeof(a));
   a.vs_dbits = index->slash_bits;
   a.vs_cbits = index->vertical_bits;
+  a.vs_cover = index->slash_cover;
   a.vs_words = ceil_div(shape->n, 32);
+  a.vs_cover_words = ceil_div(shape->n + 63, 32);
   return attention(*shape, q, k, v, o, lse, edges, units, a, (cudaStream_t)stream);
 }
 

@@ -6,18 +6,20 @@
 // item, o_i = Σ_{j in N(i)} e^{s_ij} v_j / Σ_{j in N(i)} e^{s_ij}.
 //
 // One CTA processes one item: 128 query rows (two 64-row halves) of one KV
-// group against a stream of 128-key tiles that a pattern iterator generates:
-//   warp 4     producer: builds each tile's descriptor (key segments and
-//              per-half validity masks), TMA-loads Q once and K/V per tile
-//              (two 64-row segments per tile, any start row), or gathers
-//              single columns with vector loads (Vertical-Slash columns);
-//   warp 5     MMA issuer (one thread): S = Q K^T into TMEM (double
-//              buffered), then O += P V into a TMEM accumulator;
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r); masks S
-//              (causal, pattern, sequence end) before the max, keeps the
-//              running max/denominator, writes P (bf16) to shared memory for
-//              the PV MMA, rescales O in TMEM only when the max grows by more
-//              than 2^8, and writes the normalised output.
+// group against a stream of 128-key tiles that a pattern iterator generates.
+//   warp 8     producer: builds each tile's descriptor (two 64-key segments
+//              and per-half validity masks) and TMA-loads the K and V
+//              segments (any start row), or gathers single key rows
+//              (Vertical-Slash columns) with cp.async;
+//   warp 9     MMA issuer (one thread): S = Q K^T into TMEM (two buffers),
+//              then O += P V into a TMEM accumulator; Q and P are read from
+//              TMEM, K and V from shared memory;
+//   warps 0-7  softmax: query row r is TMEM lane r; warps w and w+4 share
+//              the lanes of quarter w and split the 128 keys (and the O
+//              columns) in halves, exchanging the row max through shared
+//              memory.  Masks (causal, pattern, sequence end) are applied
+//              before the max; O is rescaled in TMEM only when the max grows
+//              by more than 2^8; P is written to TMEM as bf16 pairs.
 // Every (i, j) pair enters the softmax at most once: tiles partition the keys
 // of an item, and masks drop what lies outside N(i) (MInference page §3.2 and
 // §5.1 "boundary masks": set to -inf before the max).
@@ -30,12 +32,15 @@ namespace msa {
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kStages = 2;
+constexpr int kSoftWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 32 * (kSoftWarps + 2);
+constexpr int kStages = 3;
 constexpr int kDescSlots = 4;
 constexpr uint32_t kTmemCols = 512;
+// TMEM columns: two S buffers, the O accumulator, Q and P (bf16 pairs)
+constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384, kColP = 448;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct TileDesc {
@@ -58,19 +63,20 @@ enum {
   kBarPEmpty = kBarPFull + 1,
   kBarDFull = kBarPEmpty + 1,
   kBarDEmpty = kBarDFull + kDescSlots,
-  kNumBars = kBarDEmpty + kDescSlots
+  kBarX = kBarDEmpty + kDescSlots,  // row exchange of the two warps of each quarter
+  kNumBars = kBarX + 4
 };
 
 template <int D>
 struct Layout {
-  static constexpr int kTile = 128 * D * 2;  // 128 rows of d_h bf16
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;
+  static constexpr int kTile = 128 * D * 2;  // 128 key rows of d_h bf16
+  static constexpr int kK = 0;
   static constexpr int kV = kK + kStages * kTile;
-  static constexpr int kP = kV + kStages * kTile;
-  static constexpr int kDesc = kP + 128 * 128 * 2;
+  static constexpr int kDesc = kV + kStages * kTile;
   static constexpr int kStage = kDesc + kDescSlots * (int)sizeof(TileDesc);  // gather staging (256 ints)
-  static constexpr int kBars = kStage + 256 * 4;
+  // row exchange: [2 parities][2 key halves][128] maxima, then [2][128] denominators
+  static constexpr int kXchg = kStage + 256 * 4;
+  static constexpr int kBars = kXchg + 6 * 128 * 4;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 64;
   // > 113 KB keeps one CTA per SM, so the 512-column TMEM allocation never waits.
@@ -90,6 +96,11 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint64_t low_mask64(int c) {  // bits [0, c), c clamped to [0, 64]
   c = c < 0 ? 0 : (c > 64 ? 64 : c);
   return c >= 64 ? ~0ull : ((1ull << c) - 1ull);
+}
+
+__device__ __forceinline__ uint32_t low_mask32(int c) {
+  c = c < 0 ? 0 : (c > 32 ? 32 : c);
+  return c >= 32 ? 0xFFFFFFFFu : ((1u << c) - 1u);
 }
 
 // Any bit of `bits` (an n-bit map) set in [lo, hi] ∩ [0, n)?
@@ -124,6 +135,18 @@ __device__ __forceinline__ int bits_count(const uint32_t* bits, int n, int lo, i
 
 __device__ __forceinline__ bool bit_at(const uint32_t* bits, int j) { return (__ldg(bits + (j >> 5)) >> (j & 31)) & 1u; }
 
+// 32 bits of an nw-word map starting at bit p >= 0 (bits past the end read 0).
+__device__ __forceinline__ uint32_t bits_window32(const uint32_t* bits, int nw, int p) {
+  const int w = p >> 5, sh = p & 31;
+  const uint32_t lo = w < nw ? __ldg(bits + w) : 0u;
+  const uint32_t hi = (w + 1) < nw ? __ldg(bits + w + 1) : 0u;
+  return __funnelshift_r(lo, hi, sh);
+}
+
+__device__ __forceinline__ uint32_t keys_below(int base, int limit) {  // bits k with base + k < limit
+  return low_mask32(limit - base);
+}
+
 // ------------------------------------------------------------------ item geometry
 struct Item {
   int row0[2];   // first query row of each half
@@ -149,20 +172,19 @@ __device__ __forceinline__ Item make_item(const Unit& U, int t, int n) {
 // The key ranges [0, g) and [a0-w+1, a0+127] (merged when they touch) are cut
 // into 128-key tiles; a per-tile row rule applies the exact set.
 struct AshapeIter {
-  int nr;
   int lo[2], hi[2], rule[2], tiles[2];
   __device__ void init(const Unit& U, const Item& it, int n) {
     const int hi_key = min(it.a0 + 127, n - 1);
     const int g = U.sink, w = U.window;
     const int sw = max(0, it.a0 - w + 1);
     if (sw <= g) {
-      nr = 1; lo[0] = 0; hi[0] = hi_key; rule[0] = 3;
+      lo[0] = 0; hi[0] = hi_key; rule[0] = 3;
+      lo[1] = 0; hi[1] = -1; rule[1] = 0;
     } else {
-      nr = 2;
       lo[0] = 0; hi[0] = min(g, n) - 1; rule[0] = 1;
       lo[1] = sw; hi[1] = hi_key; rule[1] = 2;
     }
-    for (int r = 0; r < 2; ++r) tiles[r] = (r < nr && hi[r] >= lo[r]) ? (hi[r] - lo[r] + 128) / 128 : 0;
+    for (int r = 0; r < 2; ++r) tiles[r] = hi[r] >= lo[r] ? (hi[r] - lo[r] + 128) / 128 : 0;
   }
   __device__ int count() const { return tiles[0] + tiles[1]; }
   __device__ void emit(int j, int n, TileDesc& d) const {
@@ -173,9 +195,7 @@ struct AshapeIter {
     d.kind = 0;
     d.rule = rule[r];
     for (int w = 0; w < 4; ++w) {
-      const int base = t0 + 32 * w;
-      const int c = n - base;  // keys below n
-      const uint32_t m = c >= 32 ? 0xFFFFFFFFu : (c <= 0 ? 0u : ((1u << c) - 1u));
+      const uint32_t m = keys_below(t0 + 32 * w, n);
       d.mask[0][w] = m;
       d.mask[1][w] = m;
     }
@@ -206,7 +226,6 @@ struct BlockIter {
         cnt[h] = 0;
       }
     }
-    // size of the union
     int x = 0, y = 0, m = 0;
     while (x < cnt[0] || y < cnt[1]) {
       const int vx = x < cnt[0] ? __ldg(J[0] + x) : 0x7FFFFFFF;
@@ -220,7 +239,6 @@ struct BlockIter {
     last = -1;
   }
   __device__ int count() const { return (total + 1) / 2; }
-  // Next block of the union with its membership bits; false at the end.
   __device__ bool next_block(int& v, int& bits) {
     if (p[0] >= cnt[0] && p[1] >= cnt[1]) return false;
     const int vx = p[0] < cnt[0] ? __ldg(J[0] + p[0]) : 0x7FFFFFFF;
@@ -240,7 +258,6 @@ struct BlockIter {
     int vs[2] = {v0, v1}, bs[2] = {b0, b1};
     for (int s = 0; s < 2; ++s) {
       if (bs[s] < 0) { bs[s] = 0; set_error(err, kErrIndex); }
-      // a block must be causal for the half that keeps it
       for (int h = 0; h < 2; ++h)
         if ((bs[s] >> h & 1) && (vs[s] < 0 || vs[s] > u[h])) { bs[s] &= ~(1 << h); set_error(err, kErrIndex); }
       if (vs[s] < 0 || 64 * vs[s] >= n) { vs[s] = 0; bs[s] = 0; }
@@ -250,9 +267,7 @@ struct BlockIter {
     for (int s = 0; s < 2; ++s) {
       d.seg[s] = 64 * vs[s];
       for (int w = 0; w < 2; ++w) {
-        const int base = 64 * vs[s] + 32 * w;
-        const int c = n - base;
-        const uint32_t m = c >= 32 ? 0xFFFFFFFFu : (c <= 0 ? 0u : ((1u << c) - 1u));
+        const uint32_t m = keys_below(64 * vs[s] + 32 * w, n);
         d.mask[0][2 * s + w] = (bs[s] & 1) ? m : 0u;
         d.mask[1][2 * s + w] = (bs[s] & 2) ? m : 0u;
       }
@@ -263,21 +278,27 @@ struct BlockIter {
 // ------------------------------------------------------------------ Vertical-Slash tiles
 // Physical set of row i in query block [a, e] (MInference page §2.1 and §4.1):
 // keys covered by some slash tile [a-δ, e-δ] (δ in D), plus the vertical
-// columns C, restricted to j <= i.  Key j is covered by a slash tile of the
-// block iff D has an offset in [a-j, e-j].  Aligned 128-key windows that some
-// slash tile touches become range tiles whose masks include the verticals in
-// them; verticals in the other windows are gathered into column tiles.
+// columns C, restricted to j <= i.  For a full block, key j is covered iff bit
+// n-1-a+j of the dilated coverage map is set, so a tile's mask is a 128-bit
+// window of that map.  Aligned 128-key windows that some slash tile touches
+// become range tiles whose masks include the verticals in them; verticals in
+// the other windows are gathered into column tiles.
 struct VSIter {
   const uint32_t* dbits;
   const uint32_t* cbits;
+  const uint32_t* cover;
+  int cw;  // cover words
   int n, M, hi_key;
   int a[2], e[2], L[2], ex[2];
-  int m;       // window cursor
-  int staged;  // columns waiting in the staging list
+  int grp;                // first window of the current 32-window group
+  uint32_t smask, cmask;  // group windows with slash coverage / with only columns
+  int staged;             // columns waiting in the staging list
   __device__ void init(const Unit& U, const Item& it, const AttnArgs& A) {
     n = A.n;
     dbits = A.vs_dbits + (int64_t)U.slot[0] * A.vs_words;
     cbits = A.vs_cbits + (int64_t)U.slot[0] * A.vs_words;
+    cover = A.vs_cover + (int64_t)U.slot[0] * A.vs_cover_words;
+    cw = A.vs_cover_words;
     hi_key = min(it.a0 + 127, n - 1);
     M = hi_key / 128 + 1;
     for (int h = 0; h < 2; ++h) {
@@ -286,19 +307,20 @@ struct VSIter {
       ex[h] = it.exists[h];
       L[h] = e[h] - a[h] + 1;
     }
-    m = 0;
+    grp = -32;
+    smask = cmask = 0u;
     staged = 0;
   }
-  __device__ bool window_has_slash(int w) const {
+  // Keys of window w covered by a slash tile of half h?
+  __device__ bool half_has_slash(int h, int w) const {
+    if (!ex[h]) return false;
     const int j0 = 128 * w;
-    for (int h = 0; h < 2; ++h) {
-      if (!ex[h]) continue;
-      const int jhi = min(j0 + 127, e[h]);
-      if (j0 > jhi) continue;
-      if (bits_any(dbits, n, a[h] - jhi, a[h] - j0 + L[h] - 1)) return true;
-    }
-    return false;
+    const int jhi = min(j0 + 127, e[h]);
+    if (j0 > jhi) return false;
+    if (L[h] == 64) return bits_any(cover, 32 * cw, n - 1 - a[h] + j0, n - 1 - a[h] + jhi);
+    return bits_any(dbits, n, a[h] - jhi, a[h] - j0 + L[h] - 1);
   }
+  __device__ bool window_has_slash(int w) const { return half_has_slash(0, w) || half_has_slash(1, w); }
   // Tile count: windows with slash coverage, plus the columns of the others
   // packed 128 per tile.  Whole warp; result in every lane.
   __device__ int count(int lane) const {
@@ -313,15 +335,37 @@ struct VSIter {
     }
     return P + (G + 127) / 128;
   }
+  __device__ void load_group(int lane) {
+    grp += 32;
+    const int w = grp + lane;
+    bool s = false, c = false;
+    if (w < M) {
+      s = window_has_slash(w);
+      if (!s) c = bits_count(cbits, n, 128 * w, min(128 * w + 127, hi_key)) > 0;
+    }
+    smask = __ballot_sync(0xFFFFFFFFu, s);
+    cmask = __ballot_sync(0xFFFFFFFFu, c);
+  }
   __device__ void range_masks(int w, int lane, TileDesc& d) const {
     const int j0 = 128 * w;
     for (int h = 0; h < 2; ++h) {
-      for (int q = 0; q < 4; ++q) {
-        const int j = j0 + 32 * q + lane;
-        bool ok = false;
-        if (ex[h] && j <= e[h]) ok = bit_at(cbits, j) || bits_any(dbits, n, a[h] - j, a[h] - j + L[h] - 1);
-        const uint32_t b = __ballot_sync(0xFFFFFFFFu, ok);
-        if (lane == 0) d.mask[h][q] = b;
+      if (ex[h] && L[h] != 64) {  // partial last block: test each key (whole warp)
+        for (int q = 0; q < 4; ++q) {
+          const int j = j0 + 32 * q + lane;
+          const bool ok = j <= e[h] && (bit_at(cbits, j) || bits_any(dbits, n, a[h] - j, a[h] - j + L[h] - 1));
+          const uint32_t b = __ballot_sync(0xFFFFFFFFu, ok);
+          if (lane == 0) d.mask[h][q] = b;
+        }
+      } else if (lane == 0) {
+        for (int q = 0; q < 4; ++q) {
+          uint32_t m = 0u;
+          const int base = j0 + 32 * q;
+          if (ex[h] && base <= e[h]) {
+            m = bits_window32(cover, cw, n - 1 - a[h] + base) | __ldg(cbits + (base >> 5));
+            m &= keys_below(base, e[h] + 1);
+          }
+          d.mask[h][q] = m;
+        }
       }
     }
     if (lane == 0) { d.seg[0] = j0; d.seg[1] = j0 + 64; d.kind = 0; d.rule = 0; }
@@ -347,23 +391,35 @@ struct VSIter {
   // Produce the next tile into d (whole warp).
   __device__ void emit(int lane, int* stage, TileDesc& d) {
     for (;;) {
-      if (staged >= 128 || (m >= M && staged > 0)) { gather_tile(lane, stage, d); return; }
-      if (m >= M) {  // nothing left (cannot happen when the count was honoured): empty tile
-        if (lane == 0) { d.kind = 0; d.rule = 0; d.seg[0] = 0; d.seg[1] = 64; }
-        for (int h = 0; h < 2; ++h)
-          for (int q = 0; q < 4; ++q) if (lane == 0) d.mask[h][q] = 0u;
-        return;
+      if (staged >= 128) { gather_tile(lane, stage, d); return; }
+      if ((smask | cmask) == 0u) {
+        if (grp + 32 >= M) {
+          if (staged > 0) { gather_tile(lane, stage, d); return; }
+          // nothing left (cannot happen when the count was honoured): empty tile
+          if (lane == 0) {
+            d.kind = 0; d.rule = 0; d.seg[0] = 0; d.seg[1] = 64;
+            for (int h = 0; h < 2; ++h)
+              for (int q = 0; q < 4; ++q) d.mask[h][q] = 0u;
+          }
+          return;
+        }
+        load_group(lane);
+        continue;
       }
-      const int w = m++;
-      if (window_has_slash(w)) { range_masks(w, lane, d); return; }
+      const int b = __ffs(smask | cmask) - 1;
+      const bool is_slash = (smask >> b) & 1u;
+      smask &= ~(1u << b);
+      cmask &= ~(1u << b);
+      const int w = grp + b;
+      if (is_slash) { range_masks(w, lane, d); return; }
       // stage this window's columns (ascending)
       const int j0 = 128 * w;
       for (int q = 0; q < 4; ++q) {
         const int j = j0 + 32 * q + lane;
         const bool ok = j <= hi_key && bit_at(cbits, j);
-        const uint32_t b = __ballot_sync(0xFFFFFFFFu, ok);
-        if (ok) stage[staged + __popc(b & ((1u << lane) - 1u))] = j;
-        staged += __popc(b);
+        const uint32_t bb = __ballot_sync(0xFFFFFFFFu, ok);
+        if (ok) stage[staged + __popc(bb & ((1u << lane) - 1u))] = j;
+        staged += __popc(bb);
       }
       __syncwarp();
     }
@@ -373,15 +429,15 @@ struct VSIter {
 // ------------------------------------------------------------------ kernel
 template <int D, bool kCount>
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                       const __grid_constant__ CUtensorMap tv, const AttnArgs A,
-                       const __grid_constant__ UnitTable UT) {
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                       const AttnArgs A, const __grid_constant__ UnitTable UT) {
   using Ly = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::kBars);
   TileDesc* descs = reinterpret_cast<TileDesc*>(sm + Ly::kDesc);
   int* stage = reinterpret_cast<int*>(sm + Ly::kStage);
+  float* xchg = reinterpret_cast<float*>(sm + Ly::kXchg);
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + Ly::kMisc);  // [0] tmem, [1] tiles, [2] abort
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -400,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (threadIdx.x == 32 * kMmaWarp) {
-    mbar_init(&bars[kBarQ], 1);
+    mbar_init(&bars[kBarQ], kSoftWarps);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[kBarKFull + s], 1);
       mbar_init(&bars[kBarKEmpty + s], 1);
@@ -409,14 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kBarSFull + s], 1);
-      mbar_init(&bars[kBarSEmpty + s], 4);
+      mbar_init(&bars[kBarSEmpty + s], kSoftWarps);
     }
-    mbar_init(&bars[kBarPFull], 4);
+    mbar_init(&bars[kBarPFull], kSoftWarps);
     mbar_init(&bars[kBarPEmpty], 1);
     for (int s = 0; s < kDescSlots; ++s) {
       mbar_init(&bars[kBarDFull + s], 1);
-      mbar_init(&bars[kBarDEmpty + s], 4);
+      mbar_init(&bars[kBarDEmpty + s], kSoftWarps);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(&bars[kBarX + s], 64);
     misc[2] = 0;
     fence_mbar_init();
   }
@@ -433,22 +490,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = misc[0];
   const int T = (int)misc[1];
 
-  uint8_t* sQ = sm + Ly::kQ;
   uint8_t* sK = sm + Ly::kK;
   uint8_t* sV = sm + Ly::kV;
-  uint8_t* sP = sm + Ly::kP;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     bool ok = true;
-    if (lane == 0 && T > 0) {  // no tile, no copy: nothing may be in flight when the CTA exits
-      tma_prefetch_desc(&tq);
+    if (lane == 0 && T > 0) {
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_arrive_expect_tx(&bars[kBarQ], Ly::kTile);
-      for (int h = 0; h < 2; ++h)
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sQ + c * 16384 + h * 8192, &tq, &bars[kBarQ], 64 * c, it.row0[h], U.qh[h]);
     }
     auto load_kv = [&](int j, bool is_v) -> bool {
       const int st = j % kStages;
@@ -458,24 +508,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(empty, ph)) return false;
       const TileDesc& d = descs[j % kDescSlots];
       uint8_t* dst = (is_v ? sV : sK) + st * Ly::kTile;
-      const CUtensorMap* map = is_v ? &tv : &tk;
       if (d.kind == 0) {
         if (lane == 0) {
+          const CUtensorMap* map = is_v ? &tv : &tk;
           mbar_arrive_expect_tx(full, Ly::kTile);
           for (int s = 0; s < 2; ++s)
             for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384 + s * 8192, map, full, 64 * c, d.seg[s], U.kvh);
         }
       } else {
-        // gather single key rows with 16-byte loads into the swizzled layout
-        constexpr int kChunks16 = D / 8;  // 16-byte chunks per row
+        // gather single key rows (16-byte cp.async) into the swizzled layout
+        constexpr int kChunks16 = D / 8;
         const uint8_t* gbase = reinterpret_cast<const uint8_t*>(is_v ? A.v : A.k) + (int64_t)U.kvh * n * D * 2;
         for (int idx = lane; idx < 128 * kChunks16; idx += 32) {
           const int r = idx / kChunks16, c16 = idx % kChunks16;
           int key = d.gidx[r];
           key = key < 0 ? 0 : key;  // empty columns reload key 0 (finite data, masked)
-          const uint4 val = __ldg(reinterpret_cast<const uint4*>(gbase + (int64_t)key * D * 2) + c16);
-          *reinterpret_cast<uint4*>(dst + (c16 >> 3) * 16384 + sw128_offset(r, c16 & 7)) = val;
+          cp_async16(dst + (c16 >> 3) * 16384 + sw128_offset(r, c16 & 7), gbase + ((int64_t)key * D + 8 * c16) * 2);
         }
+        cp_async_wait_all();
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(full);
@@ -507,7 +557,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && T > 0) {
       bool ok = mbar_wait(&bars[kBarQ], 0);
-      const uint32_t q0 = smem_u32(sQ), p0 = smem_u32(sP);
       constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
       auto pv = [&](int j) -> bool {
@@ -517,15 +566,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t v0 = smem_u32(sV + st * Ly::kTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc_sw128(p0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(v0 + kk * 2048, 16384, 1024);
-          mma_bf16_ss(tmem + 256, ad, bd, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * kk, sdesc_sw128(v0 + kk * 2048, 16384, 1024), id_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kBarVEmpty + st]);
         mma_commit(&bars[kBarPEmpty]);
         return true;
       };
+      if (ok) tc_fence_after();
       for (int j = 0; ok && j < T; ++j) {
         if (misc[2]) { ok = false; break; }
         const int st = j % kStages, sb = j & 1;
@@ -537,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + 128 * sb, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024), id_qk,
+          mma_bf16_ts(tmem + kColS + 128 * sb, tmem + kColQ + 8 * kk, sdesc_sw128(k0 + off, 16, 1024), id_qk,
                       kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars[kBarSFull + sb]);
@@ -550,146 +598,168 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int r = threadIdx.x;  // 0..127 = TMEM lane = tile row
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter ..
+    const int ch = warp >> 2;              // key half of each tile (and O / Q column half)
+    const int r = quarter * 32 + lane;     // tile row = TMEM lane
     const int h = r >> 6;
     const int i = it.row0[h] + (r & 63);
     const bool row_ok = i < n;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float c2 = A.scale_log2;
     const int g = U.sink, wnd = U.window;
+    uint64_t* xbar = &bars[kBarX + quarter];  // warps quarter and quarter+4, one phase per exchange
     float m_used = -INFINITY, l = 0.f;
     unsigned long long count = 0;
     bool ok = true;
+
+    // ---- Q row into TMEM (A operand of S = Q K^T): 32 columns of bf16 pairs per writer
+    if (T > 0) {
+      if (D == 128 || ch == 0) {
+        const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(A.q) + ((int64_t)U.qh[h] * n + i) * D;
+        const int e0 = D == 128 ? ch * 64 : 0;
+        uint32_t qw[32];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          uint4 v4 = make_uint4(0, 0, 0, 0);
+          if (row_ok) v4 = __ldg(reinterpret_cast<const uint4*>(qrow + e0) + x);
+          qw[4 * x] = v4.x; qw[4 * x + 1] = v4.y; qw[4 * x + 2] = v4.z; qw[4 * x + 3] = v4.w;
+        }
+        tmem_st32(tmem + lane_base + kColQ + (D == 128 ? 32 * ch : 0), qw);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarQ]);
+    }
+
     for (int j = 0; j < T; ++j) {
       if (misc[2]) { ok = false; break; }
-      // ---- tile descriptor -> validity words for this row
+      // ---- tile descriptor -> validity word of this thread's 64 keys
       const int slot = j % kDescSlots;
       if (!mbar_wait(&bars[kBarDFull + slot], (j / kDescSlots) & 1)) { ok = false; break; }
       const TileDesc& d = descs[slot];
-      uint64_t vw0, vw1;
-      if (!row_ok) {
-        vw0 = vw1 = 0ull;
-      } else if (d.kind == 0) {
-        uint64_t v[2];
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const int base = d.seg[s];
-          uint64_t m64 = ((uint64_t)d.mask[h][2 * s + 1] << 32) | d.mask[h][2 * s];
-          m64 &= low_mask64(i - base + 1);  // causal: j <= i
+      uint64_t vw = 0ull;
+      if (row_ok) {
+        const uint64_t m64 = ((uint64_t)d.mask[h][2 * ch + 1] << 32) | d.mask[h][2 * ch];
+        if (d.kind == 0) {
+          const int base = d.seg[ch];
+          vw = m64 & low_mask64(i - base + 1);  // causal: j <= i
           if (d.rule) {
             uint64_t keep = 0;
             if (d.rule & 1) keep |= low_mask64(g - base);             // j < g
             if (d.rule & 2) keep |= ~low_mask64(i - wnd + 1 - base);  // j > i - w
-            m64 &= keep;
+            vw &= keep;
           }
-          v[s] = m64;
+        } else {
+          for (int k = 0; k < 64; ++k) {
+            const int gj = d.gidx[64 * ch + k];
+            if (((m64 >> k) & 1ull) && gj >= 0 && gj <= i) vw |= 1ull << k;
+          }
         }
-        vw0 = v[0];
-        vw1 = v[1];
-      } else {
-        uint64_t v[2] = {0ull, 0ull};
-        for (int k = 0; k < 128; ++k) {
-          const int gj = d.gidx[k];
-          const bool bit = ((d.mask[h][k >> 5] >> (k & 31)) & 1u) && gj >= 0 && gj <= i;
-          v[k >> 6] |= (uint64_t)bit << (k & 63);
-        }
-        vw0 = v[0];
-        vw1 = v[1];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarDEmpty + slot]);
-      if (kCount) count += __popcll(vw0) + __popcll(vw1);
+      if (kCount) count += __popcll(vw);
 
-      // ---- S tile from TMEM
+      // ---- S tile (this thread's 64 keys) from TMEM
       const int sb = j & 1;
       if (!mbar_wait(&bars[kBarSFull + sb], (j >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      float sv[128];
+      float sv[64];
       {
-        uint32_t* u = reinterpret_cast<uint32_t*>(sv);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + 128 * sb + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(u + 32 * c));
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tmem + lane_base + kColS + 128 * sb + 64 * ch, u0);
+        tmem_ld32(tmem + lane_base + kColS + 128 * sb + 64 * ch + 32, u1);
         tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          sv[k] = __uint_as_float(u0[k]);
+          sv[32 + k] = __uint_as_float(u1[k]);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarSEmpty + sb]);
 
-      // ---- mask, max
-      if (~vw0 | ~vw1) {
+      // ---- mask, row max (tree), exchanged with the partner warp
+      if (~vw) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) sv[k] = ((vw0 >> k) & 1ull) ? sv[k] : -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 64; ++k) sv[64 + k] = ((vw1 >> k) & 1ull) ? sv[64 + k] : -INFINITY;
+        for (int k = 0; k < 64; ++k) sv[k] = ((vw >> k) & 1ull) ? sv[k] : -INFINITY;
       }
-      float mt = sv[0];
+      float mx[8];
 #pragma unroll
-      for (int k = 1; k < 128; ++k) mt = fmaxf(mt, sv[k]);
+      for (int x = 0; x < 8; ++x) mx[x] = fmaxf(sv[x], sv[x + 8]);
+#pragma unroll
+      for (int k = 16; k < 64; k += 8)
+#pragma unroll
+        for (int x = 0; x < 8; ++x) mx[x] = fmaxf(mx[x], sv[k + x]);
+      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      float* xc = xchg + (j & 1) * 256;
+      xc[ch * 128 + r] = mt;
+      mbar_arrive(xbar);
+      if (!mbar_wait(xbar, j & 1)) { ok = false; break; }
+      mt = fmaxf(mt, xc[(ch ^ 1) * 128 + r]);
+
       const float m_new = fmaxf(m_used, mt * c2);
       const bool need = m_new > m_used + kRescaleThreshold;
-      const bool any = __any_sync(0xFFFFFFFFu, need);
+      const bool any = __any_sync(0xFFFFFFFFu, need);  // the partner warp sees the same rows
       float alpha = 1.f;
       if (any && m_new != -INFINITY) {
         alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_new);
         m_used = m_new;
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      float rs = 0.f;
-      uint32_t pk[64];
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[32];
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
+      for (int k = 0; k < 32; ++k) {
         const float p0 = ex2(fmaf(sv[2 * k], c2, -mref));
         const float p1 = ex2(fmaf(sv[2 * k + 1], c2, -mref));
-        rs += p0 + p1;
+        rs[k & 3] += p0 + p1;
         pk[k] = pack_bf16x2(p0, p1);
       }
-      l = l * alpha + rs;
+      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
 
       // ---- PV(j-1) must be done before P is overwritten or O is rescaled
       if (j > 0 && !mbar_wait(&bars[kBarPEmpty], (j - 1) & 1)) { ok = false; break; }
+      tc_fence_after();
       if (any && j > 0) {
-        tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_base + 256 + 32 * c, o);
+          const uint32_t col = kColO + (D / 2) * ch + 32 * c;
+          tmem_ld32(tmem + lane_base + col, o);
           tmem_ld_wait();
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-          tmem_st32(tmem + lane_base + 256 + 32 * c, o);
+          tmem_st32(tmem + lane_base + col, o);
         }
-        tmem_st_wait();
       }
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const int k = 32 * c + 4 * cc;
-          const uint32_t addr = smem_u32(sP + c * 16384 + sw128_offset(r, cc));
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[k]), "r"(pk[k + 1]),
-                       "r"(pk[k + 2]), "r"(pk[k + 3])
-                       : "memory");
-        }
-      fence_proxy_async_smem();
+      tmem_st32(tmem + lane_base + kColP + 32 * ch, pk);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarPFull]);
     }
     if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
 
-    // ---- epilogue: O / l, LSE
+    // ---- epilogue: O / l, LSE (the pair adds its partial denominators)
     const int qh = U.qh[h];
     if (ok && T > 0) {
       if (!mbar_wait(&bars[kBarPEmpty], (T - 1) & 1)) { ok = false; misc[2] = 1; set_error(A.err, kErrTimeout); }
       tc_fence_after();
     }
+    xchg[512 + ch * 128 + r] = l;
+    mbar_arrive(xbar);
+    if (!mbar_wait(xbar, T & 1)) { ok = false; misc[2] = 1; set_error(A.err, kErrTimeout); }
+    l += xchg[512 + (ch ^ 1) * 128 + r];
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(A.o) + ((int64_t)qh * n + i) * D;
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(A.o) + ((int64_t)qh * n + i) * D + (D / 2) * ch;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < D / 64; ++c) {
       uint32_t o[32];
       if (ok && T > 0) {
-        tmem_ld32(tmem + lane_base + 256 + 32 * c, o);
+        tmem_ld32(tmem + lane_base + kColO + (D / 2) * ch + 32 * c, o);
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -705,7 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 4; ++x) dst[x] = make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
       }
     }
-    if (row_ok && A.lse) A.lse[(int64_t)qh * n + i] = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    if (row_ok && A.lse && ch == 0)
+      A.lse[(int64_t)qh * n + i] = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     if (kCount && A.edges) {
       unsigned long long c = count;
       for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
@@ -722,8 +793,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, bool kCount>
-msa_status launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
-                       const UnitTable& ut, cudaStream_t stream) {
+msa_status launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, const UnitTable& ut,
+                       cudaStream_t stream) {
   auto kern = sparse_attn_kernel<D, kCount>;
   const int smem = Layout<D>::kAlloc;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -731,7 +802,7 @@ msa_status launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   const int64_t items = (int64_t)a.T * a.n_units;
   if (items <= 0) return MSA_OK;
   if (items > 0x7FFFFFFF) return MSA_ERR_UNSUPPORTED;
-  kern<<<(unsigned)items, kThreads, smem, stream>>>(tq, tk, tv, a, ut);
+  kern<<<(unsigned)items, kThreads, smem, stream>>>(tk, tv, a, ut);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
@@ -740,6 +811,7 @@ msa_status launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 
 msa_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const AttnArgs& args, const Unit* units, int n_units, cudaStream_t stream) {
+  (void)tq;  // Q rows are read by the softmax warps straight into TMEM
   for (int base = 0; base < n_units; base += kMaxUnits) {
     UnitTable ut;
     const int cnt = n_units - base < kMaxUnits ? n_units - base : kMaxUnits;
@@ -748,8 +820,10 @@ msa_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const 
     a.n_units = cnt;
     msa_status st;
     const bool count = args.edges != nullptr;
-    if (args.d == 128) st = count ? launch_impl<128, true>(tq, tk, tv, a, ut, stream) : launch_impl<128, false>(tq, tk, tv, a, ut, stream);
-    else st = count ? launch_impl<64, true>(tq, tk, tv, a, ut, stream) : launch_impl<64, false>(tq, tk, tv, a, ut, stream);
+    if (args.d == 128)
+      st = count ? launch_impl<128, true>(tk, tv, a, ut, stream) : launch_impl<128, false>(tk, tv, a, ut, stream);
+    else
+      st = count ? launch_impl<64, true>(tk, tv, a, ut, stream) : launch_impl<64, false>(tk, tv, a, ut, stream);
     if (st != MSA_OK) return st;
   }
   return MSA_OK;

@@ -44,6 +44,7 @@ struct UnitTable {
 struct AttnArgs {
   int32_t n, d, T, n_units;
   float scale_log2;  // scale * log2(e)
+  const void* q;     // bf16 [B*Hq, n, d] (rows loaded into TMEM)
   const void* k;     // bf16 [B*Hkv, n, d] (column gathers)
   const void* v;
   void* o;           // bf16 [B*Hq, n, d]
@@ -52,7 +53,8 @@ struct AttnArgs {
   // Vertical-Slash index (slot-indexed)
   const uint32_t* vs_dbits;  // [slots, words] bit δ of D
   const uint32_t* vs_cbits;  // [slots, words] bit j of C
-  int32_t vs_words;
+  const uint32_t* vs_cover;  // [slots, cover_words] dilated slash coverage (see msa_vs_index)
+  int32_t vs_words, vs_cover_words;
   // Block-Sparse index
   const int32_t* bs_idx;  // [slots, N_b, topk]
   const int32_t* bs_cnt;  // [slots, N_b]

@@ -104,6 +104,7 @@ static msa_status plan_layer(const msa_shape& s, const msa_head_cfg* table, void
     P.vs.slash_cnt = c.take<int32_t>((size_t)slots);
     P.vs.vertical_bits = c.take<uint32_t>((size_t)(slots * P.words));
     P.vs.slash_bits = c.take<uint32_t>((size_t)(slots * P.words));
+    P.vs.slash_cover = c.take<uint32_t>((size_t)(slots * ceil_div(s.n + 63, 32)));
     P.vs_ws_bytes = vs_index_ws_bytes(s, P.vs_cfg, (int32_t)P.vs_heads.size());
     P.vs_ws = c.take<uint8_t>(P.vs_ws_bytes);
   }
@@ -221,7 +222,9 @@ static msa_status layer_attend(const msa_shape& s, const void* q, const void* k,
   memset(&a, 0, sizeof(a));
   a.vs_dbits = W.vs.slash_bits;
   a.vs_cbits = W.vs.vertical_bits;
+  a.vs_cover = W.vs.slash_cover;
   a.vs_words = W.words;
+  a.vs_cover_words = ceil_div(s.n + 63, 32);
   a.bs_idx = W.bs_idx;
   a.bs_cnt = W.bs_cnt;
   a.bs_topk = W.bs_heads.empty() ? 1 : W.bs_cfg.topk;

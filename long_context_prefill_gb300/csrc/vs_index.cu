@@ -568,6 +568,33 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs args,
   if (threadIdx.x == 0) *J.cnt = base_sel < k ? base_sel : k;
 }
 
+// Dilated slash coverage: bit z = any offset of D in [n-1-z, n+62-z], z < n+63.
+// One thread per output bit, words assembled with a warp ballot.
+__global__ void slash_cover_kernel(const uint32_t* dbits, int n, int words, int cover_words, int slots,
+                                   uint32_t* cover) {
+  const int64_t total = (int64_t)slots * cover_words * 32;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t slot = idx / ((int64_t)cover_words * 32);
+    const int z = (int)(idx % ((int64_t)cover_words * 32));
+    const uint32_t* D = dbits + slot * words;
+    bool any = false;
+    if (z < n + 63) {
+      int lo = n - 1 - z, hi = n + 62 - z;
+      lo = lo < 0 ? 0 : lo;
+      hi = hi > n - 1 ? n - 1 : hi;
+      for (int w = lo >> 5; w <= (hi >> 5) && lo <= hi; ++w) {
+        uint32_t x = D[w];
+        if (w == (lo >> 5)) x &= 0xFFFFFFFFu << (lo & 31);
+        if (w == (hi >> 5)) x &= 0xFFFFFFFFu >> (31 - (hi & 31));
+        if (x) { any = true; break; }
+      }
+    }
+    const unsigned b = __ballot_sync(0xFFFFFFFFu, any);
+    if ((threadIdx.x & 31) == 0) cover[slot * cover_words + z / 32] = b;
+  }
+}
+
 // ------------------------------------------------------------------ per-block expansion
 // One thread per query block u: merged slash ranges [a-δ, e-δ] ∩ [0, e] in
 // ascending order (δ descending), then the verticals c <= e outside them.
@@ -738,7 +765,8 @@ msa_status run_vs_index(const msa_shape& s, const void* q, const void* k, const 
                         const msa_head_cfg& cfg, const msa_vs_index& out, void* ws, size_t ws_bytes,
                         cudaStream_t stream) {
   if (cfg.last_q > 128) return MSA_ERR_UNSUPPORTED;
-  if (!out.vertical || !out.vertical_cnt || !out.slash || !out.slash_cnt || !out.vertical_bits || !out.slash_bits)
+  if (!out.vertical || !out.vertical_cnt || !out.slash || !out.slash_cnt || !out.vertical_bits || !out.slash_bits ||
+      !out.slash_cover)
     return MSA_ERR_INVALID_ARG;
   const int vcap = cfg.n_vertical < s.n ? cfg.n_vertical : s.n;
   const int scap = cfg.n_slash < s.n ? cfg.n_slash : s.n;
@@ -796,6 +824,15 @@ msa_status run_vs_index(const msa_shape& s, const void* q, const void* k, const 
   ta.sk = scap;
   topk_kernel<<<(unsigned)(P.slots * 2), kTopkThreads, 0, stream>>>(ta, s.n);
   note_launch();
+  if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+  {
+    const int words = ceil_div(s.n, 32);
+    const int cw = ceil_div(s.n + 63, 32);
+    const int64_t threads = (int64_t)P.slots * cw * 32;
+    const int blocks = (int)((threads + 255) / 256 < 8192 ? (threads + 255) / 256 : 8192);
+    slash_cover_kernel<<<blocks, 256, 0, stream>>>(out.slash_bits, s.n, words, cw, P.slots, out.slash_cover);
+    note_launch();
+  }
   if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   return MSA_OK;
 }

@@ -4,7 +4,7 @@ import math
 import numpy as np
 import torch
 
-import oracle
+import oracle  # noqa: F401  (test-side helpers only)
 
 # Output tolerance: bf16 inputs, fp32 accumulation, bf16 output, against the
 # fp64 oracle (max-abs and mean-abs over the compared rows).
@@ -49,6 +49,19 @@ def pack_bits(idx, n) -> np.ndarray:
     for j in np.asarray(idx, dtype=np.int64).reshape(-1):
         words[j >> 5] |= np.uint32(1) << np.uint32(j & 31)
     return words.view(np.int32)
+
+
+def cover_bits(D, n) -> np.ndarray:
+    """The index's dilated slash-coverage map (msa_vs_index.slash_cover): bit z
+    set iff D holds an offset in [n-1-z, n+62-z], z < n+63."""
+    Dset = np.zeros(n, dtype=bool)
+    Dset[np.asarray(D, dtype=np.int64)] = True
+    pre = np.concatenate([[0], np.cumsum(Dset)])
+    z = np.arange(n + 63)
+    lo = np.clip(n - 1 - z, 0, n - 1)
+    hi = np.clip(n + 62 - z, -1, n - 1)
+    has = (hi >= lo) & ((pre[hi + 1] - pre[lo]) > 0)
+    return pack_bits(np.nonzero(has)[0], n + 63)
 
 
 def unpack_bits(words, n) -> np.ndarray:

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import synth
-from helpers import compare_rows, f32, head_qkv, pack_bits, scale_of
+from helpers import compare_rows, cover_bits, f32, head_qkv, pack_bits, scale_of
 
 pytestmark = pytest.mark.gpu
 
@@ -98,6 +98,7 @@ def _vs_case(msa, n, d, C, D, seed, Hq=2, Hkv=1):
     for h in range(Hq):
         index.vertical_bits[h] = torch.from_numpy(pack_bits(C[h], n)).cuda()
         index.slash_bits[h] = torch.from_numpy(pack_bits(D[h], n)).cuda()
+        index.slash_cover[h] = torch.from_numpy(cover_bits(D[h], n)).cuda()
     o = torch.zeros_like(q)
     lse = torch.empty(1, Hq, n, device="cuda")
     edges = torch.zeros(Hq, dtype=torch.int64, device="cuda")

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from helpers import f32, head_qkv, unpack_bits
+from helpers import cover_bits, f32, head_qkv, unpack_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +52,7 @@ def check_vs_against_oracle(idx, q, k, heads, last_q, v, s, exact=False):
             # bitmaps agree with the lists
             assert np.array_equal(unpack_bits(idx.vertical_bits[slot].cpu().numpy(), n), np.sort(gC))
             assert np.array_equal(unpack_bits(idx.slash_bits[slot].cpu().numpy(), n), np.sort(gD))
+            assert np.array_equal(idx.slash_cover[slot].cpu().numpy(), cover_bits(gD, n))
             if exact:
                 assert set(gC.tolist()) == set(C.tolist()) and set(gD.tolist()) == set(D.tolist())
             else:
