@@ -7,10 +7,12 @@
 //
 // One CTA processes one item: 128 query rows (two 64-row halves) of one KV
 // group against a stream of 128-key tiles that a pattern iterator generates.
-//   warp 8     producer: builds each tile's descriptor (two 64-key segments
-//              and per-half validity masks) and TMA-loads the K and V
-//              segments (any start row), or gathers single key rows
-//              (Vertical-Slash columns) with cp.async;
+//   warp 8     planner: runs the pattern's tile iterator and writes each
+//              tile's descriptor (two 64-key segments and per-half validity
+//              masks) into a ring, then a terminating descriptor;
+//   warp 10    loader: TMA-loads the K and V segments of each tile (any start
+//              row), or gathers single key rows (Vertical-Slash columns) with
+//              cp.async;
 //   warp 9     MMA issuer (one thread): S = Q K^T into TMEM (two buffers),
 //              then O += P V into a TMEM accumulator; Q and P are read from
 //              TMEM, K and V from shared memory;
@@ -33,19 +35,24 @@ namespace msa {
 namespace {
 
 constexpr int kSoftWarps = 8;
-constexpr int kProducerWarp = 8;
+constexpr int kPlannerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 32 * (kSoftWarps + 2);
+constexpr int kLoaderWarp = 10;
+constexpr int kThreads = 32 * (kSoftWarps + 3);
 constexpr int kStages = 3;
-constexpr int kDescSlots = 4;
+constexpr int kDescSlots = 8;
+constexpr int kDescReaders = kSoftWarps + 2;  // softmax warps, MMA warp, loader warp
+constexpr int kMaxStagedBlocks = 512;          // Block-Sparse lists merged in shared memory
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: two S buffers, the O accumulator, Q and P (bf16 pairs)
 constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384, kColP = 448;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+enum TileKind : int32_t { kTileRange = 0, kTileGather = 1, kTileEnd = 2 };
+
 struct TileDesc {
   int32_t seg[2];   // range tiles: first key of each 64-key segment
-  int32_t kind;     // 0 = range, 1 = gather
+  int32_t kind;     // TileKind (kTileEnd: no more tiles in this item)
   int32_t rule;     // A-shape row rule: bit0 keeps j < sink, bit1 keeps j > i - window
   uint32_t mask[2][4];  // per half: bit k = key k of the tile may be attended
   int32_t gidx[128];    // gather tiles: key of column k (-1 = empty)
@@ -74,13 +81,15 @@ struct Layout {
   static constexpr int kV = kK + kStages * kTile;
   static constexpr int kDesc = kV + kStages * kTile;
   static constexpr int kStage = kDesc + kDescSlots * (int)sizeof(TileDesc);  // gather staging (256 ints)
+  static constexpr int kBlk = kStage + 256 * 4;  // Block-Sparse lists and their union
   // row exchange: [2 parities][2 key halves][128] maxima, then [2][128] denominators
-  static constexpr int kXchg = kStage + 256 * 4;
+  static constexpr int kXchg = kBlk + 4 * kMaxStagedBlocks * 4;
   static constexpr int kBars = kXchg + 6 * 128 * 4;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 64;
   // > 113 KB keeps one CTA per SM, so the 512-column TMEM allocation never waits.
   static constexpr int kAlloc = (kTotal + 1024) > 120 * 1024 ? (kTotal + 1024) : 120 * 1024;
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ void set_error(int* err, int code) {
@@ -116,21 +125,6 @@ __device__ __forceinline__ bool bits_any(const uint32_t* bits, int n, int lo, in
     if (x) return true;
   }
   return false;
-}
-
-__device__ __forceinline__ int bits_count(const uint32_t* bits, int n, int lo, int hi) {
-  lo = lo < 0 ? 0 : lo;
-  hi = hi > n - 1 ? n - 1 : hi;
-  if (lo > hi) return 0;
-  const int w0 = lo >> 5, w1 = hi >> 5;
-  int c = 0;
-  for (int w = w0; w <= w1; ++w) {
-    uint32_t x = __ldg(bits + w);
-    if (w == w0) x &= 0xFFFFFFFFu << (lo & 31);
-    if (w == w1) x &= 0xFFFFFFFFu >> (31 - (hi & 31));
-    c += __popc(x);
-  }
-  return c;
 }
 
 __device__ __forceinline__ bool bit_at(const uint32_t* bits, int j) { return (__ldg(bits + (j >> 5)) >> (j & 31)) & 1u; }
@@ -206,55 +200,95 @@ struct AshapeIter {
 // MInference page eq.(6): half h (query block u_h) attends the key blocks J_{u_h}.
 // The sorted lists of both halves are merged; every pair of consecutive key
 // blocks of the union forms one 128-key tile, and each half keeps only its own
-// blocks.
+// blocks.  The union is built once per item in shared memory (whole warp
+// stages the lists, one lane merges); lists longer than the staging buffer are
+// merged straight from global memory.
 struct BlockIter {
   const int32_t* J[2];
   int cnt[2], u[2];
-  int p[2];
-  int total;
-  int last;  // last block emitted (lists must be strictly ascending)
-  __device__ void init(const Unit& U, const Item& it, const AttnArgs& a) {
+  int total;   // blocks in the union
+  int pos;     // next union entry to emit
+  bool staged; // union lives in shared memory (else merged on the fly)
+  int p[2], last;
+  int* un;     // union entries: block id | membership bits << 28
+  __device__ void init(const Unit& U, const Item& it, const AttnArgs& a, int lane, int* sblk) {
     for (int h = 0; h < 2; ++h) {
       u[h] = it.row0[h] / 64;
+      J[h] = nullptr;
+      cnt[h] = 0;
       if (it.exists[h]) {
         const int64_t off = (int64_t)U.slot[h] * a.bs_nb + u[h];
         J[h] = a.bs_idx + off * a.bs_topk;
-        int c = __ldg(a.bs_cnt + off);
+        const int c = __ldg(a.bs_cnt + off);
         cnt[h] = c < 0 ? 0 : (c > a.bs_topk ? a.bs_topk : c);
-      } else {
-        J[h] = nullptr;
-        cnt[h] = 0;
       }
     }
-    int x = 0, y = 0, m = 0;
-    while (x < cnt[0] || y < cnt[1]) {
-      const int vx = x < cnt[0] ? __ldg(J[0] + x) : 0x7FFFFFFF;
-      const int vy = y < cnt[1] ? __ldg(J[1] + y) : 0x7FFFFFFF;
-      if (vx <= vy) ++x;
-      if (vy <= vx) ++y;
-      ++m;
-    }
-    total = m;
+    pos = 0;
     p[0] = p[1] = 0;
     last = -1;
+    un = sblk + 2 * kMaxStagedBlocks;
+    staged = cnt[0] <= kMaxStagedBlocks && cnt[1] <= kMaxStagedBlocks;
+    if (staged) {
+      for (int h = 0; h < 2; ++h)
+        for (int x = lane; x < cnt[h]; x += 32) sblk[h * kMaxStagedBlocks + x] = __ldg(J[h] + x);
+      __syncwarp();
+      if (lane == 0) {
+        int x = 0, y = 0, m = 0;
+        const int* A0 = sblk;
+        const int* A1 = sblk + kMaxStagedBlocks;
+        while (x < cnt[0] || y < cnt[1]) {
+          const int vx = x < cnt[0] ? A0[x] : 0x7FFFFFFF;
+          const int vy = y < cnt[1] ? A1[y] : 0x7FFFFFFF;
+          const int v = min(vx, vy);
+          int bits = 0;
+          if (vx == v) { bits |= 1; ++x; }
+          if (vy == v) { bits |= 2; ++y; }
+          if (v <= last || v < 0 || v >= (1 << 28)) bits = 3 << 2;  // not ascending / out of range: flagged
+          else last = v;
+          un[m++] = (v & 0x0FFFFFFF) | (bits << 28);
+        }
+        total = m;
+      }
+      total = __shfl_sync(0xFFFFFFFFu, total, 0);
+      __syncwarp();
+    } else {
+      int x = 0, y = 0, m = 0;
+      while (x < cnt[0] || y < cnt[1]) {
+        const int vx = x < cnt[0] ? __ldg(J[0] + x) : 0x7FFFFFFF;
+        const int vy = y < cnt[1] ? __ldg(J[1] + y) : 0x7FFFFFFF;
+        if (vx <= vy) ++x;
+        if (vy <= vx) ++y;
+        ++m;
+      }
+      total = m;
+      last = -1;
+    }
   }
-  __device__ int count() const { return (total + 1) / 2; }
-  __device__ bool next_block(int& v, int& bits) {
-    if (p[0] >= cnt[0] && p[1] >= cnt[1]) return false;
-    const int vx = p[0] < cnt[0] ? __ldg(J[0] + p[0]) : 0x7FFFFFFF;
-    const int vy = p[1] < cnt[1] ? __ldg(J[1] + p[1]) : 0x7FFFFFFF;
-    v = min(vx, vy);
-    bits = 0;
-    if (vx == v) { bits |= 1; ++p[0]; }
-    if (vy == v) { bits |= 2; ++p[1]; }
-    if (v <= last) bits = -1;  // not ascending: flagged and dropped by emit()
-    else last = v;
-    return true;
+  __device__ bool done() const { return pos >= total; }
+  __device__ void next_block(int& v, int& bits) {
+    if (staged) {
+      const int e = un[pos];
+      v = e & 0x0FFFFFFF;
+      bits = (e >> 28) & 0xF;
+      if (bits & 12) bits = -1;
+    } else {
+      const int vx = p[0] < cnt[0] ? __ldg(J[0] + p[0]) : 0x7FFFFFFF;
+      const int vy = p[1] < cnt[1] ? __ldg(J[1] + p[1]) : 0x7FFFFFFF;
+      v = min(vx, vy);
+      bits = 0;
+      if (vx == v) { bits |= 1; ++p[0]; }
+      if (vy == v) { bits |= 2; ++p[1]; }
+      if (v <= last) bits = -1;
+      else last = v;
+    }
+    ++pos;
   }
+  // Lane 0: the next tile (two union entries).
   __device__ void emit(int n, TileDesc& d, int* err) {
     int v0 = 0, b0 = 0, v1 = 0, b1 = 0;
     next_block(v0, b0);
-    if (!next_block(v1, b1)) { v1 = v0; b1 = 0; }  // odd tail: reload a valid block, fully masked
+    if (!done()) next_block(v1, b1);
+    else { v1 = v0; b1 = 0; }  // odd tail: reload a valid block, fully masked
     int vs[2] = {v0, v1}, bs[2] = {b0, b1};
     for (int s = 0; s < 2; ++s) {
       if (bs[s] < 0) { bs[s] = 0; set_error(err, kErrIndex); }
@@ -262,7 +296,7 @@ struct BlockIter {
         if ((bs[s] >> h & 1) && (vs[s] < 0 || vs[s] > u[h])) { bs[s] &= ~(1 << h); set_error(err, kErrIndex); }
       if (vs[s] < 0 || 64 * vs[s] >= n) { vs[s] = 0; bs[s] = 0; }
     }
-    d.kind = 0;
+    d.kind = kTileRange;
     d.rule = 0;
     for (int s = 0; s < 2; ++s) {
       d.seg[s] = 64 * vs[s];
@@ -283,6 +317,28 @@ struct BlockIter {
 // window of that map.  Aligned 128-key windows that some slash tile touches
 // become range tiles whose masks include the verticals in them; verticals in
 // the other windows are gathered into column tiles.
+
+// Any bit set in [lo, hi] (hi - lo < 160) of an nbits map: every word loaded
+// up front, so the loads overlap instead of chaining.
+__device__ __forceinline__ bool bits_any5(const uint32_t* bits, int nbits, int lo, int hi) {
+  lo = lo < 0 ? 0 : lo;
+  hi = hi > nbits - 1 ? nbits - 1 : hi;
+  if (lo > hi) return false;
+  const int w0 = lo >> 5, w1 = hi >> 5;
+  uint32_t x[6];
+#pragma unroll
+  for (int q = 0; q < 6; ++q) x[q] = (w0 + q <= w1) ? __ldg(bits + w0 + q) : 0u;
+  x[0] &= 0xFFFFFFFFu << (lo & 31);
+  uint32_t acc = 0u;
+#pragma unroll
+  for (int q = 0; q < 6; ++q) {
+    uint32_t v = x[q];
+    if (w0 + q == w1) v &= 0xFFFFFFFFu >> (31 - (hi & 31));
+    if (w0 + q <= w1) acc |= v;
+  }
+  return acc != 0u;
+}
+
 struct VSIter {
   const uint32_t* dbits;
   const uint32_t* cbits;
@@ -317,31 +373,16 @@ struct VSIter {
     const int j0 = 128 * w;
     const int jhi = min(j0 + 127, e[h]);
     if (j0 > jhi) return false;
-    if (L[h] == 64) return bits_any(cover, 32 * cw, n - 1 - a[h] + j0, n - 1 - a[h] + jhi);
+    if (L[h] == 64) return bits_any5(cover, 32 * cw, n - 1 - a[h] + j0, n - 1 - a[h] + jhi);
     return bits_any(dbits, n, a[h] - jhi, a[h] - j0 + L[h] - 1);
-  }
-  __device__ bool window_has_slash(int w) const { return half_has_slash(0, w) || half_has_slash(1, w); }
-  // Tile count: windows with slash coverage, plus the columns of the others
-  // packed 128 per tile.  Whole warp; result in every lane.
-  __device__ int count(int lane) const {
-    int P = 0, G = 0;
-    for (int w = lane; w < M; w += 32) {
-      if (window_has_slash(w)) ++P;
-      else G += bits_count(cbits, n, 128 * w, min(128 * w + 127, hi_key));
-    }
-    for (int o = 16; o; o >>= 1) {
-      P += __shfl_xor_sync(0xFFFFFFFFu, P, o);
-      G += __shfl_xor_sync(0xFFFFFFFFu, G, o);
-    }
-    return P + (G + 127) / 128;
   }
   __device__ void load_group(int lane) {
     grp += 32;
     const int w = grp + lane;
     bool s = false, c = false;
     if (w < M) {
-      s = window_has_slash(w);
-      if (!s) c = bits_count(cbits, n, 128 * w, min(128 * w + 127, hi_key)) > 0;
+      s = half_has_slash(0, w) | half_has_slash(1, w);
+      c = !s && bits_any5(cbits, n, 128 * w, min(128 * w + 127, hi_key));
     }
     smask = __ballot_sync(0xFFFFFFFFu, s);
     cmask = __ballot_sync(0xFFFFFFFFu, c);
@@ -356,19 +397,18 @@ struct VSIter {
           const uint32_t b = __ballot_sync(0xFFFFFFFFu, ok);
           if (lane == 0) d.mask[h][q] = b;
         }
-      } else if (lane == 0) {
-        for (int q = 0; q < 4; ++q) {
-          uint32_t m = 0u;
-          const int base = j0 + 32 * q;
-          if (ex[h] && base <= e[h]) {
-            m = bits_window32(cover, cw, n - 1 - a[h] + base) | __ldg(cbits + (base >> 5));
-            m &= keys_below(base, e[h] + 1);
-          }
-          d.mask[h][q] = m;
+      } else if ((lane >> 2) == h) {  // lanes 4h .. 4h+3: one mask word each
+        const int q = lane & 3;
+        const int base = j0 + 32 * q;
+        uint32_t m = 0u;
+        if (ex[h] && base <= e[h]) {
+          m = bits_window32(cover, cw, n - 1 - a[h] + base) | __ldg(cbits + (base >> 5));
+          m &= keys_below(base, e[h] + 1);
         }
+        d.mask[h][q] = m;
       }
     }
-    if (lane == 0) { d.seg[0] = j0; d.seg[1] = j0 + 64; d.kind = 0; d.rule = 0; }
+    if (lane == 0) { d.seg[0] = j0; d.seg[1] = j0 + 64; d.kind = kTileRange; d.rule = 0; }
   }
   __device__ void gather_tile(int lane, int* stage, TileDesc& d) {
     const int take = staged < 128 ? staged : 128;
@@ -386,22 +426,16 @@ struct VSIter {
     for (int k = lane; k < rest; k += 32) stage[k] = stage[take + k];
     __syncwarp();
     staged = rest;
-    if (lane == 0) { d.kind = 1; d.rule = 0; d.seg[0] = 0; d.seg[1] = 0; }
+    if (lane == 0) { d.kind = kTileGather; d.rule = 0; d.seg[0] = 0; d.seg[1] = 0; }
   }
-  // Produce the next tile into d (whole warp).
-  __device__ void emit(int lane, int* stage, TileDesc& d) {
+  // Produce the next tile into d (whole warp); false when the item has no more tiles.
+  __device__ bool emit(int lane, int* stage, TileDesc& d) {
     for (;;) {
-      if (staged >= 128) { gather_tile(lane, stage, d); return; }
+      if (staged >= 128) { gather_tile(lane, stage, d); return true; }
       if ((smask | cmask) == 0u) {
         if (grp + 32 >= M) {
-          if (staged > 0) { gather_tile(lane, stage, d); return; }
-          // nothing left (cannot happen when the count was honoured): empty tile
-          if (lane == 0) {
-            d.kind = 0; d.rule = 0; d.seg[0] = 0; d.seg[1] = 64;
-            for (int h = 0; h < 2; ++h)
-              for (int q = 0; q < 4; ++q) d.mask[h][q] = 0u;
-          }
-          return;
+          if (staged > 0) { gather_tile(lane, stage, d); return true; }
+          return false;
         }
         load_group(lane);
         continue;
@@ -411,7 +445,7 @@ struct VSIter {
       smask &= ~(1u << b);
       cmask &= ~(1u << b);
       const int w = grp + b;
-      if (is_slash) { range_masks(w, lane, d); return; }
+      if (is_slash) { range_masks(w, lane, d); return true; }
       // stage this window's columns (ascending)
       const int j0 = 128 * w;
       for (int q = 0; q < 4; ++q) {
@@ -437,8 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::kBars);
   TileDesc* descs = reinterpret_cast<TileDesc*>(sm + Ly::kDesc);
   int* stage = reinterpret_cast<int*>(sm + Ly::kStage);
+  int* sblk = reinterpret_cast<int*>(sm + Ly::kBlk);
   float* xchg = reinterpret_cast<float*>(sm + Ly::kXchg);
-  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + Ly::kMisc);  // [0] tmem, [1] tiles, [2] abort
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + Ly::kMisc);  // [0] tmem, [2] abort
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item_id = blockIdx.x;
@@ -446,10 +481,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Unit& U = UT.u[item_id % A.n_units];
   const int n = A.n;
   const Item it = make_item(U, t, n);
-
-  AshapeIter ai;
-  BlockIter bi;
-  VSIter vi;
 
   if (warp == 0) {
     tmem_alloc(const_cast<uint32_t*>(&misc[0]), kTmemCols);
@@ -471,32 +502,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarPEmpty], 1);
     for (int s = 0; s < kDescSlots; ++s) {
       mbar_init(&bars[kBarDFull + s], 1);
-      mbar_init(&bars[kBarDEmpty + s], kSoftWarps);
+      mbar_init(&bars[kBarDEmpty + s], kDescReaders);
     }
     for (int s = 0; s < 4; ++s) mbar_init(&bars[kBarX + s], 64);
     misc[2] = 0;
     fence_mbar_init();
   }
-  if (warp == kProducerWarp) {
-    int T = 0;
-    if (U.pattern == kUnitAshape) { ai.init(U, it, n); T = ai.count(); }
-    else if (U.pattern == kUnitBlock) { bi.init(U, it, A); T = bi.count(); }
-    else { vi.init(U, it, A); T = vi.count(lane); }
-    if (lane == 0) misc[1] = (uint32_t)T;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  const int T = (int)misc[1];
 
   uint8_t* sK = sm + Ly::kK;
   uint8_t* sV = sm + Ly::kV;
+  auto desc_full = [&](int j) { return mbar_wait(&bars[kBarDFull + j % kDescSlots], (j / kDescSlots) & 1); };
+  auto desc_release = [&](int j) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kBarDEmpty + j % kDescSlots]);
+  };
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
+  if (warp == kPlannerWarp) {
+    // ------------------------------------------------------------ planner
+    AshapeIter ai;
+    BlockIter bi;
+    VSIter vi;
+    int T = 0;
+    if (U.pattern == kUnitAshape) { ai.init(U, it, n); T = ai.count(); }
+    else if (U.pattern == kUnitBlock) bi.init(U, it, A, lane, sblk);
+    else vi.init(U, it, A);
     bool ok = true;
-    if (lane == 0 && T > 0) {
+    for (int j = 0;; ++j) {
+      if (misc[2]) { ok = false; break; }
+      const int slot = j % kDescSlots;
+      if (!mbar_wait(&bars[kBarDEmpty + slot], ((j / kDescSlots) & 1) ^ 1)) { ok = false; break; }
+      TileDesc& d = descs[slot];
+      bool more;
+      if (U.pattern == kUnitVS) {
+        more = vi.emit(lane, stage, d);
+      } else if (U.pattern == kUnitAshape) {
+        more = j < T;
+        if (more && lane == 0) ai.emit(j, n, d);
+      } else {
+        more = !bi.done();  // the cursor advances in lane 0 only: its answer is the warp's
+        more = __shfl_sync(0xFFFFFFFFu, more, 0);
+        if (more && lane == 0) bi.emit(n, d, A.err);
+      }
+      if (!more && lane == 0) d.kind = kTileEnd;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarDFull + slot]);
+      if (!more) break;
+    }
+    if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
+  } else if (warp == kLoaderWarp) {
+    // ------------------------------------------------------------ loader
+    if (lane == 0) {
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
     }
@@ -508,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(empty, ph)) return false;
       const TileDesc& d = descs[j % kDescSlots];
       uint8_t* dst = (is_v ? sV : sK) + st * Ly::kTile;
-      if (d.kind == 0) {
+      if (d.kind == kTileRange) {
         if (lane == 0) {
           const CUtensorMap* map = is_v ? &tv : &tk;
           mbar_arrive_expect_tx(full, Ly::kTile);
@@ -532,38 +591,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    auto make_desc = [&](int j) -> bool {
-      const int slot = j % kDescSlots;
-      if (!mbar_wait(&bars[kBarDEmpty + slot], ((j / kDescSlots) & 1) ^ 1)) return false;
-      TileDesc& d = descs[slot];
-      if (U.pattern == kUnitVS) {
-        vi.emit(lane, stage, d);
-      } else if (lane == 0) {
-        if (U.pattern == kUnitAshape) ai.emit(j, n, d);
-        else bi.emit(n, d, A.err);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarDFull + slot]);
-      return true;
-    };
-    if (T > 0) ok = make_desc(0) && load_kv(0, false);
-    for (int j = 0; ok && j < T; ++j) {
+    // K runs one tile ahead of V; a descriptor is released once its V is issued
+    bool ok = true;
+    int j = 0;
+    for (;; ++j) {
       if (misc[2]) { ok = false; break; }
-      if (j + 1 < T) ok = make_desc(j + 1) && load_kv(j + 1, false);
-      if (ok) ok = load_kv(j, true);
+      if (!desc_full(j)) { ok = false; break; }
+      const bool end = descs[j % kDescSlots].kind == kTileEnd;
+      if (!end && !load_kv(j, false)) { ok = false; break; }
+      if (j > 0) {
+        if (!load_kv(j - 1, true)) { ok = false; break; }
+        desc_release(j - 1);
+      }
+      if (end) { desc_release(j); break; }
     }
     if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && T > 0) {
-      bool ok = mbar_wait(&bars[kBarQ], 0);
-      constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
-      auto pv = [&](int j) -> bool {
-        const int st = j % kStages;
-        if (!mbar_wait(&bars[kBarPFull], j & 1)) return false;
-        if (!mbar_wait(&bars[kBarVFull + st], (j / kStages) & 1)) return false;
-        tc_fence_after();
+    bool ok = mbar_wait(&bars[kBarQ], 0);
+    constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
+    auto pv = [&](int j) -> bool {
+      const int st = j % kStages;
+      if (!mbar_wait(&bars[kBarPFull], j & 1)) return false;
+      if (!mbar_wait(&bars[kBarVFull + st], (j / kStages) & 1)) return false;
+      tc_fence_after();
+      if (lane == 0) {
         const uint32_t v0 = smem_u32(sV + st * Ly::kTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -571,16 +624,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars[kBarVEmpty + st]);
         mma_commit(&bars[kBarPEmpty]);
-        return true;
-      };
-      if (ok) tc_fence_after();
-      for (int j = 0; ok && j < T; ++j) {
-        if (misc[2]) { ok = false; break; }
-        const int st = j % kStages, sb = j & 1;
-        ok = mbar_wait(&bars[kBarKFull + st], (j / kStages) & 1) &&
-             mbar_wait(&bars[kBarSEmpty + sb], ((j >> 1) & 1) ^ 1);
-        if (!ok) break;
-        tc_fence_after();
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok) tc_fence_after();
+    int j = 0;
+    for (; ok; ++j) {
+      if (misc[2]) { ok = false; break; }
+      if (!desc_full(j)) { ok = false; break; }
+      const bool end = descs[j % kDescSlots].kind == kTileEnd;
+      desc_release(j);
+      if (end) break;
+      const int st = j % kStages, sb = j & 1;
+      ok = mbar_wait(&bars[kBarKFull + st], (j / kStages) & 1) &&
+           mbar_wait(&bars[kBarSEmpty + sb], ((j >> 1) & 1) ^ 1);
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
         const uint32_t k0 = smem_u32(sK + st * Ly::kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -590,12 +651,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&bars[kBarSFull + sb]);
         mma_commit(&bars[kBarKEmpty + st]);
-        if (j > 0) ok = pv(j - 1);
       }
-      if (ok) ok = pv(T - 1);
-      if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
+      __syncwarp();
+      if (j > 0) ok = pv(j - 1);
     }
-    __syncwarp();
+    if (ok && j > 0) ok = pv(j - 1);
+    if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
   } else {
     // ------------------------------------------------------------ softmax warps
     const int quarter = warp & 3;          // TMEM lanes 32*quarter ..
@@ -613,35 +674,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     // ---- Q row into TMEM (A operand of S = Q K^T): 32 columns of bf16 pairs per writer
-    if (T > 0) {
-      if (D == 128 || ch == 0) {
-        const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(A.q) + ((int64_t)U.qh[h] * n + i) * D;
-        const int e0 = D == 128 ? ch * 64 : 0;
-        uint32_t qw[32];
+    if (D == 128 || ch == 0) {
+      const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(A.q) + ((int64_t)U.qh[h] * n + i) * D;
+      const int e0 = D == 128 ? ch * 64 : 0;
+      uint32_t qw[32];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          uint4 v4 = make_uint4(0, 0, 0, 0);
-          if (row_ok) v4 = __ldg(reinterpret_cast<const uint4*>(qrow + e0) + x);
-          qw[4 * x] = v4.x; qw[4 * x + 1] = v4.y; qw[4 * x + 2] = v4.z; qw[4 * x + 3] = v4.w;
-        }
-        tmem_st32(tmem + lane_base + kColQ + (D == 128 ? 32 * ch : 0), qw);
+      for (int x = 0; x < 8; ++x) {
+        uint4 v4 = make_uint4(0, 0, 0, 0);
+        if (row_ok) v4 = __ldg(reinterpret_cast<const uint4*>(qrow + e0) + x);
+        qw[4 * x] = v4.x; qw[4 * x + 1] = v4.y; qw[4 * x + 2] = v4.z; qw[4 * x + 3] = v4.w;
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarQ]);
+      tmem_st32(tmem + lane_base + kColQ + (D == 128 ? 32 * ch : 0), qw);
     }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kBarQ]);
 
-    for (int j = 0; j < T; ++j) {
+    int j = 0;
+    for (;; ++j) {
       if (misc[2]) { ok = false; break; }
       // ---- tile descriptor -> validity word of this thread's 64 keys
-      const int slot = j % kDescSlots;
-      if (!mbar_wait(&bars[kBarDFull + slot], (j / kDescSlots) & 1)) { ok = false; break; }
-      const TileDesc& d = descs[slot];
+      if (!desc_full(j)) { ok = false; break; }
+      const TileDesc& d = descs[j % kDescSlots];
+      if (d.kind == kTileEnd) { desc_release(j); break; }
       uint64_t vw = 0ull;
       if (row_ok) {
         const uint64_t m64 = ((uint64_t)d.mask[h][2 * ch + 1] << 32) | d.mask[h][2 * ch];
-        if (d.kind == 0) {
+        if (d.kind == kTileRange) {
           const int base = d.seg[ch];
           vw = m64 & low_mask64(i - base + 1);  // causal: j <= i
           if (d.rule) {
@@ -657,8 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarDEmpty + slot]);
+      desc_release(j);
       if (kCount) count += __popcll(vw);
 
       // ---- S tile (this thread's 64 keys) from TMEM
@@ -742,6 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[kBarPFull]);
     }
     if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
+    const int T = j;  // tiles processed
 
     // ---- epilogue: O / l, LSE (the pair adds its partial denominators)
     const int qh = U.qh[h];
