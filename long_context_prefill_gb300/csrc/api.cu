@@ -103,80 +103,114 @@ static msa_status check_qkv(const msa_shape* s, const void* q, const void* k, co
 }
 
 // ------------------------------------------------------------------ units
-void ashape_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t sink, int32_t window,
-                  std::vector<Unit>& out) {
+// Every unit pairs two sub-items that read one KV head; item t of a unit
+// covers query tile 2t + offset of each sub-item, so all units of a launch
+// have ceil(tiles / 2) items and items of equal t cost about the same.  Heads
+// of one KV group are paired (they read the same keys, and their selected
+// keys tend to coincide); a head left alone is paired with itself (its even
+// and odd query tiles).
+
+static SubUnit sub_unit(int32_t qh0, int32_t qh1, int32_t off0, int32_t off1, int32_t slot0, int32_t slot1,
+                        int32_t offset, int32_t sink, int32_t window) {
+  SubUnit s;
+  memset(&s, 0, sizeof(s));
+  s.qh[0] = qh0;
+  s.qh[1] = qh1;
+  s.row_off[0] = off0;
+  s.row_off[1] = off1;
+  s.slot[0] = slot0;
+  s.slot[1] = slot1;
+  s.stride = 2;
+  s.offset = offset;
+  s.sink = sink;
+  s.window = window;
+  return s;
+}
+
+static void push_unit(std::vector<Unit>& out, int32_t pattern, int32_t kvh, const SubUnit& s0, const SubUnit& s1) {
+  Unit u;
+  memset(&u, 0, sizeof(u));
+  u.pattern = pattern;
+  u.kvh = kvh;
+  u.has1 = 1;
+  u.sub[0] = s0;
+  u.sub[1] = s1;
+  out.push_back(u);
+}
+
+// Positions x (into heads[]) of the heads of each KV group, in heads[] order.
+static std::vector<std::vector<int>> kv_groups(const msa_shape& s, const int32_t* heads, int32_t nh) {
   const int g = s.Hq / s.Hkv;
+  std::vector<std::vector<int>> G((size_t)s.Hkv);
+  for (int x = 0; x < nh; ++x) G[(size_t)(heads[x] / g)].push_back(x);
+  return G;
+}
+
+// Head-per-sub-item units (A-shape and Vertical-Slash): a pair of heads gives
+// two units (even and odd tiles), a single head one unit.  slot[x] is the
+// index slot of position x in batch 0; batch b adds b * slots_per_batch.
+static void head_units(const msa_shape& s, int32_t pattern, const int32_t* heads, int32_t nh, const int32_t* sink,
+                       const int32_t* window, const int32_t* slot, int32_t slots_per_batch, std::vector<Unit>& out) {
+  const auto G = kv_groups(s, heads, nh);
   for (int b = 0; b < s.B; ++b)
-    for (int x = 0; x < nh; ++x) {
-      Unit u;
-      memset(&u, 0, sizeof(u));
-      u.pattern = kUnitAshape;
-      u.kvh = b * s.Hkv + heads[x] / g;
-      u.qh[0] = u.qh[1] = b * s.Hq + heads[x];
-      u.row_off[0] = 0;
-      u.row_off[1] = 64;
-      u.sink = sink;
-      u.window = window;
-      out.push_back(u);
+    for (int kv = 0; kv < s.Hkv; ++kv) {
+      const std::vector<int>& P = G[(size_t)kv];
+      const int32_t kvh = b * s.Hkv + kv;
+      auto sub = [&](int x, int offset) {
+        const int32_t qh = b * s.Hq + heads[x];
+        const int32_t sl = slot ? b * slots_per_batch + slot[x] : 0;
+        return sub_unit(qh, qh, 0, 64, sl, sl, offset, sink ? sink[x] : 0, window ? window[x] : 0);
+      };
+      size_t p = 0;
+      for (; p + 1 < P.size(); p += 2)
+        for (int o = 0; o < 2; ++o) push_unit(out, pattern, kvh, sub(P[p], o), sub(P[p + 1], o));
+      if (p < P.size()) push_unit(out, pattern, kvh, sub(P[p], 0), sub(P[p], 1));
     }
+}
+
+void ashape_units(const msa_shape& s, const int32_t* heads, int32_t nh, const int32_t* sink, const int32_t* window,
+                  std::vector<Unit>& out) {
+  head_units(s, kUnitAshape, heads, nh, sink, window, nullptr, 0, out);
 }
 
 void vs_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t slot_base_per_batch,
               int32_t slots_per_batch, std::vector<Unit>& out) {
-  const int g = s.Hq / s.Hkv;
-  for (int b = 0; b < s.B; ++b)
-    for (int x = 0; x < nh; ++x) {
-      Unit u;
-      memset(&u, 0, sizeof(u));
-      u.pattern = kUnitVS;
-      u.kvh = b * s.Hkv + heads[x] / g;
-      u.qh[0] = u.qh[1] = b * s.Hq + heads[x];
-      u.row_off[0] = 0;
-      u.row_off[1] = 64;
-      u.slot[0] = u.slot[1] = b * slots_per_batch + slot_base_per_batch + x;
-      out.push_back(u);
-    }
+  std::vector<int32_t> slot((size_t)nh);
+  for (int x = 0; x < nh; ++x) slot[(size_t)x] = slot_base_per_batch + x;
+  head_units(s, kUnitVS, heads, nh, nullptr, nullptr, slot.data(), slots_per_batch, out);
 }
 
-// Block-Sparse units: two heads of one KV group at the same query block share
-// the K/V blocks they both selected, so such heads are paired (one unit per
-// parity of the query block); a head left alone takes two consecutive blocks.
+// Block-Sparse units: a half is one 64-row query block of one head.  Four
+// heads of a KV group at the same query block form one item (their block
+// lists tend to coincide); two heads take both blocks of a tile; a single
+// head takes both blocks of its even and of its odd tile.
 void block_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t slots_per_batch,
                  std::vector<Unit>& out) {
-  const int g = s.Hq / s.Hkv;
-  for (int b = 0; b < s.B; ++b) {
+  const auto G = kv_groups(s, heads, nh);
+  for (int b = 0; b < s.B; ++b)
     for (int kv = 0; kv < s.Hkv; ++kv) {
-      std::vector<int> pos;
-      for (int x = 0; x < nh; ++x)
-        if (heads[x] / g == kv) pos.push_back(x);
-      size_t p = 0;
-      for (; p + 1 < pos.size(); p += 2)
-        for (int par = 0; par < 2; ++par) {
-          Unit u;
-          memset(&u, 0, sizeof(u));
-          u.pattern = kUnitBlock;
-          u.kvh = b * s.Hkv + kv;
-          for (int h = 0; h < 2; ++h) {
-            u.qh[h] = b * s.Hq + heads[pos[p + h]];
-            u.slot[h] = b * slots_per_batch + pos[p + h];
-            u.row_off[h] = 64 * par;
-          }
-          out.push_back(u);
-        }
-      if (p < pos.size()) {
-        Unit u;
-        memset(&u, 0, sizeof(u));
-        u.pattern = kUnitBlock;
-        u.kvh = b * s.Hkv + kv;
-        for (int h = 0; h < 2; ++h) {
-          u.qh[h] = b * s.Hq + heads[pos[p]];
-          u.slot[h] = b * slots_per_batch + pos[p];
-          u.row_off[h] = 64 * h;
-        }
-        out.push_back(u);
+      const std::vector<int>& P = G[(size_t)kv];
+      const int32_t kvh = b * s.Hkv + kv;
+      auto qh = [&](int x) { return b * s.Hq + heads[P[(size_t)x]]; };
+      auto sl = [&](int x) { return b * slots_per_batch + P[(size_t)x]; };
+      int p = 0;
+      const int m = (int)P.size();
+      for (; p + 3 < m; p += 4)
+        for (int par = 0; par < 2; ++par)
+          for (int o = 0; o < 2; ++o)
+            push_unit(out, kUnitBlock, kvh,
+                      sub_unit(qh(p), qh(p + 1), 64 * par, 64 * par, sl(p), sl(p + 1), o, 0, 0),
+                      sub_unit(qh(p + 2), qh(p + 3), 64 * par, 64 * par, sl(p + 2), sl(p + 3), o, 0, 0));
+      if (p + 1 < m) {
+        for (int o = 0; o < 2; ++o)
+          push_unit(out, kUnitBlock, kvh, sub_unit(qh(p), qh(p + 1), 0, 0, sl(p), sl(p + 1), o, 0, 0),
+                    sub_unit(qh(p), qh(p + 1), 64, 64, sl(p), sl(p + 1), o, 0, 0));
+        p += 2;
       }
+      if (p < m)
+        push_unit(out, kUnitBlock, kvh, sub_unit(qh(p), qh(p), 0, 64, sl(p), sl(p), 0, 0, 0),
+                  sub_unit(qh(p), qh(p), 0, 64, sl(p), sl(p), 1, 0, 0));
     }
-  }
 }
 
 msa_status attention(const msa_shape& s, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -189,7 +223,8 @@ msa_status attention(const msa_shape& s, const void* q, const void* k, const voi
   AttnArgs a = idx;
   a.n = s.n;
   a.d = s.d_h;
-  a.T = ceil_div(s.n, 128);
+  a.nqt = ceil_div(s.n, 128);
+  a.T = (a.nqt + 1) / 2;
   a.scale_log2 = effective_scale(s) * 1.4426950408889634f;
   a.q = q;
   a.k = k;
@@ -231,7 +266,8 @@ msa_status msa_attn_ashape(const msa_shape* shape, const void* q, const void* k,
   MSA_TRY(check_heads(heads, n_heads, shape->Hq));
   if (sink < 0 || window < 1) return MSA_ERR_INVALID_ARG;
   std::vector<Unit> units;
-  ashape_units(*shape, heads, n_heads, sink, window, units);
+  const std::vector<int32_t> sinks((size_t)n_heads, sink), windows((size_t)n_heads, window);
+  ashape_units(*shape, heads, n_heads, sinks.data(), windows.data(), units);
   AttnArgs a;
   memset(&a, 0, sizeof(a));
   return attention(*shape, q, k, v, o, lse, edges, units, a, (cudaStream_t)stream);

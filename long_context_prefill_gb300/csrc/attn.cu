@@ -5,27 +5,32 @@
 // the online-softmax merge of eq.(7)-(8)): for every query row i of a work
 // item, o_i = Σ_{j in N(i)} e^{s_ij} v_j / Σ_{j in N(i)} e^{s_ij}.
 //
-// One CTA processes one item: 128 query rows (two 64-row halves) of one KV
-// group against a stream of 128-key tiles that a pattern iterator generates.
-//   warp 8     planner: runs the pattern's tile iterator and writes each
-//              tile's descriptor (two 64-key segments and per-half validity
-//              masks) into a ring, then a terminating descriptor;
-//   warp 10    loader: TMA-loads the K and V segments of each tile (any start
-//              row), or gathers single key rows (Vertical-Slash columns) with
-//              cp.async;
-//   warp 9     MMA issuer (one thread): S = Q K^T into TMEM (two buffers),
-//              then O += P V into a TMEM accumulator; Q and P are read from
-//              TMEM, K and V from shared memory;
-//   warps 0-7  softmax: query row r is TMEM lane r; warps w and w+4 share
-//              the lanes of quarter w and split the 128 keys (and the O
-//              columns) in halves, exchanging the row max through shared
-//              memory.  Masks (causal, pattern, sequence end) are applied
-//              before the max; O is rescaled in TMEM only when the max grows
-//              by more than 2^8; P is written to TMEM as bf16 pairs.
-// Every (i, j) pair enters the softmax at most once: tiles partition the keys
-// of an item, and masks drop what lies outside N(i) (MInference page §3.2 and
-// §5.1 "boundary masks": set to -inf before the max).
+// One CTA processes one item: two 128-row query tiles ("sub-items" X = 0, 1,
+// each of two 64-row halves) that read the same KV head, against one stream of
+// 128-key tiles holding every key either sub-item needs.  Sharing the K/V
+// stream doubles the tensor work per loaded byte.
+//   warp 8     planner: merges the sub-items' key sets into tiles of two
+//              64-key segments (or of 128 gathered key columns) and writes
+//              each tile's descriptor (segments, per-half validity masks,
+//              per-sub-item activity and A-shape row rules) into a ring; a
+//              terminating descriptor ends the item;
+//   warp 10    loader: TMA-loads both Q tiles once, then K(j) and V(j) of
+//              every tile into a four-slot ring (K in slots 0/2, V in 1/3), or
+//              gathers single key rows with cp.async;
+//   warp 9     MMA issuer (one thread): per tile and sub-item, O_X += P_X V of
+//              the previous tile, then S_X = Q_X K^T.  While one sub-item's
+//              softmax runs, the tensor core works for the other;
+//   warps 0-7  softmax: warps 4X..4X+3 own sub-item X; thread r is query row r
+//              (TMEM lane r) with all 128 keys of a tile.  Masks (causal,
+//              pattern, sequence end) are applied before the max; O_X is
+//              rescaled in TMEM only when the max grows by more than 2^8; P
+//              (bf16 pairs) overwrites the first 64 columns of S_X.
+// Every (i, j) pair enters the softmax at most once: a key lies in one tile
+// of the item, and masks drop what lies outside N(i) (MInference page §3.2
+// and §5.1 "boundary masks": set to -inf before the max).
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -39,52 +44,50 @@ constexpr int kPlannerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kLoaderWarp = 10;
 constexpr int kThreads = 32 * (kSoftWarps + 3);
-constexpr int kStages = 3;
+constexpr int kSlots = 4;  // K(j) in slot 2j mod 4, V(j) in slot 2j+1 mod 4
 constexpr int kDescSlots = 8;
 constexpr int kDescReaders = kSoftWarps + 2;  // softmax warps, MMA warp, loader warp
-constexpr int kMaxStagedBlocks = 512;          // Block-Sparse lists merged in shared memory
+constexpr int kMaxStagedBlocks = 512;         // Block-Sparse list entries staged per half
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: two S buffers, the O accumulator, Q and P (bf16 pairs)
-constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384, kColP = 448;
+// TMEM columns: S of sub-item X at 128 X (P over its first 64 columns), O of
+// sub-item X at 256 + 128 X
+constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kPolyPairs = 0;              // of every 8 key pairs, exponentiated on the FMA pipe
 
 enum TileKind : int32_t { kTileRange = 0, kTileGather = 1, kTileEnd = 2 };
 
 struct TileDesc {
-  int32_t seg[2];   // range tiles: first key of each 64-key segment
-  int32_t kind;     // TileKind (kTileEnd: no more tiles in this item)
-  int32_t rule;     // A-shape row rule: bit0 keeps j < sink, bit1 keeps j > i - window
-  uint32_t mask[2][4];  // per half: bit k = key k of the tile may be attended
-  int32_t gidx[128];    // gather tiles: key of column k (-1 = empty)
+  int32_t seg[2];       // range tiles: first key of each 64-key segment
+  int32_t kind;         // TileKind (kTileEnd: no more tiles in this item)
+  uint8_t rule[2][2];   // A-shape row rule per [sub-item][segment]: bit0 j < sink, bit1 j > i - window
+  uint8_t active[2];    // sub-item X attends some key of this tile
+  uint8_t pad[2];
+  uint32_t mask[4][4];  // per half 2X+h: bit k = key k of the tile may be attended
+  int32_t gidx[128];    // gather tiles: key of column k, ascending, then -1
 };
 
 enum {
   kBarQ = 0,
-  kBarKFull = 1,
-  kBarKEmpty = kBarKFull + kStages,
-  kBarVFull = kBarKEmpty + kStages,
-  kBarVEmpty = kBarVFull + kStages,
-  kBarSFull = kBarVEmpty + kStages,
-  kBarSEmpty = kBarSFull + 2,
-  kBarPFull = kBarSEmpty + 2,
-  kBarPEmpty = kBarPFull + 1,
-  kBarDFull = kBarPEmpty + 1,
+  kBarFull = 1,
+  kBarEmpty = kBarFull + kSlots,
+  kBarSFull = kBarEmpty + kSlots,  // per sub-item: S of its latest tile is in TMEM
+  kBarPFull = kBarSFull + 2,       // per sub-item: P of its latest tile is in TMEM
+  kBarODone = kBarPFull + 2,       // every MMA of the item has completed
+  kBarDFull = kBarODone + 1,
   kBarDEmpty = kBarDFull + kDescSlots,
-  kBarX = kBarDEmpty + kDescSlots,  // row exchange of the two warps of each quarter
-  kNumBars = kBarX + 4
+  kNumBars = kBarDEmpty + kDescSlots
 };
 
 template <int D>
 struct Layout {
-  static constexpr int kTile = 128 * D * 2;  // 128 key rows of d_h bf16
-  static constexpr int kK = 0;
-  static constexpr int kV = kK + kStages * kTile;
-  static constexpr int kDesc = kV + kStages * kTile;
+  static constexpr int kTile = 128 * D * 2;  // 128 rows of d_h bf16
+  static constexpr int kQ = 0;               // the two Q tiles
+  static constexpr int kRing = kQ + 2 * kTile;
+  static constexpr int kDesc = kRing + kSlots * kTile;
   static constexpr int kStage = kDesc + kDescSlots * (int)sizeof(TileDesc);  // gather staging (256 ints)
-  static constexpr int kBlk = kStage + 256 * 4;  // Block-Sparse lists and their union
-  // row exchange: [2 parities][2 key halves][128] maxima, then [2][128] denominators
-  static constexpr int kXchg = kBlk + 4 * kMaxStagedBlocks * 4;
-  static constexpr int kBars = kXchg + 6 * 128 * 4;
+  static constexpr int kBlk = kStage + 256 * 4;                             // Block-Sparse lists
+  static constexpr int kBars = kBlk + 4 * kMaxStagedBlocks * 4;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 64;
   // > 113 KB keeps one CTA per SM, so the 512-column TMEM allocation never waits.
@@ -102,6 +105,62 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two fp32 values in one 64-bit register pair, for the packed f32x2 instructions.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void up2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// 2^x for a pair on the FMA pipe (the MUFU unit is the softmax's bottleneck):
+// x = n + f with n = round(x) and f in [-1/2, 1/2]; 2^f by a cubic fitted
+// for minimax relative error on that interval (7.5e-5, far below bf16's
+// 2^-9), and 2^n added to the exponent field.  Inputs are clamped at -125 so
+// the result stays a normal float (masked entries come out as ~2^-125, not 0;
+// a row with no attended key is recognised by its max staying -inf).
+__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer held in the low mantissa bits
+  float x0, x1;
+  up2(x, x0, x1);
+  const uint64_t xc = pk2(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f));
+  const uint64_t t = add2(xc, pk2(kRound, kRound));
+  const uint64_t f = sub2(xc, sub2(t, pk2(kRound, kRound)));
+  uint64_t p = fma2(f, pk2(0.0551716685295105f, 0.0551716685295105f), pk2(0.2426111251115799f, 0.2426111251115799f));
+  p = fma2(p, f, pk2(0.6932609677314758f, 0.6932609677314758f));
+  p = fma2(p, f, pk2(0.9999280571937561f, 0.9999280571937561f));
+  float t0, t1, p0, p1;
+  up2(t, t0, t1);
+  up2(p, p0, p1);
+  // t's bits are 0x4B400000 + n, so (t << 23) mod 2^32 is n << 23
+  const uint32_t r0 = __float_as_uint(t0) * (1u << 23) + __float_as_uint(p0);
+  const uint32_t r1 = __float_as_uint(t1) * (1u << 23) + __float_as_uint(p1);
+  return pk2(__uint_as_float(r0), __uint_as_float(r1));
+}
+
 __device__ __forceinline__ uint64_t low_mask64(int c) {  // bits [0, c), c clamped to [0, 64]
   c = c < 0 ? 0 : (c > 64 ? 64 : c);
   return c >= 64 ? ~0ull : ((1ull << c) - 1ull);
@@ -112,22 +171,9 @@ __device__ __forceinline__ uint32_t low_mask32(int c) {
   return c >= 32 ? 0xFFFFFFFFu : ((1u << c) - 1u);
 }
 
-// Any bit of `bits` (an n-bit map) set in [lo, hi] ∩ [0, n)?
-__device__ __forceinline__ bool bits_any(const uint32_t* bits, int n, int lo, int hi) {
-  lo = lo < 0 ? 0 : lo;
-  hi = hi > n - 1 ? n - 1 : hi;
-  if (lo > hi) return false;
-  const int w0 = lo >> 5, w1 = hi >> 5;
-  for (int w = w0; w <= w1; ++w) {
-    uint32_t x = __ldg(bits + w);
-    if (w == w0) x &= 0xFFFFFFFFu << (lo & 31);
-    if (w == w1) x &= 0xFFFFFFFFu >> (31 - (hi & 31));
-    if (x) return true;
-  }
-  return false;
+__device__ __forceinline__ uint32_t keys_below(int base, int limit) {  // bits k with base + k < limit
+  return low_mask32(limit - base);
 }
-
-__device__ __forceinline__ bool bit_at(const uint32_t* bits, int j) { return (__ldg(bits + (j >> 5)) >> (j & 31)) & 1u; }
 
 // 32 bits of an nw-word map starting at bit p >= 0 (bits past the end read 0).
 __device__ __forceinline__ uint32_t bits_window32(const uint32_t* bits, int nw, int p) {
@@ -137,325 +183,361 @@ __device__ __forceinline__ uint32_t bits_window32(const uint32_t* bits, int nw, 
   return __funnelshift_r(lo, hi, sh);
 }
 
-__device__ __forceinline__ uint32_t keys_below(int base, int limit) {  // bits k with base + k < limit
-  return low_mask32(limit - base);
-}
-
 // ------------------------------------------------------------------ item geometry
-struct Item {
-  int row0[2];   // first query row of each half
-  int exists[2]; // half has at least one row < n
-  int e[2];      // last row of each half's query block (clipped to n-1)
-  int a0;        // 128 * t
+// The four halves of an item are hh = 2X + h (sub-item X, half h).
+struct Geo {
+  int row0[4];    // first query row of each half
+  int ex[4];      // half has at least one row < n
+  int e[4];       // last row of each half's query block (clipped to n-1)
+  int sub_ex[2];  // sub-item has a half with rows
+  int hi_key[2];  // last key sub-item X may attend
 };
 
-__device__ __forceinline__ Item make_item(const Unit& U, int t, int n) {
-  Item it;
-  it.a0 = 128 * t;
-  for (int h = 0; h < 2; ++h) {
-    it.row0[h] = 128 * t + U.row_off[h];
-    it.exists[h] = it.row0[h] < n;
-    int e = it.row0[h] + 63;
-    it.e[h] = e < n - 1 ? e : n - 1;
+__device__ __forceinline__ Geo make_geo(const Unit& U, int t, int n, int nqt) {
+  Geo G;
+  for (int X = 0; X < 2; ++X) {
+    const SubUnit& S = U.sub[X];
+    const int tq = t * S.stride + S.offset;
+    const bool live = (X == 0 || U.has1) && tq < nqt;
+    G.sub_ex[X] = 0;
+    G.hi_key[X] = -1;
+    for (int h = 0; h < 2; ++h) {
+      const int hh = 2 * X + h;
+      G.row0[hh] = 128 * tq + S.row_off[h];
+      G.ex[hh] = live && G.row0[hh] < n;
+      const int e = G.row0[hh] + 63;
+      G.e[hh] = e < n - 1 ? e : n - 1;
+      if (G.ex[hh]) {
+        G.sub_ex[X] = 1;
+        G.hi_key[X] = max(G.hi_key[X], G.e[hh]);
+      }
+    }
   }
-  return it;
+  return G;
 }
 
-// ------------------------------------------------------------------ A-shape tiles
-// MInference page eq.(3): rows i of the item attend j < g or i-w < j <= i.
-// The key ranges [0, g) and [a0-w+1, a0+127] (merged when they touch) are cut
-// into 128-key tiles; a per-tile row rule applies the exact set.
-struct AshapeIter {
-  int lo[2], hi[2], rule[2], tiles[2];
-  __device__ void init(const Unit& U, const Item& it, int n) {
-    const int hi_key = min(it.a0 + 127, n - 1);
-    const int g = U.sink, w = U.window;
-    const int sw = max(0, it.a0 - w + 1);
-    if (sw <= g) {
-      lo[0] = 0; hi[0] = hi_key; rule[0] = 3;
-      lo[1] = 0; hi[1] = -1; rule[1] = 0;
-    } else {
-      lo[0] = 0; hi[0] = min(g, n) - 1; rule[0] = 1;
-      lo[1] = sw; hi[1] = hi_key; rule[1] = 2;
+// ------------------------------------------------------------------ A-shape segments
+// MInference page eq.(3): rows i attend j < g or i-w < j <= i.  Per sub-item
+// X, the key ranges [0, g) (slot 2X) and [a0-w+1, last row] (slot 2X+1), or
+// one range [0, last row] when they touch, become intervals of 64-key
+// segments with a row rule; the union over both sub-items is walked in
+// ascending order.  Lane 0 runs it; unused slots have lo > hi.
+struct AshapeSeg {
+  int lo[4], hi[4], rule[4];
+  int cur;
+  __device__ void init(const Unit& U, const Geo& G, int n) {
+    cur = 0;
+#pragma unroll
+    for (int X = 0; X < 2; ++X) {
+      lo[2 * X] = lo[2 * X + 1] = 1;
+      hi[2 * X] = hi[2 * X + 1] = 0;
+      rule[2 * X] = 1;
+      rule[2 * X + 1] = 2;
+      if (!G.sub_ex[X]) continue;
+      const int g = U.sub[X].sink, w = U.sub[X].window;
+      const int a0 = min(G.row0[2 * X], G.row0[2 * X + 1]);
+      const int hk = G.hi_key[X];
+      const int sw = max(0, a0 - w + 1);
+      if (sw <= g) {
+        lo[2 * X] = 0; hi[2 * X] = hk >> 6; rule[2 * X] = 3;
+      } else {
+        if (g > 0) { lo[2 * X] = 0; hi[2 * X] = (min(g, n) - 1) >> 6; }
+        lo[2 * X + 1] = sw >> 6; hi[2 * X + 1] = hk >> 6;
+      }
     }
-    for (int r = 0; r < 2; ++r) tiles[r] = hi[r] >= lo[r] ? (hi[r] - lo[r] + 128) / 128 : 0;
   }
-  __device__ int count() const { return tiles[0] + tiles[1]; }
-  __device__ void emit(int j, int n, TileDesc& d) const {
-    const int r = j < tiles[0] ? 0 : 1;
-    const int t0 = lo[r] + 128 * (r == 0 ? j : j - tiles[0]);
-    d.seg[0] = t0;
-    d.seg[1] = t0 + 64;
-    d.kind = 0;
-    d.rule = rule[r];
-    for (int w = 0; w < 4; ++w) {
-      const uint32_t m = keys_below(t0 + 32 * w, n);
-      d.mask[0][w] = m;
-      d.mask[1][w] = m;
-    }
+  // Next segment of the union with each sub-item's rule (0: not attended).
+  __device__ bool next(int& seg, int (&r)[2]) {
+    int best = 0x7FFFFFFF;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (hi[q] >= cur && lo[q] <= hi[q]) best = min(best, max(lo[q], cur));
+    if (best == 0x7FFFFFFF) return false;
+    seg = best;
+    r[0] = r[1] = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (lo[q] <= best && best <= hi[q]) r[q >> 1] |= rule[q];
+    cur = best + 1;
+    return true;
   }
 };
 
-// ------------------------------------------------------------------ Block-Sparse tiles
-// MInference page eq.(6): half h (query block u_h) attends the key blocks J_{u_h}.
-// The sorted lists of both halves are merged; every pair of consecutive key
-// blocks of the union forms one 128-key tile, and each half keeps only its own
-// blocks.  The union is built once per item in shared memory (whole warp
-// stages the lists, one lane merges); lists longer than the staging buffer are
-// merged straight from global memory.
-struct BlockIter {
-  const int32_t* J[2];
-  int cnt[2], u[2];
-  int total;   // blocks in the union
-  int pos;     // next union entry to emit
-  bool staged; // union lives in shared memory (else merged on the fly)
-  int p[2], last;
-  int* un;     // union entries: block id | membership bits << 28
-  __device__ void init(const Unit& U, const Item& it, const AttnArgs& a, int lane, int* sblk) {
-    for (int h = 0; h < 2; ++h) {
-      u[h] = it.row0[h] / 64;
-      J[h] = nullptr;
-      cnt[h] = 0;
-      if (it.exists[h]) {
-        const int64_t off = (int64_t)U.slot[h] * a.bs_nb + u[h];
-        J[h] = a.bs_idx + off * a.bs_topk;
+// ------------------------------------------------------------------ Block-Sparse segments
+// MInference page eq.(6): half hh (query block u_hh) attends the key blocks
+// J_{u_hh}.  The four halves' ascending lists are staged in shared memory
+// (lists longer than the staging buffer are read from global memory) and
+// merged; each union block is one segment with its membership bits.  Lane 0
+// runs the merge.
+struct BlockSeg {
+  const int32_t* L[4];
+  int cnt[4], u[4], p[4];
+  int last;
+  __device__ void init(const Unit& U, const Geo& G, const AttnArgs& a, int lane, int* sblk) {
+    bool fits = true;
+    for (int hh = 0; hh < 4; ++hh) {
+      const int X = hh >> 1, h = hh & 1;
+      u[hh] = G.row0[hh] / 64;
+      cnt[hh] = 0;
+      L[hh] = nullptr;
+      p[hh] = 0;
+      if (G.ex[hh]) {
+        const int64_t off = (int64_t)U.sub[X].slot[h] * a.bs_nb + u[hh];
+        L[hh] = a.bs_idx + off * a.bs_topk;
         const int c = __ldg(a.bs_cnt + off);
-        cnt[h] = c < 0 ? 0 : (c > a.bs_topk ? a.bs_topk : c);
+        cnt[hh] = c < 0 ? 0 : (c > a.bs_topk ? a.bs_topk : c);
+        fits = fits && cnt[hh] <= kMaxStagedBlocks;
       }
     }
-    pos = 0;
-    p[0] = p[1] = 0;
+    if (fits) {
+      for (int hh = 0; hh < 4; ++hh) {
+        for (int x = lane; x < cnt[hh]; x += 32) sblk[hh * kMaxStagedBlocks + x] = __ldg(L[hh] + x);
+        L[hh] = sblk + hh * kMaxStagedBlocks;
+      }
+      __syncwarp();
+    }
     last = -1;
-    un = sblk + 2 * kMaxStagedBlocks;
-    staged = cnt[0] <= kMaxStagedBlocks && cnt[1] <= kMaxStagedBlocks;
-    if (staged) {
-      for (int h = 0; h < 2; ++h)
-        for (int x = lane; x < cnt[h]; x += 32) sblk[h * kMaxStagedBlocks + x] = __ldg(J[h] + x);
-      __syncwarp();
-      if (lane == 0) {
-        int x = 0, y = 0, m = 0;
-        const int* A0 = sblk;
-        const int* A1 = sblk + kMaxStagedBlocks;
-        while (x < cnt[0] || y < cnt[1]) {
-          const int vx = x < cnt[0] ? A0[x] : 0x7FFFFFFF;
-          const int vy = y < cnt[1] ? A1[y] : 0x7FFFFFFF;
-          const int v = min(vx, vy);
-          int bits = 0;
-          if (vx == v) { bits |= 1; ++x; }
-          if (vy == v) { bits |= 2; ++y; }
-          if (v <= last || v < 0 || v >= (1 << 28)) bits = 3 << 2;  // not ascending / out of range: flagged
-          else last = v;
-          un[m++] = (v & 0x0FFFFFFF) | (bits << 28);
-        }
-        total = m;
-      }
-      total = __shfl_sync(0xFFFFFFFFu, total, 0);
-      __syncwarp();
-    } else {
-      int x = 0, y = 0, m = 0;
-      while (x < cnt[0] || y < cnt[1]) {
-        const int vx = x < cnt[0] ? __ldg(J[0] + x) : 0x7FFFFFFF;
-        const int vy = y < cnt[1] ? __ldg(J[1] + y) : 0x7FFFFFFF;
-        if (vx <= vy) ++x;
-        if (vy <= vx) ++y;
-        ++m;
-      }
-      total = m;
-      last = -1;
-    }
   }
-  __device__ bool done() const { return pos >= total; }
-  __device__ void next_block(int& v, int& bits) {
-    if (staged) {
-      const int e = un[pos];
-      v = e & 0x0FFFFFFF;
-      bits = (e >> 28) & 0xF;
-      if (bits & 12) bits = -1;
-    } else {
-      const int vx = p[0] < cnt[0] ? __ldg(J[0] + p[0]) : 0x7FFFFFFF;
-      const int vy = p[1] < cnt[1] ? __ldg(J[1] + p[1]) : 0x7FFFFFFF;
-      v = min(vx, vy);
-      bits = 0;
-      if (vx == v) { bits |= 1; ++p[0]; }
-      if (vy == v) { bits |= 2; ++p[1]; }
-      if (v <= last) bits = -1;
-      else last = v;
+  // Next union block and the halves that hold it; bits = -1 flags a list
+  // that is not strictly ascending.
+  __device__ bool next(int& v, int& bits) {
+    int best = 0x7FFFFFFF;
+    int val[4];
+    for (int hh = 0; hh < 4; ++hh) {
+      val[hh] = p[hh] < cnt[hh] ? L[hh][p[hh]] : 0x7FFFFFFF;
+      best = min(best, val[hh]);
     }
-    ++pos;
-  }
-  // Lane 0: the next tile (two union entries).
-  __device__ void emit(int n, TileDesc& d, int* err) {
-    int v0 = 0, b0 = 0, v1 = 0, b1 = 0;
-    next_block(v0, b0);
-    if (!done()) next_block(v1, b1);
-    else { v1 = v0; b1 = 0; }  // odd tail: reload a valid block, fully masked
-    int vs[2] = {v0, v1}, bs[2] = {b0, b1};
-    for (int s = 0; s < 2; ++s) {
-      if (bs[s] < 0) { bs[s] = 0; set_error(err, kErrIndex); }
-      for (int h = 0; h < 2; ++h)
-        if ((bs[s] >> h & 1) && (vs[s] < 0 || vs[s] > u[h])) { bs[s] &= ~(1 << h); set_error(err, kErrIndex); }
-      if (vs[s] < 0 || 64 * vs[s] >= n) { vs[s] = 0; bs[s] = 0; }
-    }
-    d.kind = kTileRange;
-    d.rule = 0;
-    for (int s = 0; s < 2; ++s) {
-      d.seg[s] = 64 * vs[s];
-      for (int w = 0; w < 2; ++w) {
-        const uint32_t m = keys_below(64 * vs[s] + 32 * w, n);
-        d.mask[0][2 * s + w] = (bs[s] & 1) ? m : 0u;
-        d.mask[1][2 * s + w] = (bs[s] & 2) ? m : 0u;
-      }
-    }
+    if (best == 0x7FFFFFFF) return false;
+    v = best;
+    bits = 0;
+    for (int hh = 0; hh < 4; ++hh)
+      if (val[hh] == best) { bits |= 1 << hh; ++p[hh]; }
+    if (v <= last) bits = -1;
+    else last = v;
+    return true;
   }
 };
 
-// ------------------------------------------------------------------ Vertical-Slash tiles
+// ------------------------------------------------------------------ Vertical-Slash segments
 // Physical set of row i in query block [a, e] (MInference page §2.1 and §4.1):
 // keys covered by some slash tile [a-δ, e-δ] (δ in D), plus the vertical
 // columns C, restricted to j <= i.  For a full block, key j is covered iff bit
-// n-1-a+j of the dilated coverage map is set, so a tile's mask is a 128-bit
-// window of that map.  Aligned 128-key windows that some slash tile touches
-// become range tiles whose masks include the verticals in them; verticals in
-// the other windows are gathered into column tiles.
+// n-1-a+j of the dilated coverage map is set, so a 32-key mask word is a
+// 32-bit window of that map; a ragged last block (fewer than 64 rows) is
+// dilated exactly from D.  64-key blocks that some half's slash tiles touch
+// become range segments (two per tile) whose masks include the verticals in
+// them; verticals in the other blocks are gathered into column tiles.
+//
+// The whole warp runs it: lane l evaluates key block grp + l of a group of 32
+// (all loads of a group in flight at once), then the group is emitted in
+// ascending block order.
 
-// Any bit set in [lo, hi] (hi - lo < 160) of an nbits map: every word loaded
-// up front, so the loads overlap instead of chaining.
-__device__ __forceinline__ bool bits_any5(const uint32_t* bits, int nbits, int lo, int hi) {
-  lo = lo < 0 ? 0 : lo;
-  hi = hi > nbits - 1 ? nbits - 1 : hi;
-  if (lo > hi) return false;
-  const int w0 = lo >> 5, w1 = hi >> 5;
-  uint32_t x[6];
-#pragma unroll
-  for (int q = 0; q < 6; ++q) x[q] = (w0 + q <= w1) ? __ldg(bits + w0 + q) : 0u;
-  x[0] &= 0xFFFFFFFFu << (lo & 31);
-  uint32_t acc = 0u;
-#pragma unroll
-  for (int q = 0; q < 6; ++q) {
-    uint32_t v = x[q];
-    if (w0 + q == w1) v &= 0xFFFFFFFFu >> (31 - (hi & 31));
-    if (w0 + q <= w1) acc |= v;
-  }
-  return acc != 0u;
+// Bits [p, p+32) of an n-bit map held in nw words (zeros outside the map).
+__device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int nw, int p) {
+  const int w = p >> 5, sh = p & 31;  // floor division for negative p
+  const uint32_t lo = (w >= 0 && w < nw) ? __ldg(bits + w) : 0u;
+  const uint32_t hi = (w + 1 >= 0 && w + 1 < nw) ? __ldg(bits + w + 1) : 0u;
+  return __funnelshift_r(lo, hi, sh);
 }
 
-struct VSIter {
-  const uint32_t* dbits;
-  const uint32_t* cbits;
-  const uint32_t* cover;
-  int cw;  // cover words
-  int n, M, hi_key;
-  int a[2], e[2], L[2], ex[2];
-  int grp;                // first window of the current 32-window group
-  uint32_t smask, cmask;  // group windows with slash coverage / with only columns
-  int staged;             // columns waiting in the staging list
-  __device__ void init(const Unit& U, const Item& it, const AttnArgs& A) {
-    n = A.n;
-    dbits = A.vs_dbits + (int64_t)U.slot[0] * A.vs_words;
-    cbits = A.vs_cbits + (int64_t)U.slot[0] * A.vs_words;
-    cover = A.vs_cover + (int64_t)U.slot[0] * A.vs_cover_words;
+// Bit k set iff the n-bit map D has a bit in [A-k, A-k+L-1] (1 <= L <= 64):
+// key base+k is covered by the slash tiles of the L-row block starting at
+// row base+A.
+__device__ __forceinline__ uint32_t exact_cover32(const uint32_t* dbits, int nw, int A, int L) {
+  const int lo = A - 31;  // δ held in bit 0 of the window
+  unsigned __int128 v = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v |= (unsigned __int128)bits32_at(dbits, nw, lo + 32 * q) << (32 * q);
+  // e bit p = OR of v bits [p, p+L-1]
+  unsigned __int128 e = v;
+  int span = 1;
+  while (2 * span <= L) {
+    e |= e >> span;
+    span *= 2;
+  }
+  if (span < L) e |= e >> (L - span);
+  return __brev((uint32_t)e);  // bit k = e bit 31-k
+}
+
+struct VSSeg {
+  const uint32_t* cbits[2];
+  const uint32_t* dbits[2];
+  const uint32_t* cover[2];
+  int cw, nw, NB, hi_key, two;
+  int a[4], e[4], L[4], ex[4];
+  int grp;                // first block of the current 32-block group
+  uint32_t rmask, cmask;  // group blocks that are range segments / that only hold columns
+  uint32_t m[4][2];       // this lane's block: attend masks per half (range blocks)
+  uint32_t cf[2][2];      // this lane's block: column words of each index slot
+  int staged;             // staged columns: key | in-slot-0 << 28 | in-slot-1 << 29
+  __device__ void init(const Unit& U, const Geo& G, const AttnArgs& A) {
     cw = A.vs_cover_words;
-    hi_key = min(it.a0 + 127, n - 1);
-    M = hi_key / 128 + 1;
-    for (int h = 0; h < 2; ++h) {
-      a[h] = it.row0[h];
-      e[h] = it.e[h];
-      ex[h] = it.exists[h];
-      L[h] = e[h] - a[h] + 1;
+    nw = A.vs_words;
+#pragma unroll
+    for (int X = 0; X < 2; ++X) {
+      const int slot = U.sub[X].slot[0];
+      dbits[X] = A.vs_dbits + (int64_t)slot * A.vs_words;
+      cbits[X] = A.vs_cbits + (int64_t)slot * A.vs_words;
+      cover[X] = A.vs_cover + (int64_t)slot * A.vs_cover_words;
+    }
+    two = U.has1 && U.sub[1].slot[0] != U.sub[0].slot[0];
+    hi_key = max(G.hi_key[0], G.hi_key[1]);
+    NB = hi_key < 0 ? 0 : hi_key / 64 + 1;
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      a[hh] = G.row0[hh];
+      e[hh] = G.e[hh];
+      ex[hh] = G.ex[hh];
+      L[hh] = e[hh] - a[hh] + 1;
     }
     grp = -32;
-    smask = cmask = 0u;
+    rmask = cmask = 0u;
     staged = 0;
   }
-  // Keys of window w covered by a slash tile of half h?
-  __device__ bool half_has_slash(int h, int w) const {
-    if (!ex[h]) return false;
-    const int j0 = 128 * w;
-    const int jhi = min(j0 + 127, e[h]);
-    if (j0 > jhi) return false;
-    if (L[h] == 64) return bits_any5(cover, 32 * cw, n - 1 - a[h] + j0, n - 1 - a[h] + jhi);
-    return bits_any(dbits, n, a[h] - jhi, a[h] - j0 + L[h] - 1);
-  }
-  __device__ void load_group(int lane) {
+  __device__ void load_group(int lane, int n) {
     grp += 32;
-    const int w = grp + lane;
-    bool s = false, c = false;
-    if (w < M) {
-      s = half_has_slash(0, w) | half_has_slash(1, w);
-      c = !s && bits_any5(cbits, n, 128 * w, min(128 * w + 127, hi_key));
+    const int b = grp + lane;
+    bool sl = false, cols = false;
+    if (b < NB) {
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const int base = 64 * b + 32 * w;
+        const uint32_t kin = keys_below(base, hi_key + 1);
+        cf[0][w] = base <= hi_key ? __ldg(cbits[0] + (base >> 5)) & kin : 0u;
+        cf[1][w] = two ? (base <= hi_key ? __ldg(cbits[1] + (base >> 5)) & kin : 0u) : cf[0][w];
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+          uint32_t s = 0u;
+          if (ex[hh] && base <= e[hh]) {
+            s = L[hh] == 64 ? bits_window32(cover[hh >> 1], cw, n - 1 - a[hh] + base)
+                            : exact_cover32(dbits[hh >> 1], nw, a[hh] - base, L[hh]);
+            s &= keys_below(base, e[hh] + 1);
+          }
+          m[hh][w] = s;
+          sl = sl || s != 0u;
+        }
+      }
+      if (sl) {
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+#pragma unroll
+          for (int w = 0; w < 2; ++w)
+            if (ex[hh]) m[hh][w] |= cf[hh >> 1][w] & keys_below(64 * b + 32 * w, e[hh] + 1);
+      }
+      cols = !sl && (cf[0][0] | cf[0][1] | cf[1][0] | cf[1][1]) != 0u;
     }
-    smask = __ballot_sync(0xFFFFFFFFu, s);
-    cmask = __ballot_sync(0xFFFFFFFFu, c);
+    rmask = __ballot_sync(0xFFFFFFFFu, sl);
+    cmask = __ballot_sync(0xFFFFFFFFu, cols);
   }
-  __device__ void range_masks(int w, int lane, TileDesc& d) const {
-    const int j0 = 128 * w;
-    for (int h = 0; h < 2; ++h) {
-      if (ex[h] && L[h] != 64) {  // partial last block: test each key (whole warp)
-        for (int q = 0; q < 4; ++q) {
-          const int j = j0 + 32 * q + lane;
-          const bool ok = j <= e[h] && (bit_at(cbits, j) || bits_any(dbits, n, a[h] - j, a[h] - j + L[h] - 1));
-          const uint32_t b = __ballot_sync(0xFFFFFFFFu, ok);
-          if (lane == 0) d.mask[h][q] = b;
-        }
-      } else if ((lane >> 2) == h) {  // lanes 4h .. 4h+3: one mask word each
-        const int q = lane & 3;
-        const int base = j0 + 32 * q;
-        uint32_t m = 0u;
-        if (ex[h] && base <= e[h]) {
-          m = bits_window32(cover, cw, n - 1 - a[h] + base) | __ldg(cbits + (base >> 5));
-          m &= keys_below(base, e[h] + 1);
-        }
-        d.mask[h][q] = m;
+  // Block grp+b (its masks live in lane b) becomes segment s of d.
+  __device__ void put_segment(int lane, int b, int s, TileDesc& d) const {
+    if (lane == b) {
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        d.mask[hh][2 * s] = m[hh][0];
+        d.mask[hh][2 * s + 1] = m[hh][1];
+      }
+      d.seg[s] = 64 * (grp + b);
+    }
+  }
+  __device__ static void finish_range(int lane, TileDesc& d, bool single) {
+    __syncwarp();
+    if (lane == 0) {
+      if (single) {  // reload the same segment, masked
+        d.seg[1] = d.seg[0];
+        for (int hh = 0; hh < 4; ++hh) d.mask[hh][2] = d.mask[hh][3] = 0u;
+      }
+      d.kind = kTileRange;
+      for (int X = 0; X < 2; ++X) {
+        uint32_t any = 0;
+        for (int q = 0; q < 4; ++q) any |= d.mask[2 * X][q] | d.mask[2 * X + 1][q];
+        d.active[X] = any != 0u;
+        d.rule[X][0] = d.rule[X][1] = 0;
       }
     }
-    if (lane == 0) { d.seg[0] = j0; d.seg[1] = j0 + 64; d.kind = kTileRange; d.rule = 0; }
+  }
+  // Append the columns of block grp+b (ascending) to the staging list.
+  __device__ void stage_block(int lane, int b, int* stage) {
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const uint32_t w0 = __shfl_sync(0xFFFFFFFFu, cf[0][w], b);
+      const uint32_t w1 = __shfl_sync(0xFFFFFFFFu, cf[1][w], b);
+      const uint32_t in0 = (w0 >> lane) & 1u, in1 = (w1 >> lane) & 1u;
+      const bool ok = (in0 | in1) != 0u;
+      const uint32_t bb = __ballot_sync(0xFFFFFFFFu, ok);
+      if (ok)
+        stage[staged + __popc(bb & ((1u << lane) - 1u))] =
+            (64 * (grp + b) + 32 * w + lane) | (int)(in0 << 28) | (int)(in1 << 29);
+      staged += __popc(bb);
+    }
+    __syncwarp();
   }
   __device__ void gather_tile(int lane, int* stage, TileDesc& d) {
     const int take = staged < 128 ? staged : 128;
-    for (int k = lane; k < 128; k += 32) d.gidx[k] = k < take ? stage[k] : -1;
-    __syncwarp();
-    for (int h = 0; h < 2; ++h)
-      for (int q = 0; q < 4; ++q) {
-        const int g = d.gidx[32 * q + lane];
-        const bool ok = ex[h] && g >= 0 && g <= e[h];
-        const uint32_t b = __ballot_sync(0xFFFFFFFFu, ok);
-        if (lane == 0) d.mask[h][q] = b;
+    uint32_t mk[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int k = 32 * q + lane;
+      const int s = k < take ? stage[k] : 0;
+      const int key = s & 0x0FFFFFFF;
+      d.gidx[k] = k < take ? key : -1;
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) {
+        const bool ok = ex[hh] && k < take && key <= e[hh] && ((s >> (28 + (hh >> 1))) & 1);
+        mk[hh][q] = __ballot_sync(0xFFFFFFFFu, ok);
       }
+    }
+    __syncwarp();
     // shift the rest of the staging list down (rest < take, so the ranges do not overlap)
     const int rest = staged - take;
     for (int k = lane; k < rest; k += 32) stage[k] = stage[take + k];
     __syncwarp();
     staged = rest;
-    if (lane == 0) { d.kind = kTileGather; d.rule = 0; d.seg[0] = 0; d.seg[1] = 0; }
+    if (lane == 0) {
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d.mask[hh][q] = mk[hh][q];
+      d.kind = kTileGather;
+      d.seg[0] = d.seg[1] = 0;
+#pragma unroll
+      for (int X = 0; X < 2; ++X) {
+        uint32_t any = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) any |= mk[2 * X][q] | mk[2 * X + 1][q];
+        d.active[X] = any != 0u;
+        d.rule[X][0] = d.rule[X][1] = 0;
+      }
+    }
   }
-  // Produce the next tile into d (whole warp); false when the item has no more tiles.
-  __device__ bool emit(int lane, int* stage, TileDesc& d) {
+  // Produce the next tile into d; false when the item has no more tiles.
+  __device__ bool emit(int lane, int n, int* stage, TileDesc& d) {
+    int filled = 0;  // range segments already placed in d
     for (;;) {
-      if (staged >= 128) { gather_tile(lane, stage, d); return true; }
-      if ((smask | cmask) == 0u) {
-        if (grp + 32 >= M) {
+      if (staged >= 128) {
+        if (filled == 0) { gather_tile(lane, stage, d); return true; }
+        finish_range(lane, d, true);
+        return true;
+      }
+      if ((rmask | cmask) == 0u) {
+        if (grp + 32 >= NB) {
+          if (filled == 1) { finish_range(lane, d, true); return true; }
           if (staged > 0) { gather_tile(lane, stage, d); return true; }
           return false;
         }
-        load_group(lane);
+        load_group(lane, n);
         continue;
       }
-      const int b = __ffs(smask | cmask) - 1;
-      const bool is_slash = (smask >> b) & 1u;
-      smask &= ~(1u << b);
+      const int b = __ffs(rmask | cmask) - 1;
+      const bool is_range = (rmask >> b) & 1u;
+      rmask &= ~(1u << b);
       cmask &= ~(1u << b);
-      const int w = grp + b;
-      if (is_slash) { range_masks(w, lane, d); return true; }
-      // stage this window's columns (ascending)
-      const int j0 = 128 * w;
-      for (int q = 0; q < 4; ++q) {
-        const int j = j0 + 32 * q + lane;
-        const bool ok = j <= hi_key && bit_at(cbits, j);
-        const uint32_t bb = __ballot_sync(0xFFFFFFFFu, ok);
-        if (ok) stage[staged + __popc(bb & ((1u << lane) - 1u))] = j;
-        staged += __popc(bb);
+      if (is_range) {
+        put_segment(lane, b, filled, d);
+        if (++filled == 2) { finish_range(lane, d, false); return true; }
+      } else {
+        stage_block(lane, b, stage);
       }
-      __syncwarp();
     }
   }
 };
@@ -463,8 +545,9 @@ struct VSIter {
 // ------------------------------------------------------------------ kernel
 template <int D, bool kCount>
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                       const AttnArgs A, const __grid_constant__ UnitTable UT) {
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const AttnArgs A,
+                       const __grid_constant__ UnitTable UT) {
   using Ly = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -472,39 +555,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   TileDesc* descs = reinterpret_cast<TileDesc*>(sm + Ly::kDesc);
   int* stage = reinterpret_cast<int*>(sm + Ly::kStage);
   int* sblk = reinterpret_cast<int*>(sm + Ly::kBlk);
-  float* xchg = reinterpret_cast<float*>(sm + Ly::kXchg);
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + Ly::kMisc);  // [0] tmem, [2] abort
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item_id = blockIdx.x;
-  const int t = A.T - 1 - item_id / A.n_units;
-  const Unit& U = UT.u[item_id % A.n_units];
+  int rem = blockIdx.x, band = 0;
+  while (band + 1 < A.n_bands && rem >= (UT.band[band + 1] - UT.band[band]) * A.T) {
+    rem -= (UT.band[band + 1] - UT.band[band]) * A.T;
+    ++band;
+  }
+  const int band_units = UT.band[band + 1] - UT.band[band];
+  const int t = A.T - 1 - rem / band_units;
+  const Unit& U = UT.u[UT.band[band] + rem % band_units];
   const int n = A.n;
-  const Item it = make_item(U, t, n);
+  const Geo G = make_geo(U, t, n, A.nqt);
 
   if (warp == 0) {
     tmem_alloc(const_cast<uint32_t*>(&misc[0]), kTmemCols);
     tmem_relinquish();
   }
   if (threadIdx.x == 32 * kMmaWarp) {
-    mbar_init(&bars[kBarQ], kSoftWarps);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars[kBarKFull + s], 1);
-      mbar_init(&bars[kBarKEmpty + s], 1);
-      mbar_init(&bars[kBarVFull + s], 1);
-      mbar_init(&bars[kBarVEmpty + s], 1);
+    mbar_init(&bars[kBarQ], 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&bars[kBarFull + s], 1);
+      mbar_init(&bars[kBarEmpty + s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars[kBarSFull + s], 1);
-      mbar_init(&bars[kBarSEmpty + s], kSoftWarps);
+    for (int X = 0; X < 2; ++X) {
+      mbar_init(&bars[kBarSFull + X], 1);
+      mbar_init(&bars[kBarPFull + X], 4);
     }
-    mbar_init(&bars[kBarPFull], kSoftWarps);
-    mbar_init(&bars[kBarPEmpty], 1);
+    mbar_init(&bars[kBarODone], 1);
     for (int s = 0; s < kDescSlots; ++s) {
       mbar_init(&bars[kBarDFull + s], 1);
       mbar_init(&bars[kBarDEmpty + s], kDescReaders);
     }
-    for (int s = 0; s < 4; ++s) mbar_init(&bars[kBarX + s], 64);
     misc[2] = 0;
     fence_mbar_init();
   }
@@ -513,8 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
-  uint8_t* sK = sm + Ly::kK;
-  uint8_t* sV = sm + Ly::kV;
+  uint8_t* sQ = sm + Ly::kQ;
+  uint8_t* sR = sm + Ly::kRing;
   auto desc_full = [&](int j) { return mbar_wait(&bars[kBarDFull + j % kDescSlots], (j / kDescSlots) & 1); };
   auto desc_release = [&](int j) {
     __syncwarp();
@@ -523,13 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kPlannerWarp) {
     // ------------------------------------------------------------ planner
-    AshapeIter ai;
-    BlockIter bi;
-    VSIter vi;
-    int T = 0;
-    if (U.pattern == kUnitAshape) { ai.init(U, it, n); T = ai.count(); }
-    else if (U.pattern == kUnitBlock) bi.init(U, it, A, lane, sblk);
-    else vi.init(U, it, A);
+    AshapeSeg as;
+    BlockSeg bs;
+    VSSeg vw;
+    if (U.pattern == kUnitAshape) as.init(U, G, n);
+    else if (U.pattern == kUnitBlock) bs.init(U, G, A, lane, sblk);
+    else vw.init(U, G, A);
     bool ok = true;
     for (int j = 0;; ++j) {
       if (misc[2]) { ok = false; break; }
@@ -538,14 +620,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileDesc& d = descs[slot];
       bool more;
       if (U.pattern == kUnitVS) {
-        more = vi.emit(lane, stage, d);
-      } else if (U.pattern == kUnitAshape) {
-        more = j < T;
-        if (more && lane == 0) ai.emit(j, n, d);
+        more = vw.emit(lane, n, stage, d);
       } else {
-        more = !bi.done();  // the cursor advances in lane 0 only: its answer is the warp's
-        more = __shfl_sync(0xFFFFFFFFu, more, 0);
-        if (more && lane == 0) bi.emit(n, d, A.err);
+        // lane 0 takes up to two segments of the union
+        int sg[2] = {0, 0}, rl[2][2] = {{0, 0}, {0, 0}}, bits[2] = {0, 0};
+        int got = 0;
+        if (lane == 0) {
+          for (; got < 2; ++got) {
+            int s = 0, r2[2] = {0, 0}, b = 0;
+            bool has;
+            if (U.pattern == kUnitAshape) {
+              has = as.next(s, r2);
+              if (has) b = (r2[0] ? 3 : 0) | (r2[1] ? 12 : 0);
+            } else {
+              has = bs.next(s, b);
+              if (has && b < 0) { b = 0; set_error(A.err, kErrIndex); }
+              if (has)
+                for (int hh = 0; hh < 4; ++hh)  // a block must be causal for each half that keeps it
+                  if (((b >> hh) & 1) && (s < 0 || s > bs.u[hh])) { b &= ~(1 << hh); set_error(A.err, kErrIndex); }
+              if (has && (s < 0 || 64 * s >= n)) { s = 0; b = 0; }
+            }
+            if (!has) break;
+            sg[got] = s;
+            rl[0][got] = r2[0];
+            rl[1][got] = r2[1];
+            bits[got] = b;
+          }
+        }
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        more = got > 0;
+        if (more && lane == 0) {
+          if (got == 1) { sg[1] = sg[0]; bits[1] = 0; rl[0][1] = rl[1][1] = 0; }  // reload a valid segment, masked
+          d.kind = kTileRange;
+          for (int s = 0; s < 2; ++s) {
+            d.seg[s] = 64 * sg[s];
+            for (int w = 0; w < 2; ++w) {
+              const uint32_t m = keys_below(64 * sg[s] + 32 * w, n);
+              for (int hh = 0; hh < 4; ++hh) d.mask[hh][2 * s + w] = ((bits[s] >> hh) & 1) ? m : 0u;
+            }
+          }
+          for (int X = 0; X < 2; ++X) {
+            d.rule[X][0] = (uint8_t)rl[X][0];
+            d.rule[X][1] = (uint8_t)rl[X][1];
+            d.active[X] = (((bits[0] | bits[1]) >> (2 * X)) & 3) != 0;
+          }
+        }
       }
       if (!more && lane == 0) d.kind = kTileEnd;
       __syncwarp();
@@ -556,17 +675,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kLoaderWarp) {
     // ------------------------------------------------------------ loader
     if (lane == 0) {
+      tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
+      // Q rows of the halves that exist (a tail past n reads zeros)
+      int halves = 0;
+      for (int hh = 0; hh < 4; ++hh) halves += G.ex[hh];
+      mbar_arrive_expect_tx(&bars[kBarQ], (uint32_t)(halves * (D / 64) * 8192));
+      for (int hh = 0; hh < 4; ++hh)
+        if (G.ex[hh])
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sQ + (hh >> 1) * Ly::kTile + c * 16384 + (hh & 1) * 8192, &tq, &bars[kBarQ], 64 * c,
+                        G.row0[hh], U.sub[hh >> 1].qh[hh & 1]);
     }
-    auto load_kv = [&](int j, bool is_v) -> bool {
-      const int st = j % kStages;
-      const uint32_t ph = ((j / kStages) & 1) ^ 1;
-      uint64_t* empty = &bars[(is_v ? kBarVEmpty : kBarKEmpty) + st];
-      uint64_t* full = &bars[(is_v ? kBarVFull : kBarKFull) + st];
-      if (!mbar_wait(empty, ph)) return false;
+    // K(j) into slot 2j, V(j) into 2j+1 (mod kSlots): the MMA releases them in that order
+    auto load = [&](int j, bool is_v) -> bool {
+      const int idx = 2 * j + (is_v ? 1 : 0);
+      const int st = idx % kSlots;
+      if (!mbar_wait(&bars[kBarEmpty + st], ((idx / kSlots) & 1) ^ 1)) return false;
       const TileDesc& d = descs[j % kDescSlots];
-      uint8_t* dst = (is_v ? sV : sK) + st * Ly::kTile;
+      uint8_t* dst = sR + st * Ly::kTile;
+      uint64_t* full = &bars[kBarFull + st];
       if (d.kind == kTileRange) {
         if (lane == 0) {
           const CUtensorMap* map = is_v ? &tv : &tk;
@@ -578,8 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // gather single key rows (16-byte cp.async) into the swizzled layout
         constexpr int kChunks16 = D / 8;
         const uint8_t* gbase = reinterpret_cast<const uint8_t*>(is_v ? A.v : A.k) + (int64_t)U.kvh * n * D * 2;
-        for (int idx = lane; idx < 128 * kChunks16; idx += 32) {
-          const int r = idx / kChunks16, c16 = idx % kChunks16;
+        for (int x = lane; x < 128 * kChunks16; x += 32) {
+          const int r = x / kChunks16, c16 = x % kChunks16;
           int key = d.gidx[r];
           key = key < 0 ? 0 : key;  // empty columns reload key 0 (finite data, masked)
           cp_async16(dst + (c16 >> 3) * 16384 + sw128_offset(r, c16 & 7), gbase + ((int64_t)key * D + 8 * c16) * 2);
@@ -591,19 +720,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    // K runs one tile ahead of V; a descriptor is released once its V is issued
     bool ok = true;
-    int j = 0;
-    for (;; ++j) {
+    for (int j = 0;; ++j) {
       if (misc[2]) { ok = false; break; }
       if (!desc_full(j)) { ok = false; break; }
-      const bool end = descs[j % kDescSlots].kind == kTileEnd;
-      if (!end && !load_kv(j, false)) { ok = false; break; }
-      if (j > 0) {
-        if (!load_kv(j - 1, true)) { ok = false; break; }
-        desc_release(j - 1);
-      }
-      if (end) { desc_release(j); break; }
+      if (descs[j % kDescSlots].kind == kTileEnd) { desc_release(j); break; }
+      if (!load(j, false) || !load(j, true)) { ok = false; break; }
+      desc_release(j);
     }
     if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
   } else if (warp == kMmaWarp) {
@@ -611,215 +734,233 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = mbar_wait(&bars[kBarQ], 0);
     constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
-    auto pv = [&](int j) -> bool {
-      const int st = j % kStages;
-      if (!mbar_wait(&bars[kBarPFull], j & 1)) return false;
-      if (!mbar_wait(&bars[kBarVFull + st], (j / kStages) & 1)) return false;
+    int pending[2] = {-1, -1};  // tile whose PV is owed, per sub-item (always the previous tile)
+    int pv_last[2] = {0, 0};    // that PV is the last reader of its V slot
+    int done[2] = {0, 0};       // PVs issued per sub-item (the first one overwrites O)
+    int pphase[2] = {0, 0};
+    auto issue_pv = [&](int X) -> bool {
+      const int vidx = 2 * pending[X] + 1, vst = vidx % kSlots;
+      if (!mbar_wait(&bars[kBarPFull + X], pphase[X] & 1)) return false;
+      ++pphase[X];
+      if (!mbar_wait(&bars[kBarFull + vst], (vidx / kSlots) & 1)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t v0 = smem_u32(sV + st * Ly::kTile);
+        const uint32_t v0 = smem_u32(sR + vst * Ly::kTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * kk, sdesc_sw128(v0 + kk * 2048, 16384, 1024), id_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars[kBarVEmpty + st]);
-        mma_commit(&bars[kBarPEmpty]);
+          mma_bf16_ts(tmem + kColO + 128 * X, tmem + kColS + 128 * X + 8 * kk, sdesc_sw128(v0 + kk * 2048, 16384, 1024),
+                      id_pv, (done[X] > 0 || kk > 0) ? 1u : 0u);
+        if (pv_last[X]) mma_commit(&bars[kBarEmpty + vst]);
       }
       __syncwarp();
+      ++done[X];
+      pending[X] = -1;
       return true;
     };
     if (ok) tc_fence_after();
-    int j = 0;
-    for (; ok; ++j) {
-      if (misc[2]) { ok = false; break; }
-      if (!desc_full(j)) { ok = false; break; }
-      const bool end = descs[j % kDescSlots].kind == kTileEnd;
+    for (int j = 0; ok; ++j) {
+      if (misc[2] || !desc_full(j)) { ok = false; break; }
+      const TileDesc& d = descs[j % kDescSlots];
+      const bool end = d.kind == kTileEnd;
+      const int act[2] = {d.active[0], d.active[1]};
       desc_release(j);
       if (end) break;
-      const int st = j % kStages, sb = j & 1;
-      ok = mbar_wait(&bars[kBarKFull + st], (j / kStages) & 1) &&
-           mbar_wait(&bars[kBarSEmpty + sb], ((j >> 1) & 1) ^ 1);
-      if (!ok) break;
+      const int kidx = 2 * j, kst = kidx % kSlots;
+      if (!mbar_wait(&bars[kBarFull + kst], (kidx / kSlots) & 1)) { ok = false; break; }
       tc_fence_after();
-      if (lane == 0) {
-        const uint32_t k0 = smem_u32(sK + st * Ly::kTile);
+      for (int X = 0; X < 2; ++X) {
+        if (pending[X] >= 0 && !issue_pv(X)) { ok = false; break; }  // P_X of the previous tile -> O_X
+        if (!act[X]) continue;
+        if (lane == 0) {
+          const uint32_t q0 = smem_u32(sQ + X * Ly::kTile), k0 = smem_u32(sR + kst * Ly::kTile);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ts(tmem + kColS + 128 * sb, tmem + kColQ + 8 * kk, sdesc_sw128(k0 + off, 16, 1024), id_qk,
-                      kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16_ss(tmem + kColS + 128 * X, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024),
+                        id_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[kBarSFull + X]);
         }
-        mma_commit(&bars[kBarSFull + sb]);
-        mma_commit(&bars[kBarKEmpty + st]);
+        __syncwarp();
+        pending[X] = j;
+        pv_last[X] = (X == 1) || !act[1];
       }
+      if (!ok) break;
+      if (!act[0] && !act[1]) {  // V(j) has no reader: release its slot once it has landed
+        const int vidx = 2 * j + 1;
+        if (!mbar_wait(&bars[kBarFull + vidx % kSlots], (vidx / kSlots) & 1)) { ok = false; break; }
+        if (lane == 0) mma_commit(&bars[kBarEmpty + vidx % kSlots]);
+      }
+      if (lane == 0) mma_commit(&bars[kBarEmpty + kst]);  // K(j) consumed
       __syncwarp();
-      if (j > 0) ok = pv(j - 1);
     }
-    if (ok && j > 0) ok = pv(j - 1);
+    for (int X = 0; X < 2 && ok; ++X)
+      if (pending[X] >= 0 && !issue_pv(X)) ok = false;
+    if (lane == 0) mma_commit(&bars[kBarODone]);  // arrives once every MMA issued above has completed
+    __syncwarp();
     if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
   } else {
-    // ------------------------------------------------------------ softmax warps
-    const int quarter = warp & 3;          // TMEM lanes 32*quarter ..
-    const int ch = warp >> 2;              // key half of each tile (and O / Q column half)
-    const int r = quarter * 32 + lane;     // tile row = TMEM lane
-    const int h = r >> 6;
-    const int i = it.row0[h] + (r & 63);
-    const bool row_ok = i < n;
+    // ------------------------------------------------------------ softmax (sub-item X)
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter ..
+    const int X = warp >> 2;
+    const int r = quarter * 32 + lane;  // tile row = TMEM lane
+    const int hh = 2 * X + (r >> 6);
+    const int i = G.row0[hh] + (r & 63);
+    const bool row_ok = G.ex[hh] && i < n;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t colS = kColS + 128 * X, colO = kColO + 128 * X;
     const float c2 = A.scale_log2;
-    const int g = U.sink, wnd = U.window;
-    uint64_t* xbar = &bars[kBarX + quarter];  // warps quarter and quarter+4, one phase per exchange
+    const int g = U.sub[X].sink, wnd = U.sub[X].window;
+    const bool ashape = U.pattern == kUnitAshape;
     float m_used = -INFINITY, l = 0.f;
     unsigned long long count = 0;
     bool ok = true;
+    int mine = 0;  // tiles this sub-item has processed
 
-    // ---- Q row into TMEM (A operand of S = Q K^T): 32 columns of bf16 pairs per writer
-    if (D == 128 || ch == 0) {
-      const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(A.q) + ((int64_t)U.qh[h] * n + i) * D;
-      const int e0 = D == 128 ? ch * 64 : 0;
-      uint32_t qw[32];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        uint4 v4 = make_uint4(0, 0, 0, 0);
-        if (row_ok) v4 = __ldg(reinterpret_cast<const uint4*>(qrow + e0) + x);
-        qw[4 * x] = v4.x; qw[4 * x + 1] = v4.y; qw[4 * x + 2] = v4.z; qw[4 * x + 3] = v4.w;
-      }
-      tmem_st32(tmem + lane_base + kColQ + (D == 128 ? 32 * ch : 0), qw);
-    }
-    tmem_st_wait();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars[kBarQ]);
-
-    int j = 0;
-    for (;; ++j) {
+    for (int j = 0;; ++j) {
       if (misc[2]) { ok = false; break; }
-      // ---- tile descriptor -> validity word of this thread's 64 keys
       if (!desc_full(j)) { ok = false; break; }
       const TileDesc& d = descs[j % kDescSlots];
-      if (d.kind == kTileEnd) { desc_release(j); break; }
-      uint64_t vw = 0ull;
+      const int kind = d.kind;
+      if (kind == kTileEnd) { desc_release(j); break; }
+      if (!d.active[X]) { desc_release(j); continue; }
+      // ---- validity words of this row's 128 keys
+      uint64_t vw[2] = {0ull, 0ull};
       if (row_ok) {
-        const uint64_t m64 = ((uint64_t)d.mask[h][2 * ch + 1] << 32) | d.mask[h][2 * ch];
-        if (d.kind == kTileRange) {
-          const int base = d.seg[ch];
-          vw = m64 & low_mask64(i - base + 1);  // causal: j <= i
-          if (d.rule) {
-            uint64_t keep = 0;
-            if (d.rule & 1) keep |= low_mask64(g - base);             // j < g
-            if (d.rule & 2) keep |= ~low_mask64(i - wnd + 1 - base);  // j > i - w
-            vw &= keep;
+        int cg = 0;  // gather tiles: columns k < cg hold keys <= i (keys ascend, -1 last)
+        if (kind == kTileGather) {
+          int lo = 0, hi = 128;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            const int gj = d.gidx[mid];
+            if (gj >= 0 && gj <= i) lo = mid + 1;
+            else hi = mid;
           }
-        } else {
-          for (int k = 0; k < 64; ++k) {
-            const int gj = d.gidx[64 * ch + k];
-            if (((m64 >> k) & 1ull) && gj >= 0 && gj <= i) vw |= 1ull << k;
+          cg = lo;
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const uint64_t m64 = ((uint64_t)d.mask[hh][2 * s + 1] << 32) | d.mask[hh][2 * s];
+          if (kind == kTileRange) {
+            const int base = d.seg[s];
+            uint64_t v = m64 & low_mask64(i - base + 1);  // causal: j <= i
+            if (ashape) {
+              const int rule = d.rule[X][s];
+              uint64_t keep = 0;
+              if (rule & 1) keep |= low_mask64(g - base);             // j < g
+              if (rule & 2) keep |= ~low_mask64(i - wnd + 1 - base);  // j > i - w
+              v &= keep;
+            }
+            vw[s] = v;
+          } else {
+            vw[s] = m64 & low_mask64(cg - 64 * s);
           }
         }
       }
       desc_release(j);
-      if (kCount) count += __popcll(vw);
+      if (kCount) count += __popcll(vw[0]) + __popcll(vw[1]);
 
-      // ---- S tile (this thread's 64 keys) from TMEM
-      const int sb = j & 1;
-      if (!mbar_wait(&bars[kBarSFull + sb], (j >> 1) & 1)) { ok = false; break; }
+      // ---- S of this tile (its completion also means this sub-item's previous PV is done)
+      if (!mbar_wait(&bars[kBarSFull + X], mine & 1)) { ok = false; break; }
       tc_fence_after();
-      float sv[64];
+      float sv[128];
       {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(tmem + lane_base + kColS + 128 * sb + 64 * ch, u0);
-        tmem_ld32(tmem + lane_base + kColS + 128 * sb + 64 * ch + 32, u1);
+        uint32_t* u = reinterpret_cast<uint32_t*>(sv);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tmem + lane_base + colS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(u + 32 * c));
         tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          sv[k] = __uint_as_float(u0[k]);
-          sv[32 + k] = __uint_as_float(u1[k]);
-        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarSEmpty + sb]);
-
-      // ---- mask, row max (tree), exchanged with the partner warp
-      if (~vw) {
+      // ---- mask, row max (tree)
+      if ((~vw[0]) | (~vw[1])) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) sv[k] = ((vw >> k) & 1ull) ? sv[k] : -INFINITY;
+        for (int k = 0; k < 64; ++k) sv[k] = ((vw[0] >> k) & 1ull) ? sv[k] : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 64; ++k) sv[64 + k] = ((vw[1] >> k) & 1ull) ? sv[64 + k] : -INFINITY;
       }
       float mx[8];
 #pragma unroll
-      for (int x = 0; x < 8; ++x) mx[x] = fmaxf(sv[x], sv[x + 8]);
+      for (int x = 0; x < 8; ++x) mx[x] = max3f(sv[x], sv[8 + x], sv[16 + x]);
 #pragma unroll
-      for (int k = 16; k < 64; k += 8)
+      for (int k = 24; k < 120; k += 16)
 #pragma unroll
-        for (int x = 0; x < 8; ++x) mx[x] = fmaxf(mx[x], sv[k + x]);
-      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      float* xc = xchg + (j & 1) * 256;
-      xc[ch * 128 + r] = mt;
-      mbar_arrive(xbar);
-      if (!mbar_wait(xbar, j & 1)) { ok = false; break; }
-      mt = fmaxf(mt, xc[(ch ^ 1) * 128 + r]);
-
+        for (int x = 0; x < 8; ++x) mx[x] = max3f(mx[x], sv[k + x], sv[k + 8 + x]);
+#pragma unroll
+      for (int x = 0; x < 8; ++x) mx[x] = fmaxf(mx[x], sv[120 + x]);
+      const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       const float m_new = fmaxf(m_used, mt * c2);
       const bool need = m_new > m_used + kRescaleThreshold;
-      const bool any = __any_sync(0xFFFFFFFFu, need);  // the partner warp sees the same rows
+      const bool any = __any_sync(0xFFFFFFFFu, need);
       float alpha = 1.f;
       if (any && m_new != -INFINITY) {
         alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_new);
         m_used = m_new;
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
+      const uint64_t c2x2 = pk2(c2, c2), negm = pk2(-mref, -mref);
+      uint64_t acc[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};
+      // ---- P over the first 64 columns of S, 32 columns at a time
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float p0 = ex2(fmaf(sv[2 * k], c2, -mref));
-        const float p1 = ex2(fmaf(sv[2 * k + 1], c2, -mref));
-        rs[k & 3] += p0 + p1;
-        pk[k] = pack_bf16x2(p0, p1);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int e = 64 * half + 2 * k;
+          const uint64_t x = fma2(pk2(sv[e], sv[e + 1]), c2x2, negm);
+          uint64_t p;
+          if ((k & 7) >= 8 - kPolyPairs) {
+            p = exp2_poly2(x);
+          } else {
+            float x0, x1;
+            up2(x, x0, x1);
+            p = pk2(ex2(x0), ex2(x1));
+          }
+          acc[k & 1] = add2(acc[k & 1], p);
+          float p0, p1;
+          up2(p, p0, p1);
+          pk[k] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tmem + lane_base + colS + 32 * half, pk);
       }
-      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-
-      // ---- PV(j-1) must be done before P is overwritten or O is rescaled
-      if (j > 0 && !mbar_wait(&bars[kBarPEmpty], (j - 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      if (any && j > 0) {
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+      {
+        float a0, a1, a2, a3;
+        up2(acc[0], a0, a1);
+        up2(acc[1], a2, a3);
+        l = l * alpha + ((a0 + a1) + (a2 + a3));
+      }
+      // ---- rescale O_X (its previous PV completed before S was ready; the next waits for P)
+      if (any && mine > 0) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          const uint32_t col = kColO + (D / 2) * ch + 32 * c;
-          tmem_ld32(tmem + lane_base + col, o);
+          tmem_ld32(tmem + lane_base + colO + 32 * c, o);
           tmem_ld_wait();
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-          tmem_st32(tmem + lane_base + col, o);
+          tmem_st32(tmem + lane_base + colO + 32 * c, o);
         }
       }
-      tmem_st32(tmem + lane_base + kColP + 32 * ch, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarPFull]);
+      if (lane == 0) mbar_arrive(&bars[kBarPFull + X]);
+      ++mine;
     }
     if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
-    const int T = j;  // tiles processed
 
-    // ---- epilogue: O / l, LSE (the pair adds its partial denominators)
-    const int qh = U.qh[h];
-    if (ok && T > 0) {
-      if (!mbar_wait(&bars[kBarPEmpty], (T - 1) & 1)) { ok = false; misc[2] = 1; set_error(A.err, kErrTimeout); }
-      tc_fence_after();
-    }
-    xchg[512 + ch * 128 + r] = l;
-    mbar_arrive(xbar);
-    if (!mbar_wait(xbar, T & 1)) { ok = false; misc[2] = 1; set_error(A.err, kErrTimeout); }
-    l += xchg[512 + (ch ^ 1) * 128 + r];
-    const float inv_l = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(A.o) + ((int64_t)qh * n + i) * D + (D / 2) * ch;
-#pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
+    // ---- epilogue: O / l, LSE
+    if (!mbar_wait(&bars[kBarODone], 0)) { ok = false; misc[2] = 1; set_error(A.err, kErrTimeout); }
+    tc_fence_after();
+    const int qh = U.sub[X].qh[hh & 1];
+    const bool empty = !(m_used > -INFINITY);  // no attended key in any tile: o = 0
+    const float inv_l = (!empty && l > 0.f) ? 1.f / l : 0.f;
+    const bool have = ok && mine > 0;  // warp-uniform: tcgen05.ld below is warp-collective
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(A.o) + ((int64_t)qh * n + i) * D;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
-      if (ok && T > 0) {
-        tmem_ld32(tmem + lane_base + kColO + (D / 2) * ch + 32 * c, o);
+      if (have) {
+        tmem_ld32(tmem + lane_base + colO + 32 * c, o);
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -835,9 +976,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 4; ++x) dst[x] = make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
       }
     }
-    if (row_ok && A.lse && ch == 0)
-      A.lse[(int64_t)qh * n + i] = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-    if (kCount && A.edges) {
+    if (row_ok && A.lse)
+      A.lse[(int64_t)qh * n + i] = (!empty && l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    if (kCount && A.edges) {  // the 32 rows of a warp lie in one half, so in one head
       unsigned long long c = count;
       for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
       if (lane == 0 && c) atomicAdd(A.edges + qh, c);
@@ -853,8 +994,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, bool kCount>
-msa_status launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, const UnitTable& ut,
-                       cudaStream_t stream) {
+msa_status launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
+                       const UnitTable& ut, cudaStream_t stream) {
   auto kern = sparse_attn_kernel<D, kCount>;
   const int smem = Layout<D>::kAlloc;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -862,7 +1003,7 @@ msa_status launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const AttnA
   const int64_t items = (int64_t)a.T * a.n_units;
   if (items <= 0) return MSA_OK;
   if (items > 0x7FFFFFFF) return MSA_ERR_UNSUPPORTED;
-  kern<<<(unsigned)items, kThreads, smem, stream>>>(tk, tv, a, ut);
+  kern<<<(unsigned)items, kThreads, smem, stream>>>(tq, tk, tv, a, ut);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
@@ -871,19 +1012,24 @@ msa_status launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const AttnA
 
 msa_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const AttnArgs& args, const Unit* units, int n_units, cudaStream_t stream) {
-  (void)tq;  // Q rows are read by the softmax warps straight into TMEM
   for (int base = 0; base < n_units; base += kMaxUnits) {
     UnitTable ut;
     const int cnt = n_units - base < kMaxUnits ? n_units - base : kMaxUnits;
     for (int x = 0; x < cnt; ++x) ut.u[x] = units[base + x];
+    std::stable_sort(ut.u, ut.u + cnt, [](const Unit& p, const Unit& q) { return p.kvh < q.kvh; });
+    int nb = 0;
+    for (int x = 0; x < cnt; ++x)
+      if (x == 0 || ut.u[x].kvh != ut.u[x - 1].kvh) ut.band[nb++] = x;
+    ut.band[nb] = cnt;
     AttnArgs a = args;
     a.n_units = cnt;
+    a.n_bands = nb;
     msa_status st;
     const bool count = args.edges != nullptr;
     if (args.d == 128)
-      st = count ? launch_impl<128, true>(tk, tv, a, ut, stream) : launch_impl<128, false>(tk, tv, a, ut, stream);
+      st = count ? launch_impl<128, true>(tq, tk, tv, a, ut, stream) : launch_impl<128, false>(tq, tk, tv, a, ut, stream);
     else
-      st = count ? launch_impl<64, true>(tk, tv, a, ut, stream) : launch_impl<64, false>(tk, tv, a, ut, stream);
+      st = count ? launch_impl<64, true>(tq, tk, tv, a, ut, stream) : launch_impl<64, false>(tq, tk, tv, a, ut, stream);
     if (st != MSA_OK) return st;
   }
   return MSA_OK;

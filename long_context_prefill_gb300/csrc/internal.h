@@ -19,30 +19,45 @@ void note_launch();
 uint64_t launch_count();
 
 // ------------------------------------------------------------ attention work units
-// A work unit is a stream of 128-row query tiles ("items"), one per t in
-// [0, T).  Each item has two 64-row halves; half h covers rows
-// 128*t + row_off[h] .. +63 of query head qh[h] (batch folded into the head
-// index).  Both halves read the same KV head.
+// A sub-unit is a stream of 128-row query tiles of one pattern; its tile for
+// item t is q-tile t * stride + offset.  Each tile has two 64-row halves: half
+// h covers rows 128 * tile + row_off[h] .. +63 of query head qh[h] (batch
+// folded into the head index).  A unit pairs two sub-units that read the same
+// KV head: one CTA processes both tiles of an item against one shared K/V
+// stream (the key tiles either needs).
 enum UnitPattern : int32_t { kUnitAshape = 0, kUnitVS = 1, kUnitBlock = 2 };
+
+struct SubUnit {
+  int32_t qh[2];      // b * Hq + query head, per half
+  int32_t row_off[2]; // 0 or 64
+  int32_t slot[2];    // index slot per half (VS / BS)
+  int32_t stride, offset;
+  int32_t sink, window;  // A-shape
+};
+static_assert(sizeof(SubUnit) == 40, "SubUnit layout");
 
 struct Unit {
   int32_t pattern;
   int32_t kvh;        // b * Hkv + kv head
-  int32_t qh[2];      // b * Hq + query head, per half
-  int32_t row_off[2]; // 0 or 64
-  int32_t slot[2];    // index slot per half (VS / BS)
-  int32_t sink, window;
-  int32_t pad[2];
+  int32_t has1;       // sub-unit 1 present
+  int32_t pad;
+  SubUnit sub[2];
 };
-static_assert(sizeof(Unit) == 48, "Unit layout");
+static_assert(sizeof(Unit) == 96, "Unit layout");
 
-constexpr int kMaxUnits = 128;
+constexpr int kMaxUnits = 64;
+// Units sorted by KV head; band b is units [band[b], band[b+1]).  A launch
+// runs the bands one after another (items of a band by descending t), so the
+// CTAs resident at any time read few KV heads and their keys stay in L2.
 struct UnitTable {
   Unit u[kMaxUnits];
+  int32_t band[kMaxUnits + 1];
 };
 
 struct AttnArgs {
-  int32_t n, d, T, n_units;
+  int32_t n, d, T, n_units;  // T: items per unit in this launch
+  int32_t nqt;               // 128-row query tiles over n
+  int32_t n_bands;           // bands in the unit table
   float scale_log2;  // scale * log2(e)
   const void* q;     // bf16 [B*Hq, n, d] (rows loaded into TMEM)
   const void* k;     // bf16 [B*Hkv, n, d] (column gathers)

@@ -11,7 +11,7 @@ namespace msa {
 
 msa_status check_shape(const msa_shape* s);
 msa_status check_heads(const int32_t* heads, int32_t n_heads, int32_t Hq);
-void ashape_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t sink, int32_t window,
+void ashape_units(const msa_shape& s, const int32_t* heads, int32_t nh, const int32_t* sink, const int32_t* window,
                   std::vector<Unit>& out);
 void vs_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t slot_base_per_batch,
               int32_t slots_per_batch, std::vector<Unit>& out);
@@ -206,14 +206,21 @@ static msa_status layer_attend(const msa_shape& s, const void* q, const void* k,
                                const msa_head_cfg* table, void* o, float* lse, int64_t* edges, const LayerPlan& W,
                                cudaStream_t strm) {
   std::vector<Unit> units;
-  for (int32_t h : W.a_heads) ashape_units(s, &h, 1, table[h].sink, table[h].window, units);
+  if (!W.a_heads.empty()) {
+    std::vector<int32_t> sinks, windows;
+    for (int32_t h : W.a_heads) {
+      sinks.push_back(table[h].sink);
+      windows.push_back(table[h].window);
+    }
+    ashape_units(s, W.a_heads.data(), (int32_t)W.a_heads.size(), sinks.data(), windows.data(), units);
+  }
   if (!W.vs_heads.empty()) {
     const int32_t nvs = (int32_t)W.vs_heads.size();
     vs_units(s, W.vs_heads.data(), nvs, 0, nvs, units);
   }
   if (!W.bs_heads.empty())
     block_units(s, W.bs_heads.data(), (int32_t)W.bs_heads.size(), (int32_t)W.bs_heads.size(), units);
-  // heavier patterns first within each query tile: the kernel orders items by tile, then unit
+  // heavier patterns first within each item index: the kernel orders items by tile pair, then unit
   std::vector<Unit> ordered;
   for (const Unit& u : units) if (u.pattern == kUnitVS) ordered.push_back(u);
   for (const Unit& u : units) if (u.pattern == kUnitBlock) ordered.push_back(u);

@@ -57,8 +57,10 @@ def test_ashape_shapes(cuda_lib, n, d, sink, window):
     _ashape_case(cuda_lib, 1, 4, 2, n, d, [0, 3], sink, window, seed=n + d)
 
 
-def test_ashape_batch_gqa(cuda_lib):
-    _ashape_case(cuda_lib, 2, 4, 1, 513, 128, [1, 2], 64, 256, seed=7)
+@pytest.mark.parametrize("heads", [[1, 2], [0, 1, 3]])
+def test_ashape_batch_gqa(cuda_lib, heads):
+    """Heads of one KV group share an item (a pair; a pair plus a single)."""
+    _ashape_case(cuda_lib, 2, 4, 1, 513, 128, heads, 64, 256, seed=7)
 
 
 def _bs_index_host(q, k, b, heads, Hq, Hkv, topk):
@@ -71,10 +73,17 @@ def _bs_index_host(q, k, b, heads, Hq, Hkv, topk):
     return np.stack(J), np.stack(C)
 
 
-@pytest.mark.parametrize("heads,Hkv", [([0, 1], 1), ([2], 2), ([0, 1, 3], 2)])
-def test_block_with_oracle_index(cuda_lib, heads, Hkv):
-    """Block-Sparse attention on the oracle's J (paired heads and single heads)."""
-    B, Hq, n, d, topk = 1, 4, 1000, 128, 4
+@pytest.mark.parametrize("heads,Hq,Hkv", [
+    ([0, 1], 4, 1),              # a pair
+    ([2], 4, 2),                 # a single head
+    ([0, 1, 3], 4, 2),           # a pair and a single in two groups
+    ([0, 1, 2, 3], 4, 1),        # four heads of one group
+    ([0, 1, 2, 3, 4, 6], 8, 1),  # four heads, then a pair
+    ([7, 1, 2, 0, 5], 8, 1),     # four heads, then a single
+])
+def test_block_with_oracle_index(cuda_lib, heads, Hq, Hkv):
+    """Block-Sparse attention on the oracle's J for every way heads are grouped into items."""
+    B, n, d, topk = 1, 1000, 128, 4
     q, k, v = synth.random_qkv(B, Hq, Hkv, n, d, seed=11 + len(heads), device="cuda")
     J, C = _bs_index_host(q, k, 0, heads, Hq, Hkv, topk)
     bidx = torch.from_numpy(J[None]).cuda()
@@ -128,6 +137,16 @@ def test_vs_sparse_slashes_gather_columns(cuda_lib):
     C = [np.sort(rng.choice(n, 300, replace=False)), np.sort(rng.choice(n, 7, replace=False))]
     D = [np.array([3000, 1000, 0]), np.array([2500])]
     _vs_case(cuda_lib, n, 64, C, D, seed=6)
+
+
+def test_vs_single_heads_odd_tiles(cuda_lib):
+    """One head per KV group (each head's even and odd tiles share an item) with
+    an odd number of query tiles, so the last item has one tile."""
+    rng = np.random.default_rng(12)
+    n = 1100
+    C = [np.sort(rng.choice(n, 25, replace=False)), np.sort(rng.choice(n, 60, replace=False))]
+    D = [np.array([900, 400, 130, 64, 1, 0]), np.sort(rng.choice(n, 40, replace=False))[::-1]]
+    _vs_case(cuda_lib, n, 128, C, D, seed=13, Hq=2, Hkv=2)
 
 
 def test_vs_empty_sets(cuda_lib):

@@ -70,3 +70,13 @@ def test_layer_ragged_batch(cuda_lib):
              synth.vslash(64, 20, 50), synth.ashape(0, 64), synth.blocksparse(6), synth.vslash(64, 20, 50)]
     w = dict(q=q, k=k, v=v, table=table, shape=dict(B=2, Hq=8, Hkv=2, n=1111, d=128, scale=128 ** -0.5))
     run_layer(cuda_lib, w, rows_per_head=200)
+
+
+def test_layer_one_group_pairings(cuda_lib):
+    """One KV group: an A-shape pair with different sink/window, four
+    Block-Sparse heads in one item, a Vertical-Slash pair (d = 64)."""
+    q, k, v = synth.random_qkv(1, 8, 1, 1000, 64, seed=78, device="cuda")
+    table = [synth.ashape(16, 100), synth.blocksparse(5), synth.vslash(32, 30, 40), synth.blocksparse(5),
+             synth.ashape(0, 300), synth.blocksparse(5), synth.vslash(32, 30, 40), synth.blocksparse(5)]
+    w = dict(q=q, k=k, v=v, table=table, shape=dict(B=1, Hq=8, Hkv=1, n=1000, d=64, scale=64 ** -0.5))
+    run_layer(cuda_lib, w)
