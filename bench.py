@@ -191,27 +191,30 @@ class LayerRun:
 
 
 # ----------------------------------------------------------------- oracle (CPU) sample
-def oracle_sample(runs, rows_per_head=16, seed=5):
-    """Time the fp64 oracle on a bounded sample of the workload: for every layer,
-    one head of each pattern it uses (its full online index at full length,
-    then rows_per_head sampled query rows).  Returns (TFLOP/s, seconds,
-    sampled FLOPs, description)."""
+def oracle_sample(runs, target_s=12.0, seed=5):
+    """Time the fp64 oracle on a bounded sample of the workload.
+
+    For every layer, the first head of each pattern it uses: its online index
+    at full length (timed once), then seeded sampled query rows, sized from a
+    32-row pilot so that all rows together take about target_s seconds.  The
+    index time is charged to the sample in proportion to the rows sampled
+    (R / n of it), so the value is the same effective metric a full layer
+    would give.  Returns (TFLOP/s, seconds spent, sampled FLOPs, description).
+    """
     import oracle
     import synth
-    flops, secs = 0.0, 0.0
+    heads = []
     for r in runs:
         w, sh = r.w, r.sh
-        q, k, v = w["q"], w["k"], w["v"]
         g = sh["Hq"] // sh["Hkv"]
         seen = set()
         for h, e in enumerate(w["table"]):
             if e["pattern"] in seen:
                 continue
             seen.add(e["pattern"])
-            qn = q[0, h].float().cpu().numpy()
-            kn = k[0, h // g].float().cpu().numpy()
-            vn = v[0, h // g].float().cpu().numpy()
-            rows = synth.sample_rows(sh["n"], rows_per_head, seed + h)
+            qn = w["q"][0, h].float().cpu().numpy()
+            kn = w["k"][0, h // g].float().cpu().numpy()
+            vn = w["v"][0, h // g].float().cpu().numpy()
             t0 = time.perf_counter()
             idx = {}
             if e["pattern"] == "vs":
@@ -224,12 +227,29 @@ def oracle_sample(runs, rows_per_head=16, seed=5):
                 cfg = dict(pattern=oracle.BLOCK, block=64, topk=e["topk"])
             else:
                 cfg = dict(pattern=oracle.ASHAPE, sink=e["sink"], window=e["window"])
-            _, _, size = oracle.head_rows(cfg, qn, kn, vn, rows, sh["scale"], **idx)
+            heads.append(dict(cfg=cfg, q=qn, k=kn, v=vn, idx=idx, n=sh["n"], d=sh["d"], scale=sh["scale"],
+                              t_index=time.perf_counter() - t0, seed=seed + h))
+
+    def rows_pass(count):
+        flops, secs, t_idx, R = 0.0, 0.0, 0.0, 0
+        for x in heads:
+            rows = synth.sample_rows(x["n"], count, x["seed"] + count)
+            t0 = time.perf_counter()
+            _, _, size = oracle.head_rows(x["cfg"], x["q"], x["k"], x["v"], rows, x["scale"], **x["idx"])
             secs += time.perf_counter() - t0
-            flops += 4.0 * float(size.sum()) * sh["d"]
-    desc = (f"per layer ({', '.join(r.name for r in runs)}): one head of each pattern, its full online index "
-            f"at full length plus {rows_per_head}+ seeded sampled query rows (fp64, {oracle.num_threads()} threads)")
-    return flops / secs / 1e12, secs, flops, desc
+            flops += 4.0 * float(size.sum()) * x["d"]
+            t_idx += x["t_index"] * len(rows) / x["n"]
+            R += len(rows)
+        return flops, secs, t_idx, R
+
+    pilot = rows_pass(32)
+    count = int(max(32, min(min(x["n"] for x in heads), 32 * target_s / max(pilot[1], 1e-3))))
+    flops, secs, t_idx, R = rows_pass(count)
+    spent = sum(x["t_index"] for x in heads) + pilot[1] + secs
+    desc = (f"per layer ({', '.join(r.name for r in runs)}): the first head of each pattern, its online index "
+            f"at full length (time charged by rows sampled / n) and {count} seeded sampled query rows "
+            f"({R} rows in all, {secs:.1f} s of rows; fp64, {oracle.num_threads()} threads)")
+    return flops / (secs + t_idx) / 1e12, spent, flops, desc
 
 
 # ----------------------------------------------------------------- main
@@ -400,17 +420,16 @@ def reference_arm(args, world, rank, local, names):
             self.sh = self.w["shape"]
 
     runs = [HostRun(nm) for nm in names]
+    per_step = 4.0  # seconds of sampled rows per step: warm-up and timed steps end within a few minutes
     for _ in range(max(args.warmup, 3)):
-        oracle_sample(runs, rows_per_head=4)
+        oracle_sample(runs, target_s=per_step)
     vals, secs_all = [], 0.0
     desc = ""
-    flops_all = 0.0
     for _ in range(args.steps):
-        v, secs, fl, desc = oracle_sample(runs, rows_per_head=4)
+        v, secs, fl, desc = oracle_sample(runs, target_s=per_step)
         vals.append(v)
         secs_all += secs
-        flops_all += fl
-    value = flops_all / secs_all / 1e12
+    value = statistics.mean(vals)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(1e3 * secs_all / args.steps, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
