@@ -54,6 +54,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kPolyPairs = 0;              // of every 8 key pairs, exponentiated on the FMA pipe
+constexpr uint32_t kIdleNs = 256;          // poll interval of the planner's and loader's waits
+
 
 enum TileKind : int32_t { kTileRange = 0, kTileGather = 1, kTileEnd = 2 };
 
@@ -616,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0;; ++j) {
       if (misc[2]) { ok = false; break; }
       const int slot = j % kDescSlots;
-      if (!mbar_wait(&bars[kBarDEmpty + slot], ((j / kDescSlots) & 1) ^ 1)) { ok = false; break; }
+      if (!mbar_wait_idle(&bars[kBarDEmpty + slot], ((j / kDescSlots) & 1) ^ 1, kIdleNs)) { ok = false; break; }
       TileDesc& d = descs[slot];
       bool more;
       if (U.pattern == kUnitVS) {
@@ -692,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load = [&](int j, bool is_v) -> bool {
       const int idx = 2 * j + (is_v ? 1 : 0);
       const int st = idx % kSlots;
-      if (!mbar_wait(&bars[kBarEmpty + st], ((idx / kSlots) & 1) ^ 1)) return false;
+      if (!mbar_wait_idle(&bars[kBarEmpty + st], ((idx / kSlots) & 1) ^ 1, kIdleNs)) return false;
       const TileDesc& d = descs[j % kDescSlots];
       uint8_t* dst = sR + st * Ly::kTile;
       uint64_t* full = &bars[kBarFull + st];
@@ -723,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0;; ++j) {
       if (misc[2]) { ok = false; break; }
-      if (!desc_full(j)) { ok = false; break; }
+      if (!mbar_wait_idle(&bars[kBarDFull + j % kDescSlots], (j / kDescSlots) & 1, kIdleNs)) { ok = false; break; }
       if (descs[j % kDescSlots].kind == kTileEnd) { desc_release(j); break; }
       if (!load(j, false) || !load(j, true)) { ok = false; break; }
       desc_release(j);
@@ -738,6 +740,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int pv_last[2] = {0, 0};    // that PV is the last reader of its V slot
     int done[2] = {0, 0};       // PVs issued per sub-item (the first one overwrites O)
     int pphase[2] = {0, 0};
+    // Shared-memory descriptors of the operand tiles; a byte offset off within a
+    // tile adds off >> 4 to the start-address field (no carry: addresses < 2^18).
+    const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);    // + X * kTile
+    const uint64_t dk = sdesc_sw128(smem_u32(sR), 16, 1024);    // + slot * kTile
+    const uint64_t dv = sdesc_sw128(smem_u32(sR), 16384, 1024);
+    constexpr uint64_t kTileDesc = Ly::kTile >> 4;
     auto issue_pv = [&](int X) -> bool {
       const int vidx = 2 * pending[X] + 1, vst = vidx % kSlots;
       if (!mbar_wait(&bars[kBarPFull + X], pphase[X] & 1)) return false;
@@ -745,11 +753,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&bars[kBarFull + vst], (vidx / kSlots) & 1)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t v0 = smem_u32(sR + vst * Ly::kTile);
+        const uint64_t v0 = dv + (uint64_t)vst * kTileDesc;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + kColO + 128 * X, tmem + kColS + 128 * X + 8 * kk, sdesc_sw128(v0 + kk * 2048, 16384, 1024),
-                      id_pv, (done[X] > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + kColO + 128 * X, tmem + kColS + 128 * X + 8 * kk, v0 + (uint64_t)(kk * 128), id_pv,
+                      (done[X] > 0 || kk > 0) ? 1u : 0u);
         if (pv_last[X]) mma_commit(&bars[kBarEmpty + vst]);
       }
       __syncwarp();
@@ -772,12 +780,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pending[X] >= 0 && !issue_pv(X)) { ok = false; break; }  // P_X of the previous tile -> O_X
         if (!act[X]) continue;
         if (lane == 0) {
-          const uint32_t q0 = smem_u32(sQ + X * Ly::kTile), k0 = smem_u32(sR + kst * Ly::kTile);
+          const uint64_t q0 = dq + (uint64_t)X * kTileDesc, k0 = dk + (uint64_t)kst * kTileDesc;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16_ss(tmem + kColS + 128 * X, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024),
-                        id_qk, kk > 0 ? 1u : 0u);
+            const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);  // ((kk/4) * 16384 + (kk%4) * 32) >> 4
+            mma_bf16_ss(tmem + kColS + 128 * X, q0 + off, k0 + off, id_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(&bars[kBarSFull + X]);
         }
