@@ -142,6 +142,29 @@ MSA_API msa_status msa_build_block_index(const msa_shape* shape, const void* q, 
                                  int32_t n_heads, int32_t block, int32_t topk, int32_t* block_idx,
                                  int32_t* block_cnt, void* ws, size_t ws_bytes, void* stream);
 
+/* Size of the library's built-in scratch for msa_build_block_index_static
+ * (16 MiB of device memory per device, reserved when the library is loaded). */
+#define MSA_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* msa_build_block_index without a workspace argument: the same index, built
+ * in a scratch array the library holds in device memory, so the call
+ * allocates nothing and needs no workspace query.  This entry point has no
+ * counterpart in the MInference pages; it exists for callers that hold device
+ * tensors from another runtime and have no allocator of their own (or must not
+ * call cudaMalloc on their path).
+ * Limit: msa_block_index_workspace(shape, 64, n_heads) must not exceed
+ * MSA_STATIC_SCRATCH_BYTES, else MSA_ERR_WORKSPACE_TOO_SMALL is returned and
+ * nothing is launched (for d_h = 128 and one KV head per listed head: up
+ * to 42 heads at n = 16384, 15 at n = 32768, 5 at n = 65536).
+ * The scratch is shared by all calls on a device: calls that overlap in time
+ * (unordered streams, several host threads) race on it and must be ordered.
+ * The first call on a device looks up the scratch address (a runtime call),
+ * so make one call on each device before the work that must be free of
+ * set-up calls.  Arguments and outputs as for msa_build_block_index. */
+MSA_API msa_status msa_build_block_index_static(const msa_shape* shape, const void* q, const void* k,
+                                                const int32_t* heads, int32_t n_heads, int32_t block, int32_t topk,
+                                                int32_t* block_idx, int32_t* block_cnt, void* stream);
+
 /* A-shape attention (MInference page eq.(3)): N_A(i) = {0..min(g-1,i)} ∪
  * {max(0,i-w+1)..i}, exact (each key once).  o: [B,Hq,n,d_h] (only the listed
  * heads are written); lse nullable; edges nullable: if given, [B*Hq] int64

@@ -28,7 +28,7 @@ PATTERNS = {"ashape": ASHAPE, "vs": VS, "block": BLOCK}
 EXPORTS = ("msa_status_string", "msa_vs_index_workspace", "msa_block_index_workspace", "msa_layer_workspace",
            "msa_build_vs_index", "msa_build_block_index", "msa_attn_ashape", "msa_attn_vs", "msa_attn_block",
            "msa_prefill_layer", "msa_layer_index", "msa_layer_attend", "msa_kernel_launches", "msa_layer_indices",
-           "msa_vs_expand", "msa_poll_device_status")
+           "msa_vs_expand", "msa_poll_device_status", "msa_build_block_index_static")
 
 
 class MsaError(RuntimeError):
@@ -100,6 +100,8 @@ def load(path: str = LIB_PATH):
             lib.msa_vs_expand.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P]
             lib.msa_poll_device_status.restype = st
             lib.msa_poll_device_status.argtypes = [P]
+            lib.msa_build_block_index_static.restype = st
+            lib.msa_build_block_index_static.argtypes = [P, P, P, P, i32, i32, i32, P, P, P]
             _lib = lib
     return _lib
 
@@ -270,6 +272,24 @@ def build_block_index(q, k, heads, topk, block_idx=None, block_cnt=None, scale=N
                                      _ptr(block_cnt), _ptr(ws), int(ws_bytes), _stream(stream)),
            "msa_build_block_index")
     block_idx._ws = ws
+    return block_idx, block_cnt
+
+
+def build_block_index_static(q, k, heads, topk, block_idx=None, block_cnt=None, scale=None, stream=None):
+    """msa_build_block_index_static: the Block-Sparse index built in the
+    library's own scratch (no workspace); outputs as build_block_index."""
+    lib = load()
+    sh = make_shape(q, k, scale)
+    hp, nh = _heads(heads)
+    B, n = q.shape[0], q.shape[2]
+    nb = (n + 63) // 64
+    if block_idx is None:
+        block_idx = torch.empty(B, nh, nb, int(topk), dtype=torch.int32, device=q.device)
+    if block_cnt is None:
+        block_cnt = torch.empty(B, nh, nb, dtype=torch.int32, device=q.device)
+    _check(lib.msa_build_block_index_static(ctypes.byref(sh), _ptr(q), _ptr(k), hp, nh, 64, int(topk),
+                                            _ptr(block_idx), _ptr(block_cnt), _stream(stream)),
+           "msa_build_block_index_static")
     return block_idx, block_cnt
 
 
