@@ -212,6 +212,13 @@ MSA_API msa_status msa_layer_attend(const msa_shape* shape, const void* q, const
                                     const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
                                     size_t ws_bytes, void* stream);
 
+/* Failure-detection check (no counterpart in the pages): launches one thread
+ * that waits on a barrier nothing arrives at, with the same bounded wait the
+ * pipelines use but a limit of limit_ms (1..2000) milliseconds, so that the
+ * next msa_poll_device_status returns MSA_ERR_DEVICE_TIMEOUT.  The context
+ * stays usable.  Nothing faults, traps or hangs. */
+MSA_API msa_status msa_check_wait_timeout(int32_t limit_ms, void* stream);
+
 /* Number of kernels this process has launched through the library so far
  * (all devices).  Lets a caller count the launches inside a region. */
 MSA_API uint64_t msa_kernel_launches(void);

@@ -28,7 +28,8 @@ PATTERNS = {"ashape": ASHAPE, "vs": VS, "block": BLOCK}
 EXPORTS = ("msa_status_string", "msa_vs_index_workspace", "msa_block_index_workspace", "msa_layer_workspace",
            "msa_build_vs_index", "msa_build_block_index", "msa_attn_ashape", "msa_attn_vs", "msa_attn_block",
            "msa_prefill_layer", "msa_layer_index", "msa_layer_attend", "msa_kernel_launches", "msa_layer_indices",
-           "msa_vs_expand", "msa_poll_device_status", "msa_build_block_index_static")
+           "msa_vs_expand", "msa_poll_device_status", "msa_build_block_index_static",
+           "msa_check_wait_timeout")
 
 
 class MsaError(RuntimeError):
@@ -100,6 +101,8 @@ def load(path: str = LIB_PATH):
             lib.msa_vs_expand.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P]
             lib.msa_poll_device_status.restype = st
             lib.msa_poll_device_status.argtypes = [P]
+            lib.msa_check_wait_timeout.restype = st
+            lib.msa_check_wait_timeout.argtypes = [i32, P]
             lib.msa_build_block_index_static.restype = st
             lib.msa_build_block_index_static.argtypes = [P, P, P, P, i32, i32, i32, P, P, P]
             _lib = lib
@@ -368,6 +371,11 @@ class Layer:
 def kernel_launches() -> int:
     """Kernels launched through the library by this process so far."""
     return int(load().msa_kernel_launches())
+
+
+def check_wait_timeout(limit_ms: int, stream=None):
+    """Launch the failure-detection check (a bounded wait that runs out)."""
+    _check(load().msa_check_wait_timeout(int(limit_ms), _stream(stream)), "msa_check_wait_timeout")
 
 
 def poll_device_status(stream=None) -> int:

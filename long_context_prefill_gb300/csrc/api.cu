@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace msa {
 
@@ -213,6 +214,18 @@ void block_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t s
     }
 }
 
+// Failure-detection check: one thread waits on an mbarrier that nothing
+// arrives at, with a short limit, and records the timeout in the error word
+// exactly as the pipelines' bounded waits do.
+__global__ void wait_timeout_check_kernel(uint64_t limit_ns, int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, limit_ns)) atomicCAS(err, 0, kErrTimeout);
+  }
+}
+
 msa_status attention(const msa_shape& s, const void* q, const void* k, const void* v, void* o, float* lse,
                      int64_t* edges, const std::vector<Unit>& units, const AttnArgs& idx, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
@@ -320,6 +333,15 @@ msa_status msa_attn_block(const msa_shape* shape, const void* q, const void* k, 
   a.bs_topk = topk;
   a.bs_nb = ceil_div(shape->n, 64);
   return attention(*shape, q, k, v, o, lse, edges, units, a, (cudaStream_t)stream);
+}
+
+msa_status msa_check_wait_timeout(int32_t limit_ms, void* stream) {
+  if (limit_ms < 1 || limit_ms > 2000) return MSA_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (!err) return MSA_ERR_CUDA;
+  wait_timeout_check_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((uint64_t)limit_ms * 1000000ull, err);
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 msa_status msa_poll_device_status(void* stream) {

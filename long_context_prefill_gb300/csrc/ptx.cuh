@@ -54,13 +54,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait until the phase with the given parity has completed. Returns false if
-// the wait ran past MSA_WAIT_LIMIT_NS.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// the wait ran past limit_ns (MSA_WAIT_LIMIT_NS unless given).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = MSA_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u && global_timer_ns() - t0 > MSA_WAIT_LIMIT_NS) return false;
+    if ((it & 63u) == 0u && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
