@@ -17,9 +17,10 @@
 //   warp 10    loader: TMA-loads both Q tiles once, then K(j) and V(j) of
 //              every tile into a four-slot ring (K in slots 0/2, V in 1/3), or
 //              gathers single key rows with cp.async;
-//   warp 9     MMA issuer (one thread): per tile and sub-item, O_X += P_X V of
-//              the previous tile, then S_X = Q_X K^T.  While one sub-item's
-//              softmax runs, the tensor core works for the other;
+//   warps 9/11 MMA issuers (one thread each, one per sub-item X): per tile,
+//              O_X += P_X V of the previous tile, then S_X = Q_X K^T.  While
+//              one sub-item's softmax runs, the tensor core works for the
+//              other, and neither issuer waits for the other's P;
 //   warps 0-7  softmax: warps 4X..4X+3 own sub-item X; thread r is query row r
 //              (TMEM lane r) with all 128 keys of a tile.  Masks (causal,
 //              pattern, sequence end) are applied before the max; O_X is
@@ -41,12 +42,13 @@ namespace {
 
 constexpr int kSoftWarps = 8;
 constexpr int kPlannerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp0 = 9;    // MMA issuer of sub-item 0
 constexpr int kLoaderWarp = 10;
-constexpr int kThreads = 32 * (kSoftWarps + 3);
+constexpr int kMmaWarp1 = 11;   // MMA issuer of sub-item 1
+constexpr int kThreads = 32 * (kSoftWarps + 4);
 constexpr int kSlots = 4;  // K(j) in slot 2j mod 4, V(j) in slot 2j+1 mod 4
 constexpr int kDescSlots = 8;
-constexpr int kDescReaders = kSoftWarps + 2;  // softmax warps, MMA warp, loader warp
+constexpr int kDescReaders = kSoftWarps + 3;  // softmax warps, two MMA warps, loader warp
 constexpr int kMaxStagedBlocks = 512;         // Block-Sparse list entries staged per half
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S of sub-item X at 128 X (P over its first 64 columns), O of
@@ -75,8 +77,8 @@ enum {
   kBarEmpty = kBarFull + kSlots,
   kBarSFull = kBarEmpty + kSlots,  // per sub-item: S of its latest tile is in TMEM
   kBarPFull = kBarSFull + 2,       // per sub-item: P of its latest tile is in TMEM
-  kBarODone = kBarPFull + 2,       // every MMA of the item has completed
-  kBarDFull = kBarODone + 1,
+  kBarODone = kBarPFull + 2,       // per sub-item: every MMA of its issuer has completed
+  kBarDFull = kBarODone + 2,
   kBarDEmpty = kBarDFull + kDescSlots,
   kNumBars = kBarDEmpty + kDescSlots
 };
@@ -575,17 +577,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(const_cast<uint32_t*>(&misc[0]), kTmemCols);
     tmem_relinquish();
   }
-  if (threadIdx.x == 32 * kMmaWarp) {
+  if (threadIdx.x == 32 * kMmaWarp0) {
     mbar_init(&bars[kBarQ], 1);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bars[kBarFull + s], 1);
-      mbar_init(&bars[kBarEmpty + s], 1);
+      mbar_init(&bars[kBarEmpty + s], 2);  // one release per MMA issuer
     }
     for (int X = 0; X < 2; ++X) {
       mbar_init(&bars[kBarSFull + X], 1);
       mbar_init(&bars[kBarPFull + X], 4);
+      mbar_init(&bars[kBarODone + X], 1);
     }
-    mbar_init(&bars[kBarODone], 1);
     for (int s = 0; s < kDescSlots; ++s) {
       mbar_init(&bars[kBarDFull + s], 1);
       mbar_init(&bars[kBarDEmpty + s], kDescReaders);
@@ -731,38 +733,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       desc_release(j);
     }
     if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kMmaWarp0 || warp == kMmaWarp1) {
+    // ------------------------------------------------------------ MMA issuer of sub-item X
+    // Each sub-item has its own issuing thread, so one sub-item waiting for its
+    // P never holds back the other's MMAs.  Both read the shared K/V ring and
+    // each releases every slot once (the empty barriers count two arrivals).
+    const int X = warp == kMmaWarp0 ? 0 : 1;
     bool ok = mbar_wait(&bars[kBarQ], 0);
     constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
-    int pending[2] = {-1, -1};  // tile whose PV is owed, per sub-item (always the previous tile)
-    int pv_last[2] = {0, 0};    // that PV is the last reader of its V slot
-    int done[2] = {0, 0};       // PVs issued per sub-item (the first one overwrites O)
-    int pphase[2] = {0, 0};
+    int pending = -1;  // tile whose PV is owed (always the previous tile of this sub-item)
+    int done = 0;      // PVs issued (the first one overwrites O)
+    int pphase = 0;
     // Shared-memory descriptors of the operand tiles; a byte offset off within a
     // tile adds off >> 4 to the start-address field (no carry: addresses < 2^18).
-    const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);    // + X * kTile
-    const uint64_t dk = sdesc_sw128(smem_u32(sR), 16, 1024);    // + slot * kTile
-    const uint64_t dv = sdesc_sw128(smem_u32(sR), 16384, 1024);
     constexpr uint64_t kTileDesc = Ly::kTile >> 4;
-    auto issue_pv = [&](int X) -> bool {
-      const int vidx = 2 * pending[X] + 1, vst = vidx % kSlots;
-      if (!mbar_wait(&bars[kBarPFull + X], pphase[X] & 1)) return false;
-      ++pphase[X];
+    const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024) + (uint64_t)X * kTileDesc;
+    const uint64_t dk = sdesc_sw128(smem_u32(sR), 16, 1024);  // + slot * kTile
+    const uint64_t dv = sdesc_sw128(smem_u32(sR), 16384, 1024);
+    const uint32_t tS = tmem + kColS + 128 * X, tO = tmem + kColO + 128 * X;
+    auto issue_pv = [&]() -> bool {  // O_X += P_X V of tile `pending`, then release that V slot
+      const int vidx = 2 * pending + 1, vst = vidx % kSlots;
+      if (!mbar_wait(&bars[kBarPFull + X], pphase & 1)) return false;
+      ++pphase;
       if (!mbar_wait(&bars[kBarFull + vst], (vidx / kSlots) & 1)) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint64_t v0 = dv + (uint64_t)vst * kTileDesc;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + kColO + 128 * X, tmem + kColS + 128 * X + 8 * kk, v0 + (uint64_t)(kk * 128), id_pv,
-                      (done[X] > 0 || kk > 0) ? 1u : 0u);
-        if (pv_last[X]) mma_commit(&bars[kBarEmpty + vst]);
+          mma_bf16_ts(tO, tS + 8 * kk, v0 + (uint64_t)(kk * 128), id_pv, (done > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars[kBarEmpty + vst]);
       }
       __syncwarp();
-      ++done[X];
-      pending[X] = -1;
+      ++done;
+      pending = -1;
       return true;
     };
     if (ok) tc_fence_after();
@@ -770,43 +775,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (misc[2] || !desc_full(j)) { ok = false; break; }
       const TileDesc& d = descs[j % kDescSlots];
       const bool end = d.kind == kTileEnd;
-      const int act[2] = {d.active[0], d.active[1]};
+      const bool act = d.active[X] != 0;
       desc_release(j);
       if (end) break;
       const int kidx = 2 * j, kst = kidx % kSlots;
       if (!mbar_wait(&bars[kBarFull + kst], (kidx / kSlots) & 1)) { ok = false; break; }
       tc_fence_after();
-      for (int X = 0; X < 2; ++X) {
-        if (pending[X] >= 0 && !issue_pv(X)) { ok = false; break; }  // P_X of the previous tile -> O_X
-        if (!act[X]) continue;
+      if (pending >= 0 && !issue_pv()) { ok = false; break; }  // P_X of the previous tile -> O_X
+      if (act) {
         if (lane == 0) {
-          const uint64_t q0 = dq + (uint64_t)X * kTileDesc, k0 = dk + (uint64_t)kst * kTileDesc;
+          const uint64_t k0 = dk + (uint64_t)kst * kTileDesc;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);  // ((kk/4) * 16384 + (kk%4) * 32) >> 4
-            mma_bf16_ss(tmem + kColS + 128 * X, q0 + off, k0 + off, id_qk, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tS, dq + off, k0 + off, id_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(&bars[kBarSFull + X]);
         }
         __syncwarp();
-        pending[X] = j;
-        pv_last[X] = (X == 1) || !act[1];
-      }
-      if (!ok) break;
-      if (!act[0] && !act[1]) {  // V(j) has no reader: release its slot once it has landed
+        pending = j;
+      } else {  // this sub-item never reads V(j): release it once it has landed
         const int vidx = 2 * j + 1;
         if (!mbar_wait(&bars[kBarFull + vidx % kSlots], (vidx / kSlots) & 1)) { ok = false; break; }
         if (lane == 0) mma_commit(&bars[kBarEmpty + vidx % kSlots]);
       }
-      if (lane == 0) mma_commit(&bars[kBarEmpty + kst]);  // K(j) consumed
+      if (lane == 0) mma_commit(&bars[kBarEmpty + kst]);  // K(j) consumed by this issuer
       __syncwarp();
     }
-    for (int X = 0; X < 2 && ok; ++X)
-      if (pending[X] >= 0 && !issue_pv(X)) ok = false;
-    if (lane == 0) mma_commit(&bars[kBarODone]);  // arrives once every MMA issued above has completed
+    if (ok && pending >= 0 && !issue_pv()) ok = false;
+    if (lane == 0) mma_commit(&bars[kBarODone + X]);  // arrives once every MMA issued above has completed
     __syncwarp();
     if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
-  } else {
+  } else if (warp < kSoftWarps) {
     // ------------------------------------------------------------ softmax (sub-item X)
     const int quarter = warp & 3;  // TMEM lanes 32*quarter ..
     const int X = warp >> 2;
@@ -956,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) { misc[2] = 1; set_error(A.err, kErrTimeout); }
 
     // ---- epilogue: O / l, LSE
-    if (!mbar_wait(&bars[kBarODone], 0)) { ok = false; misc[2] = 1; set_error(A.err, kErrTimeout); }
+    if (!mbar_wait(&bars[kBarODone + X], 0)) { ok = false; misc[2] = 1; set_error(A.err, kErrTimeout); }
     tc_fence_after();
     const int qh = U.sub[X].qh[hh & 1];
     const bool empty = !(m_used > -INFINITY);  // no attended key in any tile: o = 0
