@@ -57,6 +57,16 @@ constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kPolyPairs = 0;              // of every 8 key pairs, exponentiated on the FMA pipe
 constexpr uint32_t kIdleNs = 256;          // poll interval of the planner's and loader's waits
+#ifndef TURN_LOCK
+#define TURN_LOCK 1
+#endif
+constexpr bool kTurnLock = TURN_LOCK;
+#ifndef MMA_P_WAIT
+#define MMA_P_WAIT(bar, parity) mbar_wait(bar, parity)
+#endif
+#ifndef SM_S_WAIT
+#define SM_S_WAIT(bar, parity) mbar_wait(bar, parity)
+#endif
 
 
 enum TileKind : int32_t { kTileRange = 0, kTileGather = 1, kTileEnd = 2 };
@@ -93,7 +103,7 @@ struct Layout {
   static constexpr int kBlk = kStage + 256 * 4;                             // Block-Sparse lists
   static constexpr int kBars = kBlk + 4 * kMaxStagedBlocks * 4;
   static constexpr int kMisc = kBars + kNumBars * 8;
-  static constexpr int kTotal = kMisc + 64;
+  static constexpr int kTotal = kMisc + 64;  // misc words: [0] TMEM base, [2] abort, [8..11] exponential turns
   // > 113 KB keeps one CTA per SM, so the 512-column TMEM allocation never waits.
   static constexpr int kAlloc = (kTotal + 1024) > 120 * 1024 ? (kTotal + 1024) : 120 * 1024;
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -593,6 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[kBarDEmpty + s], kDescReaders);
     }
     misc[2] = 0;
+    for (int q = 0; q < 4; ++q) misc[8 + q] = 0;  // exponential turns (one per SMSP)
     fence_mbar_init();
   }
   tc_fence_before();
@@ -754,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + kColS + 128 * X, tO = tmem + kColO + 128 * X;
     auto issue_pv = [&]() -> bool {  // O_X += P_X V of tile `pending`, then release that V slot
       const int vidx = 2 * pending + 1, vst = vidx % kSlots;
-      if (!mbar_wait(&bars[kBarPFull + X], pphase & 1)) return false;
+      if (!MMA_P_WAIT(&bars[kBarPFull + X], pphase & 1)) return false;
       ++pphase;
       if (!mbar_wait(&bars[kBarFull + vst], (vidx / kSlots) & 1)) return false;
       tc_fence_after();
@@ -868,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kCount) count += __popcll(vw[0]) + __popcll(vw[1]);
 
       // ---- S of this tile (its completion also means this sub-item's previous PV is done)
-      if (!mbar_wait(&bars[kBarSFull + X], mine & 1)) { ok = false; break; }
+      if (!SM_S_WAIT(&bars[kBarSFull + X], mine & 1)) { ok = false; break; }
       tc_fence_after();
       float sv[128];
       {
@@ -904,6 +915,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+      // The exponentials of the two sub-items' warps on this SMSP take turns
+      // on its MUFU unit (warp q and warp q + 4 share SMSP q): a held turn
+      // lets this sub-item's P reach the tensor core in half the time.
+      if (kTurnLock) {
+        if (lane == 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (atomicCAS(const_cast<uint32_t*>(&misc[8 + quarter]), 0u, 1u) != 0u)
+            if (global_timer_ns() - t0 > MSA_WAIT_LIMIT_NS) { misc[2] = 1; set_error(A.err, kErrTimeout); break; }
+        }
+        __syncwarp();
+      }
       const uint64_t c2x2 = pk2(c2, c2), negm = pk2(-mref, -mref);
       uint64_t acc[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};
       // ---- P over the first 64 columns of S, 32 columns at a time
@@ -934,6 +956,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         up2(acc[0], a0, a1);
         up2(acc[1], a2, a3);
         l = l * alpha + ((a0 + a1) + (a2 + a3));
+      }
+      if (kTurnLock) {
+        __syncwarp();
+        if (lane == 0) atomicExch(const_cast<uint32_t*>(&misc[8 + quarter]), 0u);
       }
       // ---- rescale O_X (its previous PV completed before S was ready; the next waits for P)
       if (any && mine > 0) {
