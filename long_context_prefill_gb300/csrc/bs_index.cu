@@ -119,6 +119,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 constexpr int kTopkWarps = 4;
+constexpr int kRegKeys = 64;  // rows of up to 2048 candidates are selected in registers
 
 // One warp per (slot, query block u): J_u = {u} ∪ top_{k-1} of row u.
 __global__ void __launch_bounds__(32 * kTopkWarps) block_topk_kernel(const float* scores, int nb, int topk,
@@ -132,6 +133,49 @@ __global__ void __launch_bounds__(32 * kTopkWarps) block_topk_kernel(const float
   int32_t* out = J + job * topk;
   int* h = hist[warp];
   const int k1 = min(topk - 1, u);  // picks among v < u
+  if (u <= 32 * kRegKeys && k1 < u && k1 > 0) {
+    // Row held in registers (key of v = lane + 32 i in key[i]; 0 below every
+    // real key for v >= u): the k1-th largest key T by a bitwise search on
+    // counts, then every key above T and the first (in index order) equal to it.
+    uint32_t key[kRegKeys];
+#pragma unroll
+    for (int i = 0; i < kRegKeys; ++i) {
+      const int v = lane + 32 * i;
+      key[i] = v < u ? order_key(row[v]) : 0u;
+    }
+    uint32_t T = 0;
+    for (int b = 31; b >= 0; --b) {
+      const uint32_t cand = T | (1u << b);
+      int c = 0;
+#pragma unroll
+      for (int i = 0; i < kRegKeys; ++i) c += key[i] >= cand ? 1 : 0;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+      if (c >= k1) T = cand;
+    }
+    int above = 0;
+#pragma unroll
+    for (int i = 0; i < kRegKeys; ++i) above += key[i] > T ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) above += __shfl_xor_sync(0xFFFFFFFFu, above, o);
+    const int need_eq = k1 - above;
+    int pos = 0, eq_seen = 0;
+#pragma unroll
+    for (int i = 0; i < kRegKeys; ++i) {
+      if (32 * i >= u) break;
+      const bool gt = key[i] > T, eq = key[i] == T;
+      const unsigned eqm = __ballot_sync(0xFFFFFFFFu, eq);
+      const int eq_rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
+      const bool sel = gt || (eq && eq_rank < need_eq);
+      const unsigned selm = __ballot_sync(0xFFFFFFFFu, sel);
+      if (sel) out[pos + __popc(selm & ((1u << lane) - 1u))] = lane + 32 * i;
+      pos += __popc(selm);
+      eq_seen += __popc(eqm);
+    }
+    for (int x = k1 + lane; x < topk; x += 32) out[x] = (x == k1) ? u : -1;  // diagonal last (largest id)
+    if (lane == 0) cnt[job] = k1 + 1;
+    return;
+  }
   uint32_t prefix = 0, pmask = 0;
   int need = k1;
   const bool all = (k1 >= u);
