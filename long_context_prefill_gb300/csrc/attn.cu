@@ -57,16 +57,7 @@ constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kPolyPairs = 0;              // of every 8 key pairs, exponentiated on the FMA pipe
 constexpr uint32_t kIdleNs = 256;          // poll interval of the planner's and loader's waits
-#ifndef TURN_LOCK
-#define TURN_LOCK 1
-#endif
-constexpr bool kTurnLock = TURN_LOCK;
-#ifndef MMA_P_WAIT
-#define MMA_P_WAIT(bar, parity) mbar_wait(bar, parity)
-#endif
-#ifndef SM_S_WAIT
-#define SM_S_WAIT(bar, parity) mbar_wait(bar, parity)
-#endif
+constexpr bool kTurnLock = true;            // sub-items take turns on each SMSP's MUFU
 
 
 enum TileKind : int32_t { kTileRange = 0, kTileGather = 1, kTileEnd = 2 };
@@ -765,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + kColS + 128 * X, tO = tmem + kColO + 128 * X;
     auto issue_pv = [&]() -> bool {  // O_X += P_X V of tile `pending`, then release that V slot
       const int vidx = 2 * pending + 1, vst = vidx % kSlots;
-      if (!MMA_P_WAIT(&bars[kBarPFull + X], pphase & 1)) return false;
+      if (!mbar_wait(&bars[kBarPFull + X], pphase & 1)) return false;
       ++pphase;
       if (!mbar_wait(&bars[kBarFull + vst], (vidx / kSlots) & 1)) return false;
       tc_fence_after();
@@ -879,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kCount) count += __popcll(vw[0]) + __popcll(vw[1]);
 
       // ---- S of this tile (its completion also means this sub-item's previous PV is done)
-      if (!SM_S_WAIT(&bars[kBarSFull + X], mine & 1)) { ok = false; break; }
+      if (!mbar_wait(&bars[kBarSFull + X], mine & 1)) { ok = false; break; }
       tc_fence_after();
       float sv[128];
       {
