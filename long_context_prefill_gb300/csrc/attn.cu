@@ -55,7 +55,6 @@ constexpr uint32_t kTmemCols = 512;
 // sub-item X at 256 + 128 X
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kPolyPairs = 0;              // of every 8 key pairs, exponentiated on the FMA pipe
 constexpr uint32_t kIdleNs = 256;          // poll interval of the planner's and loader's waits
 constexpr bool kTurnLock = true;            // sub-items take turns on each SMSP's MUFU
 
@@ -135,37 +134,6 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
-// 2^x for a pair on the FMA pipe (the MUFU unit is the softmax's bottleneck):
-// x = n + f with n = round(x) and f in [-1/2, 1/2]; 2^f by a cubic fitted
-// for minimax relative error on that interval (7.5e-5, far below bf16's
-// 2^-9), and 2^n added to the exponent field.  Inputs are clamped at -125 so
-// the result stays a normal float (masked entries come out as ~2^-125, not 0;
-// a row with no attended key is recognised by its max staying -inf).
-__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer held in the low mantissa bits
-  float x0, x1;
-  up2(x, x0, x1);
-  const uint64_t xc = pk2(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f));
-  const uint64_t t = add2(xc, pk2(kRound, kRound));
-  const uint64_t f = sub2(xc, sub2(t, pk2(kRound, kRound)));
-  uint64_t p = fma2(f, pk2(0.0551716685295105f, 0.0551716685295105f), pk2(0.2426111251115799f, 0.2426111251115799f));
-  p = fma2(p, f, pk2(0.6932609677314758f, 0.6932609677314758f));
-  p = fma2(p, f, pk2(0.9999280571937561f, 0.9999280571937561f));
-  float t0, t1, p0, p1;
-  up2(t, t0, t1);
-  up2(p, p0, p1);
-  // t's bits are 0x4B400000 + n, so (t << 23) mod 2^32 is n << 23
-  const uint32_t r0 = __float_as_uint(t0) * (1u << 23) + __float_as_uint(p0);
-  const uint32_t r1 = __float_as_uint(t1) * (1u << 23) + __float_as_uint(p1);
-  return pk2(__uint_as_float(r0), __uint_as_float(r1));
-}
-
 __device__ __forceinline__ uint64_t low_mask64(int c) {  // bits [0, c), c clamped to [0, 64]
   c = c < 0 ? 0 : (c > 64 ? 64 : c);
   return c >= 64 ? ~0ull : ((1ull << c) - 1ull);
@@ -927,14 +895,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 32; ++k) {
           const int e = 64 * half + 2 * k;
           const uint64_t x = fma2(pk2(sv[e], sv[e + 1]), c2x2, negm);
-          uint64_t p;
-          if ((k & 7) >= 8 - kPolyPairs) {
-            p = exp2_poly2(x);
-          } else {
-            float x0, x1;
-            up2(x, x0, x1);
-            p = pk2(ex2(x0), ex2(x1));
-          }
+          float x0, x1;
+          up2(x, x0, x1);
+          const uint64_t p = pk2(ex2(x0), ex2(x1));
           acc[k & 1] = add2(acc[k & 1], p);
           float p0, p1;
           up2(p, p0, p1);

@@ -220,7 +220,8 @@ static msa_status layer_attend(const msa_shape& s, const void* q, const void* k,
   }
   if (!W.bs_heads.empty())
     block_units(s, W.bs_heads.data(), (int32_t)W.bs_heads.size(), (int32_t)W.bs_heads.size(), units);
-  // heavier patterns first within each item index: the kernel orders items by tile pair, then unit
+  // heavier patterns first within each KV-head band: the kernel runs a band's items by descending
+  // tile pair, then by unit (launch_attention keeps this order when it groups units by KV head)
   std::vector<Unit> ordered;
   for (const Unit& u : units) if (u.pattern == kUnitVS) ordered.push_back(u);
   for (const Unit& u : units) if (u.pattern == kUnitBlock) ordered.push_back(u);
