@@ -353,6 +353,7 @@ def main():
             "index_bytes": r.index_bytes,
             "density": round(float(r.edges.sum()) / (r.sh["Hq"] * r.sh["n"] * (r.sh["n"] + 1) / 2), 4),
         }
+    dense_and_cold(runs, msa, per_layer, stream)
     pk, pk_src = peaks()
     achieved = attn_flops_sum / (attn_ms_sum * 1e-3) / 1e12
     peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -392,6 +393,43 @@ def main():
                                 "sample": desc, "seconds": round(secs, 2)}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def dense_and_cold(runs, msa, per_layer, stream, reps=2):
+    """Outside the timed region: (1) dense causal attention of every head on
+    the same engine and inputs, the baseline the sparse layer is measured
+    against (speedup_vs_dense = dense attention time / sparse layer time);
+    (2) the sparse layer once right after a 512 MiB write has flushed L2."""
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=runs[0].o.device)
+    for r in runs:
+        sh = r.sh
+        heads = list(range(sh["Hq"]))
+        q, k, v = r.w["q"], r.w["k"], r.w["v"]
+        msa.attn_dense(q, k, v, heads, o=r.o, stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            msa.attn_dense(q, k, v, heads, o=r.o, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        dense_ms = a.elapsed_time(b) / reps
+        dense_flops = 4.0 * sh["d"] * sh["B"] * sh["Hq"] * sh["n"] * (sh["n"] + 1) / 2
+        cold = []
+        for _ in range(reps):
+            scrub.fill_(1)
+            a.record(stream)
+            r.index()
+            r.attend()
+            b.record(stream)
+            torch.cuda.synchronize()
+            cold.append(a.elapsed_time(b))
+        lay = per_layer[r.name]
+        lay["dense_ms"] = round(dense_ms, 4)
+        lay["dense_tflops"] = round(dense_flops / (dense_ms * 1e-3) / 1e12, 2)
+        lay["speedup_vs_dense"] = round(dense_ms / lay["ms_per_layer"], 3)
+        lay["ms_per_layer_cold_l2"] = round(statistics.median(cold), 4)
+    assert msa.poll_device_status() == 0
+    del scrub
 
 
 def end_to_end(runs, msa, K, world, device, stream):

@@ -173,6 +173,14 @@ MSA_API msa_status msa_attn_ashape(const msa_shape* shape, const void* q, const 
                            const int32_t* heads, int32_t n_heads, int32_t sink, int32_t window, void* o,
                            float* lse, int64_t* edges, void* stream);
 
+/* Dense causal attention (MInference page eq.(1)-(2): N(i) = {0..i}) on the
+ * same engine: the baseline the sparse patterns are measured against, and the
+ * set every pattern reduces to when its budgets cover all keys.  Arguments as
+ * for msa_attn_ashape. */
+MSA_API msa_status msa_attn_dense(const msa_shape* shape, const void* q, const void* k, const void* v,
+                                  const int32_t* heads, int32_t n_heads, void* o, float* lse, int64_t* edges,
+                                  void* stream);
+
 /* Vertical-Slash attention over the physical set of row i in query block
  * u = [a, e] (MInference page §2.1 "1x64 verticals, 64x64 slash tiles" and
  * §4.1 "verticals as points, slashes as intervals"):

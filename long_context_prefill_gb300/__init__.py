@@ -29,7 +29,7 @@ EXPORTS = ("msa_status_string", "msa_vs_index_workspace", "msa_block_index_works
            "msa_build_vs_index", "msa_build_block_index", "msa_attn_ashape", "msa_attn_vs", "msa_attn_block",
            "msa_prefill_layer", "msa_layer_index", "msa_layer_attend", "msa_kernel_launches", "msa_layer_indices",
            "msa_vs_expand", "msa_poll_device_status", "msa_build_block_index_static",
-           "msa_check_wait_timeout")
+           "msa_check_wait_timeout", "msa_attn_dense")
 
 
 class MsaError(RuntimeError):
@@ -101,6 +101,8 @@ def load(path: str = LIB_PATH):
             lib.msa_vs_expand.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P]
             lib.msa_poll_device_status.restype = st
             lib.msa_poll_device_status.argtypes = [P]
+            lib.msa_attn_dense.restype = st
+            lib.msa_attn_dense.argtypes = [P, P, P, P, P, i32, P, P, P, P]
             lib.msa_check_wait_timeout.restype = st
             lib.msa_check_wait_timeout.argtypes = [i32, P]
             lib.msa_build_block_index_static.restype = st
@@ -167,6 +169,17 @@ def attn_ashape(q, k, v, heads, sink, window, o=None, lse=None, edges=None, scal
     hp, nh = _heads(heads)
     _check(lib.msa_attn_ashape(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), hp, nh, int(sink), int(window), _ptr(o),
                                _ptr(lse), _ptr(edges), _stream(stream)), "msa_attn_ashape")
+    return o
+
+
+def attn_dense(q, k, v, heads, o=None, lse=None, edges=None, scale=None, stream=None):
+    """Dense causal attention of the listed heads on the same engine; returns o."""
+    lib = load()
+    o = _out_like(q, o)
+    sh = make_shape(q, k, scale)
+    hp, nh = _heads(heads)
+    _check(lib.msa_attn_dense(ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), hp, nh, _ptr(o), _ptr(lse), _ptr(edges),
+                              _stream(stream)), "msa_attn_dense")
     return o
 
 

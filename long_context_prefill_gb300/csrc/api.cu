@@ -286,6 +286,13 @@ msa_status msa_attn_ashape(const msa_shape* shape, const void* q, const void* k,
   return attention(*shape, q, k, v, o, lse, edges, units, a, (cudaStream_t)stream);
 }
 
+msa_status msa_attn_dense(const msa_shape* shape, const void* q, const void* k, const void* v, const int32_t* heads,
+                          int32_t n_heads, void* o, float* lse, int64_t* edges, void* stream) {
+  MSA_TRY(check_qkv(shape, q, k, v));
+  // dense causal = A-shape with a window over every key: each row attends j <= i
+  return msa_attn_ashape(shape, q, k, v, heads, n_heads, 0, shape->n, o, lse, edges, stream);
+}
+
 msa_status msa_attn_vs(const msa_shape* shape, const void* q, const void* k, const void* v, const int32_t* heads,
                        int32_t n_heads, int32_t block, const msa_vs_index* index, void* o, float* lse,
                        int64_t* edges, void* stream) {

@@ -157,3 +157,24 @@ def test_vs_empty_sets(cuda_lib):
 def test_vs_dense_when_all_offsets(cuda_lib):
     n = 700
     _vs_case(cuda_lib, n, 128, [np.array([], np.int64)] * 2, [np.arange(n)[::-1]] * 2, seed=10)
+
+
+@pytest.mark.parametrize("n,d", [(1000, 128), (333, 64)])
+def test_dense_causal_matches_sdpa(cuda_lib, n, d):
+    """msa_attn_dense against the oracle's dense pattern and against torch's
+    fp64 causal SDPA (eq.(1)-(2) with N(i) = {0..i}); E = n(n+1)/2 per head."""
+    q, k, v = synth.random_qkv(1, 4, 2, n, d, seed=n, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 4, n, device="cuda")
+    edges = torch.zeros(4, dtype=torch.int64, device="cuda")
+    cuda_lib.attn_dense(q, k, v, [0, 1, 2, 3], o=o, lse=lse, edges=edges)
+    assert cuda_lib.poll_device_status() == 0
+    for h in range(4):
+        qn, kn, vn = head_qkv(q, k, v, 0, h, 4, 2)
+        ro, rl, _ = oracle.head_rows(dict(pattern=oracle.DENSE), qn, kn, vn, np.arange(n), scale_of(d))
+        compare_rows(f32(o[0, h]), f32(lse[0, h]), ro, rl, f"dense h{h}")
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(qn).double()[None], torch.from_numpy(kn).double()[None],
+            torch.from_numpy(vn).double()[None], is_causal=True, scale=scale_of(d))[0].numpy()
+        assert np.abs(f32(o[0, h]) - ref).max() <= 1.5e-2
+        assert int(edges[h]) == n * (n + 1) // 2
