@@ -228,10 +228,12 @@ __global__ void wait_timeout_check_kernel(uint64_t limit_ns, int* err) {
 
 msa_status attention(const msa_shape& s, const void* q, const void* k, const void* v, void* o, float* lse,
                      int64_t* edges, const std::vector<Unit>& units, const AttnArgs& idx, cudaStream_t stream) {
-  CUtensorMap tq, tk, tv;
-  if (!make_bf16_map(&tq, q, (int64_t)s.B * s.Hq, s.n, s.d_h, 64) ||
-      !make_bf16_map(&tk, k, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64) ||
-      !make_bf16_map(&tv, v, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64))
+  AttnMaps maps;
+  if (!make_bf16_map(&maps.q, q, (int64_t)s.B * s.Hq, s.n, s.d_h, 64) ||
+      !make_bf16_map(&maps.k, k, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64) ||
+      !make_bf16_map(&maps.v, v, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64) ||
+      !make_bf16_map(&maps.k16, k, (int64_t)s.B * s.Hkv, s.n, s.d_h, 16) ||
+      !make_bf16_map(&maps.v16, v, (int64_t)s.B * s.Hkv, s.n, s.d_h, 16))
     return MSA_ERR_CUDA;
   AttnArgs a = idx;
   a.n = s.n;
@@ -247,7 +249,7 @@ msa_status attention(const msa_shape& s, const void* q, const void* k, const voi
   a.edges = reinterpret_cast<unsigned long long*>(edges);
   a.err = device_error_word();
   if (!a.err) return MSA_ERR_CUDA;
-  return launch_attention(tq, tk, tv, a, units.data(), (int)units.size(), stream);
+  return launch_attention(maps, a, units.data(), (int)units.size(), stream);
 }
 
 }  // namespace msa

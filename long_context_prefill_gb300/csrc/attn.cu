@@ -10,13 +10,13 @@
 // 128-key tiles holding every key either sub-item needs.  Sharing the K/V
 // stream doubles the tensor work per loaded byte.
 //   warp 8     planner: merges the sub-items' key sets into tiles of two
-//              64-key segments (or of 128 gathered key columns) and writes
+//              64-key segments (or, for Vertical-Slash, eight 16-key
+//              segments holding attended keys) and writes
 //              each tile's descriptor (segments, per-half validity masks,
 //              per-sub-item activity and A-shape row rules) into a ring; a
 //              terminating descriptor ends the item;
 //   warp 10    loader: TMA-loads both Q tiles once, then K(j) and V(j) of
-//              every tile into a four-slot ring (K in slots 0/2, V in 1/3), or
-//              gathers single key rows with cp.async;
+//              every tile into a four-slot ring (K in slots 0/2, V in 1/3);
 //   warps 9/11 MMA issuers (one thread each, one per sub-item X): per tile,
 //              O_X += P_X V of the previous tile, then S_X = Q_X K^T.  While
 //              one sub-item's softmax runs, the tensor core works for the
@@ -59,16 +59,18 @@ constexpr uint32_t kIdleNs = 256;          // poll interval of the planner's and
 constexpr bool kTurnLock = true;            // sub-items take turns on each SMSP's MUFU
 
 
-enum TileKind : int32_t { kTileRange = 0, kTileGather = 1, kTileEnd = 2 };
+// kTileRange: two 64-key segments (seg[0], seg[1]); kTileRange16: eight 16-key
+// segments (seg[0..7], non-decreasing; seg_hi = the last attended one).
+enum TileKind : int32_t { kTileRange = 0, kTileRange16 = 1, kTileEnd = 2 };
 
 struct TileDesc {
-  int32_t seg[2];       // range tiles: first key of each 64-key segment
+  int32_t seg[8];       // first key of each segment
+  int32_t seg_hi;
   int32_t kind;         // TileKind (kTileEnd: no more tiles in this item)
   uint8_t rule[2][2];   // A-shape row rule per [sub-item][segment]: bit0 j < sink, bit1 j > i - window
   uint8_t active[2];    // sub-item X attends some key of this tile
   uint8_t pad[2];
   uint32_t mask[4][4];  // per half 2X+h: bit k = key k of the tile may be attended
-  int32_t gidx[128];    // gather tiles: key of column k, ascending, then -1
 };
 
 enum {
@@ -89,8 +91,7 @@ struct Layout {
   static constexpr int kQ = 0;               // the two Q tiles
   static constexpr int kRing = kQ + 2 * kTile;
   static constexpr int kDesc = kRing + kSlots * kTile;
-  static constexpr int kStage = kDesc + kDescSlots * (int)sizeof(TileDesc);  // gather staging (256 ints)
-  static constexpr int kBlk = kStage + 256 * 4;                             // Block-Sparse lists
+  static constexpr int kBlk = kDesc + kDescSlots * (int)sizeof(TileDesc);  // Block-Sparse lists
   static constexpr int kBars = kBlk + 4 * kMaxStagedBlocks * 4;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 64;  // misc words: [0] TMEM base, [2] abort, [8..11] exponential turns
@@ -297,13 +298,15 @@ struct BlockSeg {
 // columns C, restricted to j <= i.  For a full block, key j is covered iff bit
 // n-1-a+j of the dilated coverage map is set, so a 32-key mask word is a
 // 32-bit window of that map; a ragged last block (fewer than 64 rows) is
-// dilated exactly from D.  64-key blocks that some half's slash tiles touch
-// become range segments (two per tile) whose masks include the verticals in
-// them; verticals in the other blocks are gathered into column tiles.
+// dilated exactly from D.  Every 16-key segment holding a key that one of the
+// item's four halves attends (slash-covered or a vertical) is loaded whole;
+// eight such segments, ascending, make a tile.  Against 64-key segments this
+// drops about an eighth of the Vertical-Slash tiles (isolated slash runs and
+// verticals occupy a fraction of a 64-key block).
 //
 // The whole warp runs it: lane l evaluates key block grp + l of a group of 32
-// (all loads of a group in flight at once), then the group is emitted in
-// ascending block order.
+// (all loads of a group in flight at once); the segments are then placed in
+// ascending order from a warp prefix sum.
 
 // Bits [p, p+32) of an n-bit map held in nw words (zeros outside the map).
 __device__ __forceinline__ uint32_t bits32_at(const uint32_t* bits, int nw, int p) {
@@ -338,11 +341,9 @@ struct VSSeg {
   const uint32_t* cover[2];
   int cw, nw, NB, hi_key, two;
   int a[4], e[4], L[4], ex[4];
-  int grp;                // first block of the current 32-block group
-  uint32_t rmask, cmask;  // group blocks that are range segments / that only hold columns
-  uint32_t m[4][2];       // this lane's block: attend masks per half (range blocks)
-  uint32_t cf[2][2];      // this lane's block: column words of each index slot
-  int staged;             // staged columns: key | in-slot-0 << 28 | in-slot-1 << 29
+  int grp;           // first block of the current 32-block group
+  uint32_t m[4][2];  // this lane's block: attend masks per half
+  uint32_t qm;       // this lane's block: 16-key quarters with attended keys, not yet placed
   __device__ void init(const Unit& U, const Geo& G, const AttnArgs& A) {
     cw = A.vs_cover_words;
     nw = A.vs_words;
@@ -364,169 +365,106 @@ struct VSSeg {
       L[hh] = e[hh] - a[hh] + 1;
     }
     grp = -32;
-    rmask = cmask = 0u;
-    staged = 0;
+    qm = 0u;
   }
+  // Masks of the 32 blocks of the next group, one lane per 64-key block.
   __device__ void load_group(int lane, int n) {
     grp += 32;
     const int b = grp + lane;
-    bool sl = false, cols = false;
-    if (b < NB) {
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        const int base = 64 * b + 32 * w;
-        const uint32_t kin = keys_below(base, hi_key + 1);
-        cf[0][w] = base <= hi_key ? __ldg(cbits[0] + (base >> 5)) & kin : 0u;
-        cf[1][w] = two ? (base <= hi_key ? __ldg(cbits[1] + (base >> 5)) & kin : 0u) : cf[0][w];
-#pragma unroll
-        for (int hh = 0; hh < 4; ++hh) {
-          uint32_t s = 0u;
-          if (ex[hh] && base <= e[hh]) {
-            s = L[hh] == 64 ? bits_window32(cover[hh >> 1], cw, n - 1 - a[hh] + base)
-                            : exact_cover32(dbits[hh >> 1], nw, a[hh] - base, L[hh]);
-            s &= keys_below(base, e[hh] + 1);
-          }
-          m[hh][w] = s;
-          sl = sl || s != 0u;
-        }
-      }
-      if (sl) {
-#pragma unroll
-        for (int hh = 0; hh < 4; ++hh)
-#pragma unroll
-          for (int w = 0; w < 2; ++w)
-            if (ex[hh]) m[hh][w] |= cf[hh >> 1][w] & keys_below(64 * b + 32 * w, e[hh] + 1);
-      }
-      cols = !sl && (cf[0][0] | cf[0][1] | cf[1][0] | cf[1][1]) != 0u;
-    }
-    rmask = __ballot_sync(0xFFFFFFFFu, sl);
-    cmask = __ballot_sync(0xFFFFFFFFu, cols);
-  }
-  // Block grp+b (its masks live in lane b) becomes segment s of d.
-  __device__ void put_segment(int lane, int b, int s, TileDesc& d) const {
-    if (lane == b) {
-#pragma unroll
-      for (int hh = 0; hh < 4; ++hh) {
-        d.mask[hh][2 * s] = m[hh][0];
-        d.mask[hh][2 * s + 1] = m[hh][1];
-      }
-      d.seg[s] = 64 * (grp + b);
-    }
-  }
-  __device__ static void finish_range(int lane, TileDesc& d, bool single) {
-    __syncwarp();
-    if (lane == 0) {
-      if (single) {  // reload the same segment, masked
-        d.seg[1] = d.seg[0];
-        for (int hh = 0; hh < 4; ++hh) d.mask[hh][2] = d.mask[hh][3] = 0u;
-      }
-      d.kind = kTileRange;
-      for (int X = 0; X < 2; ++X) {
-        uint32_t any = 0;
-        for (int q = 0; q < 4; ++q) any |= d.mask[2 * X][q] | d.mask[2 * X + 1][q];
-        d.active[X] = any != 0u;
-        d.rule[X][0] = d.rule[X][1] = 0;
-      }
-    }
-  }
-  // Append the columns of block grp+b (ascending) to the staging list.
-  __device__ void stage_block(int lane, int b, int* stage) {
+    uint32_t un[2] = {0u, 0u};
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
-      const uint32_t w0 = __shfl_sync(0xFFFFFFFFu, cf[0][w], b);
-      const uint32_t w1 = __shfl_sync(0xFFFFFFFFu, cf[1][w], b);
-      const uint32_t in0 = (w0 >> lane) & 1u, in1 = (w1 >> lane) & 1u;
-      const bool ok = (in0 | in1) != 0u;
-      const uint32_t bb = __ballot_sync(0xFFFFFFFFu, ok);
-      if (ok)
-        stage[staged + __popc(bb & ((1u << lane) - 1u))] =
-            (64 * (grp + b) + 32 * w + lane) | (int)(in0 << 28) | (int)(in1 << 29);
-      staged += __popc(bb);
-    }
-    __syncwarp();
-  }
-  __device__ void gather_tile(int lane, int* stage, TileDesc& d) {
-    const int take = staged < 128 ? staged : 128;
-    uint32_t mk[4][4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int k = 32 * q + lane;
-      const int s = k < take ? stage[k] : 0;
-      const int key = s & 0x0FFFFFFF;
-      d.gidx[k] = k < take ? key : -1;
+      const int base = 64 * b + 32 * w;
+      const uint32_t kin = keys_below(base, hi_key + 1);
+      const uint32_t c0 = (b < NB && base <= hi_key) ? __ldg(cbits[0] + (base >> 5)) & kin : 0u;
+      const uint32_t c1 = two ? ((b < NB && base <= hi_key) ? __ldg(cbits[1] + (base >> 5)) & kin : 0u) : c0;
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) {
-        const bool ok = ex[hh] && k < take && key <= e[hh] && ((s >> (28 + (hh >> 1))) & 1);
-        mk[hh][q] = __ballot_sync(0xFFFFFFFFu, ok);
-      }
-    }
-    __syncwarp();
-    // shift the rest of the staging list down (rest < take, so the ranges do not overlap)
-    const int rest = staged - take;
-    for (int k = lane; k < rest; k += 32) stage[k] = stage[take + k];
-    __syncwarp();
-    staged = rest;
-    if (lane == 0) {
-#pragma unroll
-      for (int hh = 0; hh < 4; ++hh)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) d.mask[hh][q] = mk[hh][q];
-      d.kind = kTileGather;
-      d.seg[0] = d.seg[1] = 0;
-#pragma unroll
-      for (int X = 0; X < 2; ++X) {
-        uint32_t any = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) any |= mk[2 * X][q] | mk[2 * X + 1][q];
-        d.active[X] = any != 0u;
-        d.rule[X][0] = d.rule[X][1] = 0;
-      }
-    }
-  }
-  // Produce the next tile into d; false when the item has no more tiles.
-  __device__ bool emit(int lane, int n, int* stage, TileDesc& d) {
-    int filled = 0;  // range segments already placed in d
-    for (;;) {
-      if (staged >= 128) {
-        if (filled == 0) { gather_tile(lane, stage, d); return true; }
-        finish_range(lane, d, true);
-        return true;
-      }
-      if ((rmask | cmask) == 0u) {
-        if (grp + 32 >= NB) {
-          if (filled == 1) { finish_range(lane, d, true); return true; }
-          if (staged > 0) { gather_tile(lane, stage, d); return true; }
-          return false;
+        uint32_t s = 0u;
+        if (b < NB && ex[hh] && base <= e[hh]) {
+          s = L[hh] == 64 ? bits_window32(cover[hh >> 1], cw, n - 1 - a[hh] + base)
+                          : exact_cover32(dbits[hh >> 1], nw, a[hh] - base, L[hh]);
+          s = (s | (hh < 2 ? c0 : c1)) & keys_below(base, e[hh] + 1);
         }
+        m[hh][w] = s;
+        un[w] |= s;
+      }
+    }
+    qm = ((un[0] & 0xFFFFu) ? 1u : 0u) | ((un[0] >> 16) ? 2u : 0u) | ((un[1] & 0xFFFFu) ? 4u : 0u) |
+         ((un[1] >> 16) ? 8u : 0u);
+  }
+  // Produce the next tile into d: the next (up to) eight 16-key segments that
+  // hold attended keys, ascending; false when the item has no more tiles.
+  // Positions come from a warp prefix sum over the lanes' quarter counts, so
+  // the lanes place their segments (and 16-bit mask pieces) in parallel.
+  __device__ bool emit(int lane, int n, TileDesc& d) {
+    uint16_t* m16 = reinterpret_cast<uint16_t*>(&d.mask[0][0]);  // [half][segment]
+    if (lane < 16) d.mask[lane >> 2][lane & 3] = 0u;
+    __syncwarp();
+    int f = 0, hi = -1;
+    uint32_t act = 0u;  // bit X: sub-item X attends a key of this tile (this lane's pieces)
+    for (;;) {
+      if (__ballot_sync(0xFFFFFFFFu, qm != 0u) == 0u) {
+        if (grp + 32 >= NB) break;
         load_group(lane, n);
         continue;
       }
-      const int b = __ffs(rmask | cmask) - 1;
-      const bool is_range = (rmask >> b) & 1u;
-      rmask &= ~(1u << b);
-      cmask &= ~(1u << b);
-      if (is_range) {
-        put_segment(lane, b, filled, d);
-        if (++filled == 2) { finish_range(lane, d, false); return true; }
-      } else {
-        stage_block(lane, b, stage);
+      const int c = __popc(qm);
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
       }
+      int pos = f + incl - c;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (!((qm >> q) & 1u)) continue;
+        if (pos < 8) {
+          const int key0 = 64 * (grp + lane) + 16 * q;
+          d.seg[pos] = key0;
+          hi = max(hi, key0);
+#pragma unroll
+          for (int hh = 0; hh < 4; ++hh) {
+            const uint32_t bits = (m[hh][q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+            if (bits) {
+              m16[hh * 8 + pos] = (uint16_t)bits;
+              act |= 1u << (hh >> 1);
+            }
+          }
+          qm &= ~(1u << q);
+        }
+        ++pos;
+      }
+      f = min(8, f + __shfl_sync(0xFFFFFFFFu, incl, 31));
+      if (f == 8) break;
     }
+    if (f == 0) return false;
+    hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+    act = __reduce_or_sync(0xFFFFFFFFu, act);
+    __syncwarp();  // d.seg[0 .. f) and the mask pieces written
+    if (lane == 0) {
+      for (int x = f; x < 8; ++x) d.seg[x] = hi;  // reload a valid segment, masked (starts stay ascending)
+      d.seg_hi = hi;
+      d.kind = kTileRange16;
+      d.active[0] = act & 1u;
+      d.active[1] = (act >> 1) & 1u;
+      d.rule[0][0] = d.rule[0][1] = d.rule[1][0] = d.rule[1][1] = 0;
+    }
+    return true;
   }
 };
 
 // ------------------------------------------------------------------ kernel
 template <int D, bool kCount>
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                       const __grid_constant__ CUtensorMap tv, const AttnArgs A,
+    sparse_attn_kernel(const __grid_constant__ AttnMaps M, const AttnArgs A,
                        const __grid_constant__ UnitTable UT) {
   using Ly = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::kBars);
   TileDesc* descs = reinterpret_cast<TileDesc*>(sm + Ly::kDesc);
-  int* stage = reinterpret_cast<int*>(sm + Ly::kStage);
   int* sblk = reinterpret_cast<int*>(sm + Ly::kBlk);
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + Ly::kMisc);  // [0] tmem, [2] abort
 
@@ -594,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileDesc& d = descs[slot];
       bool more;
       if (U.pattern == kUnitVS) {
-        more = vw.emit(lane, n, stage, d);
+        more = vw.emit(lane, n, d);
       } else {
         // lane 0 takes up to two segments of the union
         int sg[2] = {0, 0}, rl[2][2] = {{0, 0}, {0, 0}}, bits[2] = {0, 0};
@@ -649,9 +587,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kLoaderWarp) {
     // ------------------------------------------------------------ loader
     if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&M.q);
+      tma_prefetch_desc(&M.k);
+      tma_prefetch_desc(&M.v);
       // Q rows of the halves that exist (a tail past n reads zeros)
       int halves = 0;
       for (int hh = 0; hh < 4; ++hh) halves += G.ex[hh];
@@ -659,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hh = 0; hh < 4; ++hh)
         if (G.ex[hh])
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sQ + (hh >> 1) * Ly::kTile + c * 16384 + (hh & 1) * 8192, &tq, &bars[kBarQ], 64 * c,
+            tma_load_3d(sQ + (hh >> 1) * Ly::kTile + c * 16384 + (hh & 1) * 8192, &M.q, &bars[kBarQ], 64 * c,
                         G.row0[hh], U.sub[hh >> 1].qh[hh & 1]);
     }
     // K(j) into slot 2j, V(j) into 2j+1 (mod kSlots): the MMA releases them in that order
@@ -672,25 +610,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* full = &bars[kBarFull + st];
       if (d.kind == kTileRange) {
         if (lane == 0) {
-          const CUtensorMap* map = is_v ? &tv : &tk;
+          const CUtensorMap* map = is_v ? &M.v : &M.k;
           mbar_arrive_expect_tx(full, Ly::kTile);
           for (int s = 0; s < 2; ++s)
             for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384 + s * 8192, map, full, 64 * c, d.seg[s], U.kvh);
         }
       } else {
-        // gather single key rows (16-byte cp.async) into the swizzled layout
-        constexpr int kChunks16 = D / 8;
-        const uint8_t* gbase = reinterpret_cast<const uint8_t*>(is_v ? A.v : A.k) + (int64_t)U.kvh * n * D * 2;
-        for (int x = lane; x < 128 * kChunks16; x += 32) {
-          const int r = x / kChunks16, c16 = x % kChunks16;
-          int key = d.gidx[r];
-          key = key < 0 ? 0 : key;  // empty columns reload key 0 (finite data, masked)
-          cp_async16(dst + (c16 >> 3) * 16384 + sw128_offset(r, c16 & 7), gbase + ((int64_t)key * D + 8 * c16) * 2);
-        }
-        cp_async_wait_all();
-        fence_proxy_async_smem();
+        // eight 16-key segments (lane 8c + x: segment x, columns 64c..): a run
+        // of four contiguous segments loads as one 64-row box
+        if (lane == 0) mbar_arrive_expect_tx(full, Ly::kTile);
         __syncwarp();
-        if (lane == 0) mbar_arrive(full);
+        if (lane < 8 * (D / 64)) {
+          const int x = lane & 7, c = lane >> 3, h4 = x & ~3;
+          const int s0 = d.seg[h4];
+          const bool run = d.seg[h4 + 1] == s0 + 16 && d.seg[h4 + 2] == s0 + 32 && d.seg[h4 + 3] == s0 + 48;
+          if (!run)
+            tma_load_3d(dst + c * 16384 + x * 2048, is_v ? &M.v16 : &M.k16, full, 64 * c, d.seg[x], U.kvh);
+          else if (x == h4)
+            tma_load_3d(dst + c * 16384 + x * 2048, is_v ? &M.v : &M.k, full, 64 * c, s0, U.kvh);
+        }
       }
       return true;
     };
@@ -804,33 +742,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- validity words of this row's 128 keys
       uint64_t vw[2] = {0ull, 0ull};
       if (row_ok) {
-        int cg = 0;  // gather tiles: columns k < cg hold keys <= i (keys ascend, -1 last)
-        if (kind == kTileGather) {
-          int lo = 0, hi = 128;
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            const int gj = d.gidx[mid];
-            if (gj >= 0 && gj <= i) lo = mid + 1;
-            else hi = mid;
-          }
-          cg = lo;
-        }
+        // causal keys of each 64-column half are its first c[s] columns: for
+        // 64-key segments c = i - start + 1; for 16-key segments keys ascend
+        // over the tile, so the count comes from a 3-step search over the
+        // eight segment starts and the partial one
+        int c0, c1;
+        if (kind == kTileRange) {
+          c0 = i - d.seg[0] + 1;
+          c1 = i - d.seg[1] + 1;
+        } else if (d.seg_hi + 15 <= i) {
+          c0 = c1 = 64;
+        } else {
+          int sc = 0;
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const uint64_t m64 = ((uint64_t)d.mask[hh][2 * s + 1] << 32) | d.mask[hh][2 * s];
-          if (kind == kTileRange) {
-            const int base = d.seg[s];
-            uint64_t v = m64 & low_mask64(i - base + 1);  // causal: j <= i
-            if (ashape) {
-              const int rule = d.rule[X][s];
-              uint64_t keep = 0;
-              if (rule & 1) keep |= low_mask64(g - base);             // j < g
-              if (rule & 2) keep |= ~low_mask64(i - wnd + 1 - base);  // j > i - w
-              v &= keep;
-            }
-            vw[s] = v;
-          } else {
-            vw[s] = m64 & low_mask64(cg - 64 * s);
+          for (int step = 4; step; step >>= 1)
+            if (d.seg[sc + step - 1] + 15 <= i) sc += step;
+          c0 = 16 * sc + min(max(i - d.seg[sc] + 1, 0), 16);  // sc <= 7 here
+          c1 = c0 - 64;
+        }
+        vw[0] = (((uint64_t)d.mask[hh][1] << 32) | d.mask[hh][0]) & low_mask64(c0);
+        vw[1] = (((uint64_t)d.mask[hh][3] << 32) | d.mask[hh][2]) & low_mask64(c1);
+        if (ashape) {
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            const int base = d.seg[s], rule = d.rule[X][s];
+            uint64_t keep = 0;
+            if (rule & 1) keep |= low_mask64(g - base);             // j < g
+            if (rule & 2) keep |= ~low_mask64(i - wnd + 1 - base);  // j > i - w
+            vw[s] &= keep;
           }
         }
       }
@@ -981,8 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, bool kCount>
-msa_status launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
-                       const UnitTable& ut, cudaStream_t stream) {
+msa_status launch_impl(const AttnMaps& maps, const AttnArgs& a, const UnitTable& ut, cudaStream_t stream) {
   auto kern = sparse_attn_kernel<D, kCount>;
   const int smem = Layout<D>::kAlloc;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -990,15 +928,15 @@ msa_status launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   const int64_t items = (int64_t)a.T * a.n_units;
   if (items <= 0) return MSA_OK;
   if (items > 0x7FFFFFFF) return MSA_ERR_UNSUPPORTED;
-  kern<<<(unsigned)items, kThreads, smem, stream>>>(tq, tk, tv, a, ut);
+  kern<<<(unsigned)items, kThreads, smem, stream>>>(maps, a, ut);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 }  // namespace
 
-msa_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const AttnArgs& args, const Unit* units, int n_units, cudaStream_t stream) {
+msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Unit* units, int n_units,
+                            cudaStream_t stream) {
   for (int base = 0; base < n_units; base += kMaxUnits) {
     UnitTable ut;
     const int cnt = n_units - base < kMaxUnits ? n_units - base : kMaxUnits;
@@ -1014,9 +952,9 @@ msa_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const 
     msa_status st;
     const bool count = args.edges != nullptr;
     if (args.d == 128)
-      st = count ? launch_impl<128, true>(tq, tk, tv, a, ut, stream) : launch_impl<128, false>(tq, tk, tv, a, ut, stream);
+      st = count ? launch_impl<128, true>(maps, a, ut, stream) : launch_impl<128, false>(maps, a, ut, stream);
     else
-      st = count ? launch_impl<64, true>(tq, tk, tv, a, ut, stream) : launch_impl<64, false>(tq, tk, tv, a, ut, stream);
+      st = count ? launch_impl<64, true>(maps, a, ut, stream) : launch_impl<64, false>(maps, a, ut, stream);
     if (st != MSA_OK) return st;
   }
   return MSA_OK;

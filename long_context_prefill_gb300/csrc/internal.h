@@ -77,9 +77,15 @@ struct AttnArgs {
   int* err;
 };
 
+// TMA views of the attention operands as [BH, n, d]: Q, K, V with boxes of
+// 64 columns x 64 rows, and K, V again with 64 x 16 boxes (16-key segments).
+struct alignas(64) AttnMaps {
+  CUtensorMap q, k, v, k16, v16;
+};
+
 // Launch the attention engine over n_units units of T items each.
-msa_status launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const AttnArgs& args, const Unit* units, int n_units, cudaStream_t stream);
+msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Unit* units, int n_units,
+                            cudaStream_t stream);
 
 // ------------------------------------------------------------ TMA tensor maps
 // 3-D bf16 map over [BH, n, d] with a box of 64 columns x box_rows rows and
