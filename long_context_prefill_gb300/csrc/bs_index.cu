@@ -8,7 +8,8 @@
 // Kernels: block_pool (reads Q of the listed heads and K of their KV heads
 // once: the byte cost of this index), block_scores (register-blocked fp32
 // GEMM over the causal triangle of block pairs, written packed), block_topk
-// (one warp per query block: radix select on order-preserving keys, then an
+// (one warp per query block: rows of up to 2048 candidates in registers with a
+// bitwise search for the k-th key, longer rows by radix select; then an
 // index-ordered compaction, which leaves J_u ascending).
 #include <cuda_bf16.h>
 #include <string.h>
@@ -119,63 +120,72 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 constexpr int kTopkWarps = 4;
-constexpr int kRegKeys = 64;  // rows of up to 2048 candidates are selected in registers
 
-// One warp per (slot, query block u): J_u = {u} ∪ top_{k-1} of row u.
+// J_u from a row of u <= 32 R candidates held in registers (key of v = lane +
+// 32 i in key[i]; 0, below every real key, for v >= u): the k1-th largest key
+// T by a bitwise search on warp counts, then every key above T and the first
+// (in index order) equal to it.  Rows are bucketed by length (R = 16, 32, 64)
+// so a short row does not pay for the longest one.
+template <int R>
+__device__ __forceinline__ void topk_row_regs(const float* row, int u, int k1, int topk, int lane, int32_t* out,
+                                              int32_t* cnt) {
+  uint32_t key[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int v = lane + 32 * i;
+    key[i] = v < u ? order_key(row[v]) : 0u;
+  }
+  uint32_t T = 0;
+  for (int b = 31; b >= 0; --b) {
+    const uint32_t cand = T | (1u << b);
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < R; ++i) c += key[i] >= cand ? 1 : 0;
+    c = __reduce_add_sync(0xFFFFFFFFu, c);
+    if (c >= k1) T = cand;
+  }
+  int above = 0;
+#pragma unroll
+  for (int i = 0; i < R; ++i) above += key[i] > T ? 1 : 0;
+  above = __reduce_add_sync(0xFFFFFFFFu, above);
+  const int need_eq = k1 - above;
+  int pos = 0, eq_seen = 0;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    if (32 * i >= u) break;
+    const bool gt = key[i] > T, eq = key[i] == T;
+    const unsigned eqm = __ballot_sync(0xFFFFFFFFu, eq);
+    const int eq_rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
+    const bool sel = gt || (eq && eq_rank < need_eq);
+    const unsigned selm = __ballot_sync(0xFFFFFFFFu, sel);
+    if (sel) out[pos + __popc(selm & ((1u << lane) - 1u))] = lane + 32 * i;
+    pos += __popc(selm);
+    eq_seen += __popc(eqm);
+  }
+  for (int x = k1 + lane; x < topk; x += 32) out[x] = (x == k1) ? u : -1;  // diagonal last (largest id)
+  if (lane == 0) *cnt = k1 + 1;
+}
+
+// One warp per (slot, query block u): J_u = {u} ∪ top_{k-1} of row u.  Rows
+// longer than 2048 candidates use a radix select over a per-warp histogram in
+// dynamic shared memory (kTopkWarps x 2048 ints, given only when nb > 2048).
 __global__ void __launch_bounds__(32 * kTopkWarps) block_topk_kernel(const float* scores, int nb, int topk,
                                                                       int nslots, int32_t* J, int32_t* cnt) {
-  __shared__ int hist[kTopkWarps][2048];
+  extern __shared__ int hist_all[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t job = (int64_t)blockIdx.x * kTopkWarps + warp;
   if (job >= (int64_t)nslots * nb) return;
   const int slot = (int)(job / nb), u = (int)(job % nb);
   const float* row = scores + (int64_t)slot * ((int64_t)nb * (nb + 1) / 2) + (int64_t)u * (u + 1) / 2;
   int32_t* out = J + job * topk;
-  int* h = hist[warp];
   const int k1 = min(topk - 1, u);  // picks among v < u
-  if (u <= 32 * kRegKeys && k1 < u && k1 > 0) {
-    // Row held in registers (key of v = lane + 32 i in key[i]; 0 below every
-    // real key for v >= u): the k1-th largest key T by a bitwise search on
-    // counts, then every key above T and the first (in index order) equal to it.
-    uint32_t key[kRegKeys];
-#pragma unroll
-    for (int i = 0; i < kRegKeys; ++i) {
-      const int v = lane + 32 * i;
-      key[i] = v < u ? order_key(row[v]) : 0u;
-    }
-    uint32_t T = 0;
-    for (int b = 31; b >= 0; --b) {
-      const uint32_t cand = T | (1u << b);
-      int c = 0;
-#pragma unroll
-      for (int i = 0; i < kRegKeys; ++i) c += key[i] >= cand ? 1 : 0;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
-      if (c >= k1) T = cand;
-    }
-    int above = 0;
-#pragma unroll
-    for (int i = 0; i < kRegKeys; ++i) above += key[i] > T ? 1 : 0;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) above += __shfl_xor_sync(0xFFFFFFFFu, above, o);
-    const int need_eq = k1 - above;
-    int pos = 0, eq_seen = 0;
-#pragma unroll
-    for (int i = 0; i < kRegKeys; ++i) {
-      if (32 * i >= u) break;
-      const bool gt = key[i] > T, eq = key[i] == T;
-      const unsigned eqm = __ballot_sync(0xFFFFFFFFu, eq);
-      const int eq_rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
-      const bool sel = gt || (eq && eq_rank < need_eq);
-      const unsigned selm = __ballot_sync(0xFFFFFFFFu, sel);
-      if (sel) out[pos + __popc(selm & ((1u << lane) - 1u))] = lane + 32 * i;
-      pos += __popc(selm);
-      eq_seen += __popc(eqm);
-    }
-    for (int x = k1 + lane; x < topk; x += 32) out[x] = (x == k1) ? u : -1;  // diagonal last (largest id)
-    if (lane == 0) cnt[job] = k1 + 1;
+  if (u <= 2048 && k1 < u && k1 > 0) {
+    if (u <= 512) topk_row_regs<16>(row, u, k1, topk, lane, out, cnt + job);
+    else if (u <= 1024) topk_row_regs<32>(row, u, k1, topk, lane, out, cnt + job);
+    else topk_row_regs<64>(row, u, k1, topk, lane, out, cnt + job);
     return;
   }
+  int* h = hist_all + warp * 2048;
   uint32_t prefix = 0, pmask = 0;
   int need = k1;
   const bool all = (k1 >= u);
@@ -332,7 +342,8 @@ msa_status run_bs(const msa_shape& s, const void* q, const void* k, const BSPlan
     if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   }
   const int64_t jobs = (int64_t)P.slots * P.nb;
-  block_topk_kernel<<<(unsigned)((jobs + kTopkWarps - 1) / kTopkWarps), 32 * kTopkWarps, 0, stream>>>(
+  const int hist_bytes = P.nb > 2048 ? kTopkWarps * 2048 * (int)sizeof(int) : 0;
+  block_topk_kernel<<<(unsigned)((jobs + kTopkWarps - 1) / kTopkWarps), 32 * kTopkWarps, hist_bytes, stream>>>(
       sc, P.nb, topk, P.slots, J, cnt);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;

@@ -21,6 +21,7 @@
 //                 that writes the sorted lists and the bitmaps
 // K is streamed once per pass per group of query heads sharing a KV head; the
 // second pass mostly hits L2.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <math.h>
 #include <string.h>
@@ -420,7 +421,8 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // ------------------------------------------------------------------ top-k
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 512;
+constexpr int kTopkCluster = 8;  // CTAs per score vector
 
 __device__ int block_excl_scan(int v, int* sh, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -466,11 +468,11 @@ struct TopkArgs {
   int32_t vk, sk;
 };
 
-__device__ __forceinline__ TopkJob topk_job(const TopkArgs& a, int n) {
-  const int slot = blockIdx.x >> 1;
+__device__ __forceinline__ TopkJob topk_job(const TopkArgs& a, int n, int vec) {
+  const int slot = vec >> 1;
   const int words = (n + 31) / 32;
   TopkJob J;
-  if ((blockIdx.x & 1) == 0) {
+  if ((vec & 1) == 0) {
     J.vals = a.colsum + (int64_t)slot * n;
     J.list = a.out.vertical + (int64_t)slot * a.out.v_cap;
     J.cnt = a.out.vertical_cnt + slot;
@@ -488,84 +490,204 @@ __device__ __forceinline__ TopkJob topk_job(const TopkArgs& a, int n) {
   return J;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs args, int n) {
-  const TopkJob J = topk_job(args, n);
-  __shared__ int hist[2048];
+// One cluster of kTopkCluster CTAs per score vector (cluster c: vector c, as
+// in topk_job); CTA r owns words [r cw, (r+1) cw) of the n values.
+//  1. the cluster's min and max order keys fix the bits all keys share;
+//  2. radix select, 8 bits per pass from the highest differing bit down: each
+//     CTA histograms its keys that match the prefix chosen so far (one
+//     histogram per warp, summed), the cluster adds the CTAs' histograms
+//     through distributed shared memory, and every CTA picks the same digit;
+//     the k-th largest key T and the number `need` of keys equal to T to keep
+//     come out;
+//  3. each CTA counts its keys above T and equal to T; from the counts of the
+//     CTAs before it (index order) it knows where its selected keys go, and
+//     writes the bitmap words and the sorted list (ties: lower index first).
+__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
+    topk_kernel(const TopkArgs args, int n) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const TopkJob J = topk_job(args, n, (int)(blockIdx.x / kTopkCluster));
+  __shared__ int whist[kTopkThreads / 32][256];
+  __shared__ int chist[256];     // this CTA's histogram of the current pass (read cluster-wide)
+  __shared__ int ghist[256];     // the cluster's histogram
+  __shared__ uint32_t s_mm[2];   // this CTA's min / max key (read cluster-wide)
+  __shared__ int s_cnt[2];       // this CTA's keys above / equal to T (read cluster-wide)
   __shared__ int sh[32];
-  __shared__ int s_digit, s_above;
+  __shared__ uint32_t s_u[2];
+  __shared__ int s_i[2];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int words = (n + 31) / 32;
+  const int cw = (words + kTopkCluster - 1) / kTopkCluster;
+  const int w0 = min(words, rank * cw), w1 = min(words, w0 + cw);
+  const int x0 = 32 * w0, x1 = min(n, 32 * w1);
   const int k = J.k < n ? J.k : n;
-  uint32_t prefix = 0, pmask = 0;
-  int need = k;  // how many to take among values matching the prefix
-  if (k > 0 && k < n) {
-    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
-      const int sft = shifts[pass], nb = 1 << widths[pass];
-      for (int b = threadIdx.x; b < nb; b += blockDim.x) hist[b] = 0;
-      __syncthreads();
-      for (int x = threadIdx.x; x < n; x += blockDim.x) {
-        const uint32_t key = order_key(J.vals[x]);
-        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sft) & (nb - 1)], 1);
+  const bool all = k >= n, none = k <= 0;
+  uint32_t T = 0;
+  int need = k;
+  if (!all && !none) {
+    // ---- 1. common leading bits
+    uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+    for (int x = x0 + tid; x < x1; x += kTopkThreads) {
+      const uint32_t key = order_key(J.vals[x]);
+      mn = min(mn, key);
+      mx = max(mx, key);
+    }
+    mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    if (lane == 0) { whist[warp][0] = (int)mn; whist[warp][1] = (int)mx; }
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t a = 0xFFFFFFFFu, b = 0u;
+      if (lane < kTopkThreads / 32) { a = (uint32_t)whist[lane][0]; b = (uint32_t)whist[lane][1]; }
+      a = __reduce_min_sync(0xFFFFFFFFu, a);
+      b = __reduce_max_sync(0xFFFFFFFFu, b);
+      if (lane == 0) { s_mm[0] = a; s_mm[1] = b; }
+    }
+    cluster.sync();
+    if (warp == 0) {
+      uint32_t a = 0xFFFFFFFFu, b = 0u;
+      if (lane < kTopkCluster) {
+        const uint32_t* r = cluster.map_shared_rank(s_mm, lane);
+        a = r[0];
+        b = r[1];
       }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        int cum = 0, b = nb - 1;
-        for (; b > 0; --b) {
-          if (cum + hist[b] >= need) break;
-          cum += hist[b];
+      a = __reduce_min_sync(0xFFFFFFFFu, a);
+      b = __reduce_max_sync(0xFFFFFFFFu, b);
+      if (lane == 0) { s_u[0] = a; s_u[1] = b; }
+    }
+    __syncthreads();
+    const uint32_t gmin = s_u[0], gmax = s_u[1];
+    if (gmin == gmax) {
+      T = gmin;  // every key is equal: the first k by index
+    } else {
+      // ---- 2. radix select below the shared bits
+      int lo = 32 - __clz(gmin ^ gmax);  // bits [0, lo) still open
+      uint32_t pmask = lo == 32 ? 0u : ~((1u << lo) - 1u);
+      uint32_t prefix = gmin & pmask;
+      while (lo > 0) {
+        const int width = lo < 8 ? lo : 8, sft = lo - width;
+        const uint32_t dmask = (1u << width) - 1u;
+        for (int b = lane; b < 256; b += 32) whist[warp][b] = 0;
+        __syncthreads();
+        for (int x = x0 + tid; x < x1; x += kTopkThreads) {
+          const uint32_t key = order_key(J.vals[x]);
+          if ((key & pmask) == prefix) atomicAdd(&whist[warp][(key >> sft) & dmask], 1);
         }
-        s_digit = b;
-        s_above = cum;
+        __syncthreads();
+        if (tid < 256) {
+          int v = 0;
+#pragma unroll
+          for (int w = 0; w < kTopkThreads / 32; ++w) v += whist[w][tid];
+          chist[tid] = v;
+        }
+        cluster.sync();
+        if (tid < 256) {
+          int v = 0;
+#pragma unroll
+          for (int r = 0; r < kTopkCluster; ++r) v += cluster.map_shared_rank(chist, r)[tid];
+          ghist[tid] = v;
+        }
+        __syncthreads();
+        if (warp == 0) {
+          // digit of the need-th largest: suffix sums, 8 bins per lane (higher lanes hold higher bins)
+          int mine = 0;
+#pragma unroll
+          for (int b = 0; b < 8; ++b) mine += ghist[8 * lane + b];
+          int suf = mine;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+            if (lane + o < 32) suf += y;
+          }
+          const int excl = suf - mine;
+          const unsigned who = __ballot_sync(0xFFFFFFFFu, excl < need && suf >= need);
+          const int src = __ffs(who) - 1;
+          if (lane == src) {
+            int cum = excl, d = 8 * lane;
+            for (int b = 7; b >= 0; --b) {
+              const int c = ghist[8 * lane + b];
+              if (cum + c >= need) { d = 8 * lane + b; break; }
+              cum += c;
+            }
+            s_i[0] = d;
+            s_i[1] = cum;
+          }
+        }
+        cluster.sync();  // every CTA has read the histograms of this pass
+        need -= s_i[1];
+        prefix |= (uint32_t)s_i[0] << sft;
+        pmask |= dmask << sft;
+        lo = sft;
       }
-      __syncthreads();
-      need -= s_above;
-      prefix |= (uint32_t)s_digit << sft;
-      pmask |= (uint32_t)(nb - 1) << sft;
-      __syncthreads();
+      T = prefix;
     }
   }
-  // prefix = bit pattern of the k-th largest; `need` values equal to it are taken
-  const bool all = (k >= n), none = (k <= 0);
-  int base_sel = 0, base_eq = 0;
-  for (int w0 = 0; w0 < words; w0 += blockDim.x) {
-    const int w = w0 + threadIdx.x;
-    uint32_t gt = 0, eq = 0;
-    if (w < words) {
-      for (int b = 0; b < 32; ++b) {
-        const int x = w * 32 + b;
-        if (x >= n) break;
-        const uint32_t key = order_key(J.vals[x]);
-        if (all || (!none && key > prefix)) gt |= 1u << b;
-        else if (!all && !none && key == prefix) eq |= 1u << b;
-      }
+  // ---- 3. counts, then placement in index order
+  auto word_bits = [&](int w, uint32_t& gt, uint32_t& eq) {
+    gt = eq = 0u;
+    for (int b = 0; b < 32; ++b) {
+      const int x = 32 * w + b;
+      if (x >= n) break;
+      const uint32_t key = order_key(J.vals[x]);
+      if (all || (!none && key > T)) gt |= 1u << b;
+      else if (!none && key == T) eq |= 1u << b;
     }
+  };
+  int cnt_gt = 0, cnt_eq = 0;
+  for (int w = w0 + tid; w < w1; w += kTopkThreads) {
+    uint32_t gt, eq;
+    word_bits(w, gt, eq);
+    cnt_gt += __popc(gt);
+    cnt_eq += __popc(eq);
+  }
+  {
+    int tg, te;
+    block_excl_scan(cnt_gt, sh, tg);
+    block_excl_scan(cnt_eq, sh, te);
+    if (tid == 0) { s_cnt[0] = tg; s_cnt[1] = te; }
+  }
+  cluster.sync();
+  int base_sel = 0, base_eq = 0, total_sel = 0, eq_run = 0;  // eq_run: equal keys of the CTAs before r
+  for (int r = 0; r < kTopkCluster; ++r) {
+    const int* c = cluster.map_shared_rank(s_cnt, r);
+    const int g = c[0], e = c[1];
+    const int take = min(max(need - eq_run, 0), e);
+    if (r == rank) { base_sel = total_sel; base_eq = eq_run; }
+    total_sel += g + take;
+    eq_run += e;
+  }
+  cluster.sync();  // the counts have been read: no CTA may exit before that
+  for (int wb = w0; wb < w1; wb += kTopkThreads) {
+    const int w = wb + tid;
+    uint32_t gt = 0u, eq = 0u;
+    if (w < w1) word_bits(w, gt, eq);
     int eq_total;
     const int eq_before = block_excl_scan(__popc(eq), sh, eq_total) + base_eq;
-    // keep the first `need` equal values in index order
-    uint32_t take = 0;
-    int rank = eq_before;
+    uint32_t take = 0u;
+    int rk = eq_before;
     for (int b = 0; b < 32; ++b)
       if ((eq >> b) & 1u) {
-        if (rank < need) take |= 1u << b;
-        ++rank;
+        if (rk < need) take |= 1u << b;
+        ++rk;
       }
     const uint32_t sel = gt | take;
     int sel_total;
     const int pos = block_excl_scan(__popc(sel), sh, sel_total) + base_sel;
-    if (w < words) {
+    if (w < w1) {
       J.bits[w] = sel;
       int p = pos;
       for (int b = 0; b < 32; ++b)
         if ((sel >> b) & 1u) {
           const int outp = J.descending ? (k - 1 - p) : p;
-          if (outp >= 0 && outp < k) J.list[outp] = w * 32 + b;
+          if (outp >= 0 && outp < k) J.list[outp] = 32 * w + b;
           ++p;
         }
     }
     base_sel += sel_total;
     base_eq += eq_total;
   }
-  if (threadIdx.x == 0) *J.cnt = base_sel < k ? base_sel : k;
+  if (rank == 0 && tid == 0) *J.cnt = total_sel < k ? total_sel : k;
 }
 
 // Dilated slash coverage: bit z = any offset of D in [n-1-z, n+62-z], z < n+63.
@@ -822,7 +944,7 @@ msa_status run_vs_index(const msa_shape& s, const void* q, const void* k, const 
   ta.out = out;
   ta.vk = vcap;
   ta.sk = scap;
-  topk_kernel<<<(unsigned)(P.slots * 2), kTopkThreads, 0, stream>>>(ta, s.n);
+  topk_kernel<<<(unsigned)(P.slots * 2 * kTopkCluster), kTopkThreads, 0, stream>>>(ta, s.n);
   note_launch();
   if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   {

@@ -81,6 +81,22 @@ def test_vs_index_random(cuda_lib, n, d, last_q, Hq, Hkv, heads, v, s):
     check_vs_against_oracle(idx, q, k, heads, last_q, v, s)
 
 
+def test_vs_index_exact_ties(cuda_lib):
+    """K = 0: every score is 0, so the proxy probabilities are 1/(i+1) and every
+    column j <= n - L gets the same sum, bit for bit on both sides (each column
+    adds the same row values in the same order).  The lower index must win, and
+    the tied run spans every CTA of the device's top-k.  The slash sums tie in
+    fp64 but are added along diagonals in different groupings on the device, so
+    the slash set is held to the score tolerance only."""
+    n = 20000
+    q, k, _ = synth.random_qkv(1, 2, 1, n, 128, seed=5, device="cuda")
+    k = torch.zeros_like(k)
+    idx = run_vs(cuda_lib, q, k, [0, 1], 64, 1000, 3000)
+    check_vs_against_oracle(idx, q, k, [0, 1], 64, 1000, 3000)
+    for slot in range(2):
+        assert idx.vertical[slot, :1000].cpu().tolist() == list(range(1000))
+
+
 def test_vs_index_batch(cuda_lib):
     q, k, _ = synth.random_qkv(2, 4, 2, 600, 128, seed=21, device="cuda")
     idx = run_vs(cuda_lib, q, k, [0, 3], 64, 30, 60)
