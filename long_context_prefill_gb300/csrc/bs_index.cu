@@ -124,8 +124,10 @@ constexpr int kTopkWarps = 4;
 // J_u from a row of u <= 32 R candidates held in registers (key of v = lane +
 // 32 i in key[i]; 0, below every real key, for v >= u): the k1-th largest key
 // T by a bitwise search on warp counts, then every key above T and the first
-// (in index order) equal to it.  Rows are bucketed by length (R = 16, 32, 64)
-// so a short row does not pay for the longest one.
+// (in index order) equal to it.  The search stops as soon as exactly k1 keys
+// reach a candidate (then T = candidate - 1 and no key equal to T is taken).
+// Rows are bucketed by length (R = 16, 32, 64) so a short row does not pay for
+// the longest one.
 template <int R>
 __device__ __forceinline__ void topk_row_regs(const float* row, int u, int k1, int topk, int lane, int32_t* out,
                                               int32_t* cnt) {
@@ -142,7 +144,11 @@ __device__ __forceinline__ void topk_row_regs(const float* row, int u, int k1, i
 #pragma unroll
     for (int i = 0; i < R; ++i) c += key[i] >= cand ? 1 : 0;
     c = __reduce_add_sync(0xFFFFFFFFu, c);
-    if (c >= k1) T = cand;
+    if (c == k1) {  // exactly k1 keys reach cand: they are the set (no tie to break)
+      T = cand - 1u;
+      break;
+    }
+    if (c > k1) T = cand;
   }
   int above = 0;
 #pragma unroll
