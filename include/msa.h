@@ -137,7 +137,9 @@ MSA_API msa_status msa_build_vs_index(const msa_shape* shape, const void* q, con
  *   J_u = {u} ∪ top_{k_b - 1} { v < u } by r_uv   (ties to the lower v),
  * i.e. the causal diagonal block is always kept and counts toward k_b.
  * block_idx: [B, n_heads, N_b, topk] int32, ascending, -1 padded;
- * block_cnt: [B, n_heads, N_b] int32 = min(topk, u + 1).  N_b = ceil(n/64). */
+ * block_cnt: [B, n_heads, N_b] int32 = min(topk, u + 1).  N_b = ceil(n/64).
+ * Scores are fp32-accurate: each block mean is split into three bf16 parts and
+ * the pair products accumulate in fp32 on the tensor cores. */
 MSA_API msa_status msa_build_block_index(const msa_shape* shape, const void* q, const void* k, const int32_t* heads,
                                  int32_t n_heads, int32_t block, int32_t topk, int32_t* block_idx,
                                  int32_t* block_cnt, void* ws, size_t ws_bytes, void* stream);
@@ -155,7 +157,7 @@ MSA_API msa_status msa_build_block_index(const msa_shape* shape, const void* q, 
  * Limit: msa_block_index_workspace(shape, 64, n_heads) must not exceed
  * MSA_STATIC_SCRATCH_BYTES, else MSA_ERR_WORKSPACE_TOO_SMALL is returned and
  * nothing is launched (for d_h = 128 and one KV head per listed head: up
- * to 42 heads at n = 16384, 15 at n = 32768, 5 at n = 65536).
+ * to 31 heads at n = 16384, 12 at n = 32768, 4 at n = 65536).
  * The scratch is shared by all calls on a device: calls that overlap in time
  * (unordered streams, several host threads) race on it and must be ordered.
  * The first call on a device looks up the scratch address (a runtime call),

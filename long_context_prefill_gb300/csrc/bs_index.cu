@@ -6,8 +6,9 @@
 //   J_u      = {u} ∪ top_{k_b-1}{v < u} by r_uv, ties to the lower v
 //
 // Kernels: block_pool (reads Q of the listed heads and K of their KV heads
-// once: the byte cost of this index), block_scores (register-blocked fp32
-// GEMM over the causal triangle of block pairs, written packed), block_topk
+// once: the byte cost of this index; writes each mean as three bf16 planes),
+// block_scores (tcgen05 GEMM over the causal triangle of 128 x 128 tiles of
+// block pairs, six plane products accumulated in fp32, written packed), block_topk
 // (one warp per query block: rows of up to 2048 candidates in registers with a
 // bitwise search for the k-th key, longer rows by radix select; then an
 // index-ordered compaction, which leaves J_u ascending).
@@ -17,6 +18,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace msa {
 
@@ -24,14 +26,21 @@ namespace {
 
 constexpr int kMaxSlots = 512;
 
+__device__ __forceinline__ void set_err(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
 struct HeadMap {
   int32_t row_head[kMaxSlots];  // pooled head -> b*H + h of the source tensor
 };
 
-// Mean of each 64-row block of `src` heads listed in `map` (fp32 out [nh, nb, D]).
+// Mean of each 64-row block of `src` heads listed in `map`, written as three
+// bf16 planes whose sum is the fp32 mean to about 2^-24 (out [nh, 3, nb, D]:
+// hi = bf16(m), mid = bf16(m - hi), lo = bf16(m - hi - mid)), so the score
+// products can run on the bf16 tensor cores at fp32-like accuracy.
 template <int D>
 __global__ void __launch_bounds__(128) block_pool_kernel(const __nv_bfloat16* src, int n, int nb,
-                                                         const __grid_constant__ HeadMap map, float* out) {
+                                                         const __grid_constant__ HeadMap map, __nv_bfloat16* out) {
   constexpr int kTPR = D / 8;            // threads per row (8 columns each, 16-byte loads)
   constexpr int kGroups = 128 / kTPR;    // rows handled in parallel
   __shared__ float part[kGroups][D];
@@ -56,61 +65,186 @@ __global__ void __launch_bounds__(128) block_pool_kernel(const __nv_bfloat16* sr
   for (int c = tid; c < D; c += 128) {
     float s = 0.f;
     for (int g = 0; g < kGroups; ++g) s += part[g][c];
-    out[((int64_t)hx * nb + u) * D + c] = s / (float)(e - a);
+    const float m = s / (float)(e - a);
+    const __nv_bfloat16 h = __float2bfloat16_rn(m);
+    const float r1 = m - __bfloat162float(h);
+    const __nv_bfloat16 md = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(md));
+    __nv_bfloat16* o = out + ((int64_t)hx * 3 * nb + u) * D + c;
+    o[0] = h;
+    o[(int64_t)nb * D] = md;
+    o[(int64_t)2 * nb * D] = lo;
   }
 }
 
-// Packed lower triangle (v <= u) of r_uv = Q̄_u . K̄_v for one slot per
-// blockIdx.y; 64 x 64 tiles, 4 x 4 outputs per thread.
+// Packed lower triangle (v <= u) of r_uv = Q̄_u . K̄_v on the tensor cores.
+// One CTA per (128-row tile tu of query blocks, slot), heaviest rows first: it
+// keeps the three Q̄ planes of its rows in shared memory and streams the key
+// tiles tv = 0..tu (three K̄ planes, 64 columns of d per stage, two stages).
+// Per stage, six bf16 products accumulate in fp32 in TMEM, smallest first:
+// lo.hi + mid.mid + hi.lo + mid.hi + hi.mid + hi.hi (the dropped terms are
+// below 2^-24 relative), two accumulators so that the epilogue of one tile
+// overlaps the products of the next.  The epilogue stages 32 x 32 pieces in
+// shared memory so that each warp writes one packed row segment per store.
+//   warp 0: TMA producer, warp 1: MMA issuer (one thread), warps 2-5: epilogue
+constexpr int kScThreads = 192;
+constexpr int kScStages = 2;
+
 template <int D>
-__global__ void __launch_bounds__(256) block_scores_kernel(const float* qbar, const float* kbar,
-                                                           const __grid_constant__ HeadMap kv_of_slot, int nb,
-                                                           float* scores) {
-  constexpr int kC = 32;  // reduction columns staged per step
-  __shared__ __align__(16) float sq[kC][64 + 4];
-  __shared__ __align__(16) float sk[kC][64 + 4];
-  // tile (tu, tv) with tv <= tu from the linear tile id
-  const int lin = blockIdx.x;
-  int tu = (int)((sqrtf(8.f * lin + 1.f) - 1.f) * 0.5f);
-  while ((tu + 1) * (tu + 2) / 2 <= lin) ++tu;
-  while (tu * (tu + 1) / 2 > lin) --tu;
-  const int tv = lin - tu * (tu + 1) / 2;
-  const int slot = blockIdx.y;
-  const float* qb = qbar + (int64_t)slot * nb * D;
-  const float* kb = kbar + (int64_t)kv_of_slot.row_head[slot] * nb * D;
-  const int tid = threadIdx.x;
-  const int tx = tid % 16, ty = tid / 16;
-  float acc[4][4] = {};
-  for (int c0 = 0; c0 < D; c0 += kC) {
-    for (int idx = tid; idx < 64 * kC; idx += 256) {
-      const int r = idx / kC, c = idx % kC;
-      const int u = tu * 64 + r, v = tv * 64 + r;
-      sq[c][r] = u < nb ? qb[(int64_t)u * D + c0 + c] : 0.f;
-      sk[c][r] = v < nb ? kb[(int64_t)v * D + c0 + c] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int c = 0; c < kC; ++c) {
-      const float4 a = *reinterpret_cast<const float4*>(&sq[c][ty * 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&sk[c][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-    __syncthreads();
+struct ScLayout {
+  static constexpr int kChunk = 128 * 64 * 2;              // 128 rows x 64 columns of bf16
+  static constexpr int kQ = 0;                             // [plane][D / 64 chunks]
+  static constexpr int kK = kQ + 3 * (D / 64) * kChunk;    // [stage][plane]
+  static constexpr int kStage = kK + kScStages * 3 * kChunk;
+  static constexpr int kBars = kStage + 4 * 32 * 33 * 4;   // epilogue staging, one 32 x 33 per warp
+  static constexpr int kMisc = kBars + 16 * 8;
+  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kAlloc = kTotal + 1024;
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+struct ScArgs {
+  int nb, T, cs;        // query blocks, row tiles, slots in this launch
+  int slot_base;        // first slot of this launch (for the score rows)
+  float* scores;        // packed triangles of every slot
+  int* err;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kScThreads, 1)
+    block_scores_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                        const __grid_constant__ HeadMap kv_of_slot, const ScArgs A) {
+  using Ly = ScLayout<D>;
+  constexpr int kC = D / 64;  // stages per key tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::kBars);
+  uint64_t* qfull = bars;
+  uint64_t* kfull = bars + 1;                  // [kScStages]
+  uint64_t* kempty = kfull + kScStages;        // [kScStages]
+  uint64_t* afull = kempty + kScStages;        // [2]
+  uint64_t* aempty = afull + 2;                // [2]
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + Ly::kMisc);  // [0] TMEM base, [1] abort
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tu = A.T - 1 - (int)(blockIdx.x / A.cs);
+  const int sl = (int)(blockIdx.x % A.cs);
+  const int kvp = kv_of_slot.row_head[sl];
+  const int ntile = tu + 1;  // key tiles tv = 0 .. tu
+  if (warp == 0) {
+    tmem_alloc(const_cast<uint32_t*>(&misc[0]), 256);
+    tmem_relinquish();
   }
-  float* out = scores + (int64_t)slot * ((int64_t)nb * (nb + 1) / 2);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int u = tu * 64 + ty * 4 + i;
-    if (u >= nb) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int v = tv * 64 + tx * 4 + j;
-      if (v <= u) out[(int64_t)u * (u + 1) / 2 + v] = acc[i][j];
+  if (threadIdx.x == 32) {
+    mbar_init(qfull, 1);
+    for (int x = 0; x < kScStages; ++x) {
+      mbar_init(&kfull[x], 1);
+      mbar_init(&kempty[x], 1);
     }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&afull[x], 1);
+      mbar_init(&aempty[x], 4);
+    }
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      mbar_arrive_expect_tx(qfull, 3 * kC * Ly::kChunk);
+      for (int p = 0; p < 3; ++p)
+        for (int c = 0; c < kC; ++c)
+          tma_load_3d(sm + Ly::kQ + (p * kC + c) * Ly::kChunk, &tq, qfull, 64 * c, 128 * tu, 3 * sl + p);
+      bool ok = true;
+      for (int it = 0; it < ntile * kC && ok; ++it) {
+        const int st = it % kScStages;
+        if (misc[1] || !mbar_wait(&kempty[st], ((it / kScStages) & 1) ^ 1)) { ok = false; break; }
+        const int tv = it / kC, c = it % kC;
+        mbar_arrive_expect_tx(&kfull[st], 3 * Ly::kChunk);
+        for (int p = 0; p < 3; ++p)
+          tma_load_3d(sm + Ly::kK + (st * 3 + p) * Ly::kChunk, &tk, &kfull[st], 64 * c, 128 * tv, 3 * kvp + p);
+      }
+      if (!ok) { misc[1] = 1; set_err(A.err, kErrTimeout); }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id = idesc_bf16_f32(128, 128, false, false);
+      const uint64_t dq = sdesc_sw128(smem_u32(sm + Ly::kQ), 16, 1024);
+      const uint64_t dk = sdesc_sw128(smem_u32(sm + Ly::kK), 16, 1024);
+      constexpr uint64_t kCh = Ly::kChunk >> 4;  // descriptor step of one chunk
+      // (Q plane, K plane) of the six products, smallest terms first
+      const int pa[6] = {2, 1, 0, 1, 0, 0}, pb[6] = {0, 1, 2, 0, 1, 0};
+      bool ok = mbar_wait(qfull, 0);
+      if (ok) tc_fence_after();
+      int it = 0;
+      for (int t = 0; t < ntile && ok; ++t) {
+        const int buf = t & 1;
+        if (misc[1] || !mbar_wait(&aempty[buf], ((t >> 1) & 1) ^ 1)) { ok = false; break; }
+        tc_fence_after();
+        for (int c = 0; c < kC; ++c, ++it) {
+          const int st = it % kScStages;
+          if (!mbar_wait(&kfull[st], (it / kScStages) & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int x = 0; x < 6; ++x) {
+              const uint64_t a = dq + (uint64_t)(pa[x] * kC + c) * kCh + 2 * kk;
+              const uint64_t b = dk + (uint64_t)(st * 3 + pb[x]) * kCh + 2 * kk;
+              mma_bf16_ss(tmem + 128 * buf, a, b, id, (c > 0 || kk > 0 || x > 0) ? 1u : 0u);
+            }
+          mma_commit(&kempty[st]);
+        }
+        if (ok) mma_commit(&afull[buf]);
+      }
+      if (!ok) { misc[1] = 1; set_err(A.err, kErrTimeout); }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lanes 32q ..
+    float* st = reinterpret_cast<float*>(sm + Ly::kStage) + (warp - 2) * 32 * 33;
+    const int64_t tri_base = (int64_t)(A.slot_base + sl) * ((int64_t)A.nb * (A.nb + 1) / 2);
+    bool ok = true;
+    for (int t = 0; t < ntile; ++t) {
+      const int buf = t & 1;
+      if (misc[1] || !mbar_wait(&afull[buf], (t >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      const int tv = t;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 128 * buf + 32 * cc, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) st[lane * 33 + x] = __uint_as_float(v[x]);
+        __syncwarp();
+        const int vcol = 128 * tv + 32 * cc + lane;
+#pragma unroll 4
+        for (int k = 0; k < 32; ++k) {
+          const int u = 128 * tu + 32 * q + k;
+          if (u < A.nb && vcol <= u) A.scores[tri_base + (int64_t)u * (u + 1) / 2 + vcol] = st[k * 33 + lane];
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aempty[buf]);
+    }
+    if (!ok) { misc[1] = 1; set_err(A.err, kErrTimeout); }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -302,8 +436,8 @@ BSPlan plan_bs(const msa_shape& s, const int32_t* heads, int32_t n_heads) {
     P.nkv = P.slots;  // upper bound
   }
   size_t off = 0;
-  P.off_q = off; off = al256(off + sizeof(float) * (size_t)P.slots * P.nb * s.d_h);
-  P.off_k = off; off = al256(off + sizeof(float) * (size_t)P.nkv * P.nb * s.d_h);
+  P.off_q = off; off = al256(off + sizeof(__nv_bfloat16) * 3 * (size_t)P.slots * P.nb * s.d_h);
+  P.off_k = off; off = al256(off + sizeof(__nv_bfloat16) * 3 * (size_t)P.nkv * P.nb * s.d_h);
   P.off_s = off; off = al256(off + sizeof(float) * (size_t)P.slots * ((size_t)P.nb * (P.nb + 1) / 2));
   P.total = off + 256;
   return P;
@@ -312,8 +446,8 @@ BSPlan plan_bs(const msa_shape& s, const int32_t* heads, int32_t n_heads) {
 template <int D>
 msa_status run_bs(const msa_shape& s, const void* q, const void* k, const BSPlan& P, int topk, int32_t* J,
                   int32_t* cnt, uint8_t* w, cudaStream_t stream) {
-  float* qbar = reinterpret_cast<float*>(w + P.off_q);
-  float* kbar = reinterpret_cast<float*>(w + P.off_k);
+  __nv_bfloat16* qbar = reinterpret_cast<__nv_bfloat16*>(w + P.off_q);  // [slots, 3, nb, D]
+  __nv_bfloat16* kbar = reinterpret_cast<__nv_bfloat16*>(w + P.off_k);  // [nkv, 3, nb, D]
   float* sc = reinterpret_cast<float*>(w + P.off_s);
   for (int base = 0; base < P.slots; base += kMaxSlots) {
     const int cntq = P.slots - base < kMaxSlots ? P.slots - base : kMaxSlots;
@@ -321,7 +455,7 @@ msa_status run_bs(const msa_shape& s, const void* q, const void* k, const BSPlan
     memset(&m, 0, sizeof(m));
     for (int x = 0; x < cntq; ++x) m.row_head[x] = P.q_rows[(size_t)(base + x)];
     block_pool_kernel<D><<<dim3(P.nb, cntq), 128, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(q), s.n, P.nb,
-                                                                m, qbar + (int64_t)base * P.nb * D);
+                                                                m, qbar + (int64_t)base * 3 * P.nb * D);
     note_launch();
     if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   }
@@ -331,19 +465,32 @@ msa_status run_bs(const msa_shape& s, const void* q, const void* k, const BSPlan
     memset(&m, 0, sizeof(m));
     for (int x = 0; x < cntk; ++x) m.row_head[x] = P.kv_rows[(size_t)(base + x)];
     block_pool_kernel<D><<<dim3(P.nb, cntk), 128, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(k), s.n, P.nb,
-                                                                m, kbar + (int64_t)base * P.nb * D);
+                                                                m, kbar + (int64_t)base * 3 * P.nb * D);
     note_launch();
     if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   }
-  const int T = (P.nb + 63) / 64;
-  const int tiles = T * (T + 1) / 2;
+  // scores on the tensor cores: pooled planes viewed as [planes, nb, D] with 128-row boxes
+  CUtensorMap tkm;
+  if (!make_bf16_map(&tkm, kbar, (int64_t)3 * P.nkv, P.nb, D, 128)) return MSA_ERR_CUDA;
+  auto kern = block_scores_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ScLayout<D>::kAlloc) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  ScArgs sa;
+  sa.nb = P.nb;
+  sa.T = (P.nb + 127) / 128;
+  sa.scores = sc;
+  sa.err = device_error_word();
+  if (!sa.err) return MSA_ERR_CUDA;
   for (int base = 0; base < P.slots; base += kMaxSlots) {
     const int cs = P.slots - base < kMaxSlots ? P.slots - base : kMaxSlots;
     HeadMap m;
     memset(&m, 0, sizeof(m));
     for (int x = 0; x < cs; ++x) m.row_head[x] = P.kv_of_slot[(size_t)(base + x)];
-    block_scores_kernel<D><<<dim3(tiles, cs), 256, 0, stream>>>(
-        qbar + (int64_t)base * P.nb * D, kbar, m, P.nb, sc + (int64_t)base * ((int64_t)P.nb * (P.nb + 1) / 2));
+    CUtensorMap tqm;
+    if (!make_bf16_map(&tqm, qbar + (int64_t)base * 3 * P.nb * D, (int64_t)3 * cs, P.nb, D, 128)) return MSA_ERR_CUDA;
+    sa.cs = cs;
+    sa.slot_base = base;
+    kern<<<(unsigned)(sa.T * cs), kScThreads, ScLayout<D>::kAlloc, stream>>>(tqm, tkm, m, sa);
     note_launch();
     if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   }

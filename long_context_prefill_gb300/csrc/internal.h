@@ -79,7 +79,7 @@ struct AttnArgs {
 
 // TMA views of the attention operands as [BH, n, d]: Q, K, V with boxes of
 // 64 columns x 64 rows, and K, V again with 64 x 16 boxes (16-key segments).
-struct alignas(64) AttnMaps {
+struct AttnMaps {
   CUtensorMap q, k, v, k16, v16;
 };
 
