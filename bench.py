@@ -282,6 +282,7 @@ def main():
     ap.add_argument("--workloads", default=",".join(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense-baseline and cold-L2 measurements")
     ap.add_argument("--n", type=int, default=None,
                     help="override the sequence length (scaled-down runs for profiling; not a headline number)")
     args = ap.parse_args()
@@ -353,7 +354,8 @@ def main():
             "index_bytes": r.index_bytes,
             "density": round(float(r.edges.sum()) / (r.sh["Hq"] * r.sh["n"] * (r.sh["n"] + 1) / 2), 4),
         }
-    dense_and_cold(runs, msa, per_layer, stream)
+    if not args.no_dense:
+        dense_and_cold(runs, msa, per_layer, stream)
     pk, pk_src = peaks()
     achieved = attn_flops_sum / (attn_ms_sum * 1e-3) / 1e12
     peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
