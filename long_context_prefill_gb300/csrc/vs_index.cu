@@ -37,8 +37,16 @@ namespace {
 
 constexpr int kPackMaxHeads = 8;
 constexpr int kRows = 256;  // query rows per pack (Q tile in shared memory)
-constexpr int kProxyThreads = 320;  // warps 0-7 epilogue, 8 producer, 9 MMA
-constexpr int kProdWarp = 8, kMmaWarpP = 9;
+// Warps 0..E-1 epilogue, E producer, E+1 MMA.  The scores pass with at most
+// 64 rows per head runs 16 epilogue warps (one per 32 keys x 64 columns), the
+// other passes 8 (one per 32 keys x 128 columns).
+template <int MODE, int LP>
+struct ProxyWarps {
+  static constexpr int kEpi = (MODE == 2 && LP <= 64) ? 16 : 8;
+  static constexpr int kProd = kEpi, kMma = kEpi + 1;
+  static constexpr int kThreads = 32 * (kEpi + 2);
+  static constexpr int kCols = 256 / (kEpi / 4);  // TMEM columns (proxy rows) per epilogue warp
+};
 constexpr int kKStages = 3;
 
 struct Pack {
@@ -112,7 +120,7 @@ __device__ void load_rows(uint8_t* sQ, const ProxyArgs& A, const Pack& P) {
 // MODE 1: statistics pass (S = Q K^T, lane = row).  MODE 2: scores pass
 // (S^T = K Q^T, lane = key).  LP: rows per head (32, 64 or 128).
 template <int D, int MODE, int LP>
-__global__ void __launch_bounds__(kProxyThreads, 1)
+__global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
     proxy_kernel(const __grid_constant__ CUtensorMap tk, const ProxyArgs A, const __grid_constant__ PackTable PT) {
   using Ly = PLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -142,14 +150,15 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
     tmem_alloc(const_cast<uint32_t*>(&misc[0]), 512);
     tmem_relinquish();
   }
-  if (threadIdx.x == 32 * kMmaWarpP) {
+  using PW = ProxyWarps<MODE, LP>;
+  if (threadIdx.x == 32 * PW::kMma) {
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&kfull[s], 1);
       mbar_init(&kempty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sfull[s], 1);
-      mbar_init(&sempty[s], 8);
+      mbar_init(&sempty[s], PW::kEpi);
     }
     misc[2] = 0;
     fence_mbar_init();
@@ -162,7 +171,7 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
-  if (warp == kProdWarp) {
+  if (warp == PW::kProd) {
     if (lane == 0 && T > 0) {
       tma_prefetch_desc(&tk);
       bool ok = true;
@@ -178,7 +187,7 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
       if (!ok) { misc[2] = 1; set_err(A.err, kErrTimeout); }
     }
     __syncwarp();
-  } else if (warp == kMmaWarpP) {
+  } else if (warp == PW::kMma) {
     if (lane == 0 && T > 0) {
       bool ok = true;
       const uint32_t q0 = smem_u32(sQ);
@@ -273,9 +282,9 @@ __global__ void __launch_bounds__(kProxyThreads, 1)
       // Sums are kept as (max, sum of 2^(x - max)) pairs over log2
       // probabilities x = log2 Ã, so scores far below fp32's range still
       // rank correctly; outputs are log2 of the sums.
-      constexpr int HPH = 128 / LP;   // heads per column half
+      constexpr int HPH = PW::kCols / LP;  // heads per epilogue warp
       constexpr int LB = LP / 32;     // 32-row chunks per head
-      const int ch = warp >> 2;       // column half: rows 128ch .. 128ch+127
+      const int ch = warp >> 2;            // column group: rows kCols ch .. kCols (ch + 1) - 1
       float col_log[HPH];
       float bin_log[HPH][LB + 1];
       for (int j = 0; j < T; ++j) {
@@ -849,7 +858,7 @@ msa_status launch_proxy(const CUtensorMap& tk, const ProxyArgs& a, const std::ve
     aa.part = a.part + base * nchunks * kRows;
     aa.lse2 = a.lse2 + base * kRows;
     aa.nchunks = nchunks;
-    kern<<<(unsigned)(cnt * nchunks), kProxyThreads, smem, stream>>>(tk, aa, pt);
+    kern<<<(unsigned)(cnt * nchunks), ProxyWarps<MODE, LP>::kThreads, smem, stream>>>(tk, aa, pt);
     note_launch();
     if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   }
