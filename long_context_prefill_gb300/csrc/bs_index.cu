@@ -309,7 +309,7 @@ __device__ __forceinline__ void topk_row_regs(const float* row, int u, int k1, i
 // One warp per (slot, query block u): J_u = {u} ∪ top_{k-1} of row u.  Rows
 // longer than 2048 candidates use a radix select over a per-warp histogram in
 // dynamic shared memory (kTopkWarps x 2048 ints, given only when nb > 2048).
-__global__ void __launch_bounds__(32 * kTopkWarps) block_topk_kernel(const float* scores, int nb, int topk,
+__global__ void __launch_bounds__(32 * kTopkWarps, 4) block_topk_kernel(const float* scores, int nb, int topk,
                                                                       int nslots, int32_t* J, int32_t* cnt) {
   extern __shared__ int hist_all[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
