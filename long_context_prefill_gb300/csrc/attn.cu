@@ -247,6 +247,7 @@ struct BlockSeg {
   const int32_t* L[4];
   int cnt[4], u[4], p[4];
   int last;
+  int pend[4], pendb[4];  // per class (1: sub-item 0 only, 2: sub-item 1 only, 3: both): a block waiting for a partner
   __device__ void init(const Unit& U, const Geo& G, const AttnArgs& a, int lane, int* sblk) {
     bool fits = true;
     for (int hh = 0; hh < 4; ++hh) {
@@ -271,6 +272,7 @@ struct BlockSeg {
       __syncwarp();
     }
     last = -1;
+    for (int c = 0; c < 4; ++c) pend[c] = pendb[c] = -1;
   }
   // Next union block and the halves that hold it; bits = -1 flags a list
   // that is not strictly ascending.
@@ -537,26 +539,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lane 0 takes up to two segments of the union
         int sg[2] = {0, 0}, rl[2][2] = {{0, 0}, {0, 0}}, bits[2] = {0, 0};
         int got = 0;
-        if (lane == 0) {
+        if (lane == 0 && U.pattern == kUnitAshape) {
           for (; got < 2; ++got) {
-            int s = 0, r2[2] = {0, 0}, b = 0;
-            bool has;
-            if (U.pattern == kUnitAshape) {
-              has = as.next(s, r2);
-              if (has) b = (r2[0] ? 3 : 0) | (r2[1] ? 12 : 0);
-            } else {
-              has = bs.next(s, b);
-              if (has && b < 0) { b = 0; set_error(A.err, kErrIndex); }
-              if (has)
-                for (int hh = 0; hh < 4; ++hh)  // a block must be causal for each half that keeps it
-                  if (((b >> hh) & 1) && (s < 0 || s > bs.u[hh])) { b &= ~(1 << hh); set_error(A.err, kErrIndex); }
-              if (has && (s < 0 || 64 * s >= n)) { s = 0; b = 0; }
-            }
-            if (!has) break;
+            int s = 0, r2[2] = {0, 0};
+            if (!as.next(s, r2)) break;
             sg[got] = s;
             rl[0][got] = r2[0];
             rl[1][got] = r2[1];
-            bits[got] = b;
+            bits[got] = (r2[0] ? 3 : 0) | (r2[1] ? 12 : 0);
+          }
+        } else if (lane == 0) {
+          // Block-Sparse: the two blocks of a tile are taken from the same class
+          // (kept by sub-item 0 only, by sub-item 1 only, or by both), so that a
+          // sub-item skips the tiles it does not attend; a block waits in
+          // pend[class] for its partner, and the leftovers close the item.
+          for (;;) {
+            int s = 0, b = 0;
+            const bool has = bs.next(s, b);
+            if (!has) {
+              for (int c = 1; c < 4 && got < 2; ++c)
+                if (bs.pend[c] >= 0) { sg[got] = bs.pend[c]; bits[got] = bs.pendb[c]; bs.pend[c] = -1; ++got; }
+              break;
+            }
+            if (b < 0) { b = 0; set_error(A.err, kErrIndex); }
+            for (int hh = 0; hh < 4; ++hh)  // a block must be causal for each half that keeps it
+              if (((b >> hh) & 1) && (s < 0 || s > bs.u[hh])) { b &= ~(1 << hh); set_error(A.err, kErrIndex); }
+            if (s < 0 || 64 * s >= n) b = 0;
+            const int c = ((b & 3) ? 1 : 0) | ((b & 12) ? 2 : 0);
+            if (c == 0) continue;  // kept by no half
+            if (bs.pend[c] >= 0) {
+              sg[0] = bs.pend[c]; bits[0] = bs.pendb[c];
+              sg[1] = s; bits[1] = b;
+              got = 2;
+              bs.pend[c] = -1;
+              break;
+            }
+            bs.pend[c] = s;
+            bs.pendb[c] = b;
           }
         }
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
