@@ -210,6 +210,29 @@ MSA_API msa_status msa_prefill_layer(const msa_shape* shape, const void* q, cons
                              const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
                              size_t ws_bytes, void* stream);
 
+/* Varlen prefill: a batch of n_seqs sequences of different lengths, packed
+ * without padding (cost-model page §2.2: a varlen kernel takes a cumulative
+ * length array, processes only real tokens, and keeps every sample's windows
+ * and tiles inside its own segment).  cu_seqlens: host array of n_seqs + 1
+ * non-decreasing token offsets, cu_seqlens[0] = 0; sequence s has
+ * n_s = cu_seqlens[s+1] - cu_seqlens[s] tokens (0 allowed: skipped).  Layout:
+ * the sequences' tensors back to back, sequence s as one [H, n_s, d_h] block
+ * starting at element H * cu_seqlens[s] * d_h (q, o: H = Hq; k, v: H = Hkv);
+ * lse likewise as [Hq, n_s] blocks at Hq * cu_seqlens[s]; edges: [n_seqs, Hq]
+ * counters (ADDED to).  shape gives Hq, Hkv, d_h and scale for every sequence
+ * (its B and n are ignored).  Every sequence runs as msa_prefill_layer with
+ * B = 1 and n = n_s on its own segment, in order on `stream`, reusing `ws`:
+ * its own online indices, its own attention, no key of another sequence.
+ * Requires ws_bytes >= msa_layer_varlen_workspace(...).  Errors: invalid
+ * cu_seqlens -> MSA_ERR_INVALID_ARG before anything is launched; otherwise
+ * the first failing sequence's status (earlier sequences have been queued). */
+MSA_API size_t msa_layer_varlen_workspace(const msa_shape* shape, const msa_head_cfg* table,
+                                          const int32_t* cu_seqlens, int32_t n_seqs);
+MSA_API msa_status msa_prefill_layer_varlen(const msa_shape* shape, const int32_t* cu_seqlens, int32_t n_seqs,
+                                            const void* q, const void* k, const void* v, const msa_head_cfg* table,
+                                            void* o, float* lse, int64_t* edges, void* ws, size_t ws_bytes,
+                                            void* stream);
+
 /* The two halves of msa_prefill_layer, in order (the time decomposition
  * T = T_index + T_sparse of the MInference page eq.(13)): msa_layer_index
  * builds every Vertical-Slash and Block-Sparse index of the table into `ws`;

@@ -29,7 +29,7 @@ EXPORTS = ("msa_status_string", "msa_vs_index_workspace", "msa_block_index_works
            "msa_build_vs_index", "msa_build_block_index", "msa_attn_ashape", "msa_attn_vs", "msa_attn_block",
            "msa_prefill_layer", "msa_layer_index", "msa_layer_attend", "msa_kernel_launches", "msa_layer_indices",
            "msa_vs_expand", "msa_poll_device_status", "msa_build_block_index_static",
-           "msa_check_wait_timeout", "msa_attn_dense")
+           "msa_check_wait_timeout", "msa_attn_dense", "msa_layer_varlen_workspace", "msa_prefill_layer_varlen")
 
 
 class MsaError(RuntimeError):
@@ -105,6 +105,10 @@ def load(path: str = LIB_PATH):
             lib.msa_attn_dense.argtypes = [P, P, P, P, P, i32, P, P, P, P]
             lib.msa_check_wait_timeout.restype = st
             lib.msa_check_wait_timeout.argtypes = [i32, P]
+            lib.msa_layer_varlen_workspace.restype = sz
+            lib.msa_layer_varlen_workspace.argtypes = [P, P, P, i32]
+            lib.msa_prefill_layer_varlen.restype = st
+            lib.msa_prefill_layer_varlen.argtypes = [P, P, i32, P, P, P, P, P, P, P, P, sz, P]
             lib.msa_build_block_index_static.restype = st
             lib.msa_build_block_index_static.argtypes = [P, P, P, P, i32, i32, i32, P, P, P]
             _lib = lib
@@ -379,6 +383,41 @@ class Layer:
             blk = _view_i32(bi.value, B * len(nbs) * nb * topk).view(B, len(nbs), nb, topk)
             cnt = _view_i32(bc.value, B * len(nbs) * nb).view(B, len(nbs), nb)
         return vs, blk, cnt
+
+
+# ----------------------------------------------------------------- varlen
+def pack_varlen(seqs) -> torch.Tensor:
+    """Pack per-sequence [H, n_s, d] tensors back to back (the varlen layout)."""
+    return torch.cat([x.contiguous().reshape(-1) for x in seqs])
+
+
+def unpack_varlen(flat: torch.Tensor, H: int, cu_seqlens, d: int):
+    """Split a packed varlen buffer into per-sequence [H, n_s, d] views."""
+    out = []
+    for s in range(len(cu_seqlens) - 1):
+        a, b = int(cu_seqlens[s]), int(cu_seqlens[s + 1])
+        out.append(flat[H * a * d:H * b * d].view(H, b - a, d))
+    return out
+
+
+def prefill_layer_varlen(q, k, v, table, cu_seqlens, Hq, Hkv, d, o=None, lse=None, edges=None, scale=None,
+                         ws=None, stream=None):
+    """msa_prefill_layer_varlen on packed buffers (see pack_varlen); returns o."""
+    lib = load()
+    cu = (ctypes.c_int32 * len(cu_seqlens))(*[int(x) for x in cu_seqlens])
+    shape = Shape(1, Hq, Hkv, max(1, max(int(cu_seqlens[s + 1]) - int(cu_seqlens[s]) for s in range(len(cu_seqlens) - 1))),
+                  d, float(scale) if scale else 0.0)
+    tarr = table_array(table)
+    need = int(lib.msa_layer_varlen_workspace(ctypes.byref(shape), tarr, cu, len(cu_seqlens) - 1))
+    if need == 0:
+        raise MsaError(MSA_ERR_INVALID_ARG, "msa_layer_varlen_workspace")
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q) if o is None else o
+    _check(lib.msa_prefill_layer_varlen(ctypes.byref(shape), cu, len(cu_seqlens) - 1, _ptr(q), _ptr(k), _ptr(v), tarr,
+                                        _ptr(o), _ptr(lse), _ptr(edges), _ptr(ws), ws.numel(), _stream(stream)),
+           "msa_prefill_layer_varlen")
+    return o
 
 
 def kernel_launches() -> int:

@@ -276,6 +276,63 @@ msa_status msa_prefill_layer(const msa_shape* shape, const void* q, const void* 
   return layer_attend(*shape, q, k, v, table, o, lse, edges, W, strm);
 }
 
+// ------------------------------------------------------------------ varlen
+// Sequence s of a varlen batch: tokens [cu[s], cu[s+1]); its tensors are the
+// s-th [H, n_s, d_h] segment of the packed buffers.  Each sequence is an
+// ordinary B = 1 layer on its own segment: its own online indices, its own
+// attention, so no index, window or tile reaches another sequence's tokens.
+static msa_status check_cu_seqlens(const int32_t* cu, int32_t n_seqs) {
+  if (!cu || n_seqs < 1 || cu[0] != 0) return MSA_ERR_INVALID_ARG;
+  for (int32_t x = 0; x < n_seqs; ++x) {
+    if (cu[x + 1] < cu[x]) return MSA_ERR_INVALID_ARG;
+    if (cu[x + 1] - cu[x] > (1 << 28)) return MSA_ERR_UNSUPPORTED;
+  }
+  return MSA_OK;
+}
+
+size_t msa_layer_varlen_workspace(const msa_shape* shape, const msa_head_cfg* table, const int32_t* cu_seqlens,
+                                  int32_t n_seqs) {
+  if (!shape || !table || check_cu_seqlens(cu_seqlens, n_seqs) != MSA_OK) return 0;
+  size_t need = 256;
+  for (int32_t x = 0; x < n_seqs; ++x) {
+    const int32_t len = cu_seqlens[x + 1] - cu_seqlens[x];
+    if (len == 0) continue;
+    msa_shape ss = *shape;
+    ss.B = 1;
+    ss.n = len;
+    const size_t w = msa_layer_workspace(&ss, table);
+    if (w == 0) return 0;
+    need = w > need ? w : need;
+  }
+  return need;
+}
+
+msa_status msa_prefill_layer_varlen(const msa_shape* shape, const int32_t* cu_seqlens, int32_t n_seqs,
+                                    const void* q, const void* k, const void* v, const msa_head_cfg* table, void* o,
+                                    float* lse, int64_t* edges, void* ws, size_t ws_bytes, void* stream) {
+  if (!shape || !q || !k || !v || !o || !table) return MSA_ERR_INVALID_ARG;
+  msa_status st = check_cu_seqlens(cu_seqlens, n_seqs);
+  if (st != MSA_OK) return st;
+  if (ws_bytes < msa_layer_varlen_workspace(shape, table, cu_seqlens, n_seqs)) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  const int64_t hq = shape->Hq, hkv = shape->Hkv, d = shape->d_h;
+  for (int32_t x = 0; x < n_seqs; ++x) {
+    const int32_t len = cu_seqlens[x + 1] - cu_seqlens[x];
+    if (len == 0) continue;
+    msa_shape ss = *shape;
+    ss.B = 1;
+    ss.n = len;
+    const int64_t t0 = cu_seqlens[x];
+    const char* qb = static_cast<const char*>(q) + hq * t0 * d * 2;
+    const char* kb = static_cast<const char*>(k) + hkv * t0 * d * 2;
+    const char* vb = static_cast<const char*>(v) + hkv * t0 * d * 2;
+    char* ob = static_cast<char*>(o) + hq * t0 * d * 2;
+    if ((st = msa_prefill_layer(&ss, qb, kb, vb, table, ob, lse ? lse + hq * t0 : nullptr,
+                                edges ? edges + (int64_t)x * hq : nullptr, ws, ws_bytes, stream)) != MSA_OK)
+      return st;
+  }
+  return MSA_OK;
+}
+
 uint64_t msa_kernel_launches(void) { return launch_count(); }
 
 msa_status msa_layer_indices(const msa_shape* shape, const msa_head_cfg* table, void* ws, msa_vs_index* vs,
