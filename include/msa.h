@@ -210,6 +210,32 @@ MSA_API msa_status msa_prefill_layer(const msa_shape* shape, const void* q, cons
                              const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
                              size_t ws_bytes, void* stream);
 
+/* Merge of two attention results of the same query rows over disjoint key
+ * sets (MInference page §3.2, eq.(7)-(8)): lse = log(e^{lse_a} + e^{lse_b}),
+ * o = e^{lse_a - lse} o_a + e^{lse_b - lse} o_b per row, so a pattern computed
+ * as separate key sets (verticals apart from slashes, chunks of the keys)
+ * recombines into the single-pass result.  rows: number of query rows;
+ * o_a, o_b, o: [rows, d_h] bf16 (o may alias o_a or o_b); lse_a, lse_b: [rows]
+ * fp32 natural-log LSE as the attention calls return it (-inf: empty part);
+ * lse: [rows] fp32 or NULL, must not alias lse_a / lse_b.  Errors:
+ * MSA_ERR_INVALID_ARG (null or misaligned pointers, rows < 0, aliased lse),
+ * MSA_ERR_UNSUPPORTED (d_h not 64/128). */
+MSA_API msa_status msa_merge_attention(int64_t rows, int32_t d_h, const void* o_a, const float* lse_a,
+                                       const void* o_b, const float* lse_b, void* o, float* lse, void* stream);
+
+/* Chunked prefill (MInference page §5.2: a scheduler may cut a long prefill
+ * into chunks so that it does not block short requests): msa_layer_attend
+ * restricted to the query rows [row_begin, row_end) of every head; rows
+ * outside are not written.  With the indices built once by msa_layer_index
+ * over the whole sequence, the chunks, in any order, reproduce
+ * msa_layer_attend's output and LSE bit for bit (each row meets the same
+ * tiles in the same order); edges count only the chunk's rows.
+ * row_begin: a multiple of 256; row_end: a multiple of 256 or n;
+ * 0 <= row_begin < row_end <= n, else MSA_ERR_INVALID_ARG. */
+MSA_API msa_status msa_layer_attend_rows(const msa_shape* shape, const void* q, const void* k, const void* v,
+                                         const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
+                                         size_t ws_bytes, int32_t row_begin, int32_t row_end, void* stream);
+
 /* Varlen prefill: a batch of n_seqs sequences of different lengths, packed
  * without padding (cost-model page §2.2: a varlen kernel takes a cumulative
  * length array, processes only real tokens, and keeps every sample's windows

@@ -29,7 +29,8 @@ EXPORTS = ("msa_status_string", "msa_vs_index_workspace", "msa_block_index_works
            "msa_build_vs_index", "msa_build_block_index", "msa_attn_ashape", "msa_attn_vs", "msa_attn_block",
            "msa_prefill_layer", "msa_layer_index", "msa_layer_attend", "msa_kernel_launches", "msa_layer_indices",
            "msa_vs_expand", "msa_poll_device_status", "msa_build_block_index_static",
-           "msa_check_wait_timeout", "msa_attn_dense", "msa_layer_varlen_workspace", "msa_prefill_layer_varlen")
+           "msa_check_wait_timeout", "msa_attn_dense", "msa_layer_varlen_workspace", "msa_prefill_layer_varlen",
+           "msa_layer_attend_rows", "msa_merge_attention")
 
 
 class MsaError(RuntimeError):
@@ -109,6 +110,10 @@ def load(path: str = LIB_PATH):
             lib.msa_layer_varlen_workspace.argtypes = [P, P, P, i32]
             lib.msa_prefill_layer_varlen.restype = st
             lib.msa_prefill_layer_varlen.argtypes = [P, P, i32, P, P, P, P, P, P, P, P, sz, P]
+            lib.msa_layer_attend_rows.restype = st
+            lib.msa_layer_attend_rows.argtypes = [P, P, P, P, P, P, P, P, P, sz, i32, i32, P]
+            lib.msa_merge_attention.restype = st
+            lib.msa_merge_attention.argtypes = [ctypes.c_int64, i32, P, P, P, P, P, P, P]
             lib.msa_build_block_index_static.restype = st
             lib.msa_build_block_index_static.argtypes = [P, P, P, P, i32, i32, i32, P, P, P]
             _lib = lib
@@ -363,6 +368,13 @@ class Layer:
                "msa_layer_attend")
         return o
 
+    def attend_rows(self, q, k, v, o, row_begin, row_end, lse=None, edges=None, stream=None):
+        """Chunked T_sparse: the attention of query rows [row_begin, row_end) only (indices from index())."""
+        _check(load().msa_layer_attend_rows(ctypes.byref(self.shape), _ptr(q), _ptr(k), _ptr(v), self.tarr, _ptr(o),
+                                            _ptr(lse), _ptr(edges), _ptr(self.ws), self.ws_bytes, int(row_begin),
+                                            int(row_end), _stream(stream)), "msa_layer_attend_rows")
+        return o
+
     def indices(self):
         """(VSIndex view, block_idx, block_cnt) left in the workspace by the last call."""
         lib = load()
@@ -418,6 +430,17 @@ def prefill_layer_varlen(q, k, v, table, cu_seqlens, Hq, Hkv, d, o=None, lse=Non
                                         _ptr(o), _ptr(lse), _ptr(edges), _ptr(ws), ws.numel(), _stream(stream)),
            "msa_prefill_layer_varlen")
     return o
+
+
+def merge_attention(o_a, lse_a, o_b, lse_b, o=None, lse=None, stream=None):
+    """Combine two attention results over disjoint key sets (msa_merge_attention); returns (o, lse)."""
+    d = o_a.shape[-1]
+    rows = o_a.numel() // d
+    o = torch.empty_like(o_a) if o is None else o
+    lse = torch.empty_like(lse_a) if lse is None else lse
+    _check(load().msa_merge_attention(rows, d, _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o), _ptr(lse),
+                                      _stream(stream)), "msa_merge_attention")
+    return o, lse
 
 
 def kernel_launches() -> int:

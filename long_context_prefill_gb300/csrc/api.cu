@@ -227,7 +227,8 @@ __global__ void wait_timeout_check_kernel(uint64_t limit_ns, int* err) {
 }
 
 msa_status attention(const msa_shape& s, const void* q, const void* k, const void* v, void* o, float* lse,
-                     int64_t* edges, const std::vector<Unit>& units, const AttnArgs& idx, cudaStream_t stream) {
+                     int64_t* edges, const std::vector<Unit>& units, const AttnArgs& idx, cudaStream_t stream,
+                     int32_t row_lo = 0, int32_t row_hi = 0x7FFFFFFF) {
   AttnMaps maps;
   if (!make_bf16_map(&maps.q, q, (int64_t)s.B * s.Hq, s.n, s.d_h, 64) ||
       !make_bf16_map(&maps.k, k, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64) ||
@@ -247,6 +248,8 @@ msa_status attention(const msa_shape& s, const void* q, const void* k, const voi
   a.o = o;
   a.lse = lse;
   a.edges = reinterpret_cast<unsigned long long*>(edges);
+  a.row_lo = row_lo;
+  a.row_hi = row_hi;
   a.err = device_error_word();
   if (!a.err) return MSA_ERR_CUDA;
   return launch_attention(maps, a, units.data(), (int)units.size(), stream);

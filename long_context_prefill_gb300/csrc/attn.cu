@@ -481,6 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Unit& U = UT.u[UT.band[band] + rem % band_units];
   const int n = A.n;
   const Geo G = make_geo(U, t, n, A.nqt);
+  {  // a row range (chunked attention) skips the items outside it; the whole CTA agrees
+    bool in_range = false;
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) in_range = in_range || (G.ex[hh] && G.row0[hh] >= A.row_lo && G.row0[hh] < A.row_hi);
+    if (!in_range) return;
+  }
 
   if (warp == 0) {
     tmem_alloc(const_cast<uint32_t*>(&misc[0]), kTmemCols);

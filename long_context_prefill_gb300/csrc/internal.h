@@ -75,6 +75,7 @@ struct AttnArgs {
   const int32_t* bs_cnt;  // [slots, N_b]
   int32_t bs_topk, bs_nb;
   int* err;
+  int32_t row_lo, row_hi;  // only items whose query rows lie in [row_lo, row_hi) run
 };
 
 // TMA views of the attention operands as [BH, n, d]: Q, K, V with boxes of

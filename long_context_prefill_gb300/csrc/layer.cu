@@ -18,7 +18,8 @@ void vs_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t slot
 void block_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t slots_per_batch,
                  std::vector<Unit>& out);
 msa_status attention(const msa_shape& s, const void* q, const void* k, const void* v, void* o, float* lse,
-                     int64_t* edges, const std::vector<Unit>& units, const AttnArgs& idx, cudaStream_t stream);
+                     int64_t* edges, const std::vector<Unit>& units, const AttnArgs& idx, cudaStream_t stream,
+                     int32_t row_lo = 0, int32_t row_hi = 0x7FFFFFFF);
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -204,7 +205,7 @@ static msa_status layer_index(const msa_shape& s, const void* q, const void* k, 
 
 static msa_status layer_attend(const msa_shape& s, const void* q, const void* k, const void* v,
                                const msa_head_cfg* table, void* o, float* lse, int64_t* edges, const LayerPlan& W,
-                               cudaStream_t strm) {
+                               cudaStream_t strm, int32_t row_lo = 0, int32_t row_hi = 0x7FFFFFFF) {
   std::vector<Unit> units;
   if (!W.a_heads.empty()) {
     std::vector<int32_t> sinks, windows;
@@ -237,7 +238,7 @@ static msa_status layer_attend(const msa_shape& s, const void* q, const void* k,
   a.bs_cnt = W.bs_cnt;
   a.bs_topk = W.bs_heads.empty() ? 1 : W.bs_cfg.topk;
   a.bs_nb = W.nb;
-  return attention(s, q, k, v, o, lse, edges, ordered, a, strm);
+  return attention(s, q, k, v, o, lse, edges, ordered, a, strm, row_lo, row_hi);
 }
 
 }  // namespace msa
@@ -331,6 +332,18 @@ msa_status msa_prefill_layer_varlen(const msa_shape* shape, const int32_t* cu_se
       return st;
   }
   return MSA_OK;
+}
+
+msa_status msa_layer_attend_rows(const msa_shape* shape, const void* q, const void* k, const void* v,
+                                 const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
+                                 size_t ws_bytes, int32_t row_begin, int32_t row_end, void* stream) {
+  if (!shape || !v || !o) return MSA_ERR_INVALID_ARG;
+  if (row_begin < 0 || row_end <= row_begin || row_end > shape->n) return MSA_ERR_INVALID_ARG;
+  if (row_begin % 256 != 0 || (row_end % 256 != 0 && row_end != shape->n)) return MSA_ERR_INVALID_ARG;
+  LayerPlan W;
+  msa_status st = layer_prepare(shape, q, k, v, o, lse, edges, table, ws, ws_bytes, W);
+  if (st != MSA_OK) return st;
+  return layer_attend(*shape, q, k, v, table, o, lse, edges, W, (cudaStream_t)stream, row_begin, row_end);
 }
 
 uint64_t msa_kernel_launches(void) { return launch_count(); }

@@ -227,6 +227,26 @@ def attend(q, k, v, i: int, keyset, scale: float):
     return o, float(lse[0])
 
 
+def merge(o_a, lse_a, o_b, lse_b):
+    """Attention over two disjoint key sets combined into the attention over
+    their union (MInference page §3.2, eq.(7)-(8): each part's softmax state is
+    its LSE; the union's LSE is log(e^lse_a + e^lse_b) and each part's output is
+    weighted by e^(lse_part - lse)).  o_*: [rows, d]; lse_*: [rows]; fp64.
+    Empty parts have lse = -inf."""
+    o_a, o_b = np.asarray(o_a, np.float64), np.asarray(o_b, np.float64)
+    lse_a, lse_b = np.asarray(lse_a, np.float64), np.asarray(lse_b, np.float64)
+    m = np.maximum(lse_a, lse_b)
+    both_empty = np.isneginf(m)
+    ms = np.where(both_empty, 0.0, m)
+    wa = np.where(np.isneginf(lse_a), 0.0, np.exp(lse_a - ms))
+    wb = np.where(np.isneginf(lse_b), 0.0, np.exp(lse_b - ms))
+    s = wa + wb
+    lse = np.where(both_empty, -np.inf, ms + np.log(np.where(both_empty, 1.0, s)))
+    s = np.where(both_empty, 1.0, s)
+    o = (wa / s)[:, None] * o_a + (wb / s)[:, None] * o_b
+    return o, lse
+
+
 def _head(cfg: dict) -> _Head:
     return _Head(int(cfg["pattern"]), int(cfg.get("sink", 0)), int(cfg.get("window", 0)),
                  int(cfg.get("block", 64)), int(cfg.get("topk", 0)))

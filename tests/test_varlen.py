@@ -113,3 +113,39 @@ def test_varlen_ashape_heads_against_oracle(cuda_lib):
         ro, rl, _ = oracle.head_rows(cfg, f32(qs[0, 0]), f32(ks[0, 0]), f32(vs[0, 0]), rows, D ** -0.5)
         lh = lse[HQ * cu[s]:HQ * cu[s + 1]].view(HQ, n)
         compare_rows(f32(outs[s][0])[rows], f32(lh[0])[rows], ro, rl, f"sequence {s} A-shape head")
+
+
+# ----------------------------------------------------------------- chunked rows
+@pytest.mark.parametrize("lo,hi", [(100, 512), (0, 0), (256, 300), (512, 256)])
+def test_attend_rows_rejects_bad_ranges(lib, lo, hi):
+    shape = msa.Shape(1, HQ, HKV, 1000, D, 0.0)
+    st = lib.msa_layer_attend_rows(ctypes.byref(shape), FAKE, FAKE, FAKE, msa.table_array(TABLE), FAKE, None, None,
+                                   FAKE, 1 << 30, lo, hi, None)
+    assert st == msa.MSA_ERR_INVALID_ARG
+
+
+@pytest.mark.gpu
+def test_chunked_rows_reproduce_the_whole_layer(cuda_lib):
+    """Indices built once; the attention run in three row chunks (out of
+    order) equals the whole-layer attention bit for bit, rows outside a chunk
+    are left untouched, and the chunks' edge counts add up."""
+    n, B = 1300, 2
+    q, k, v = synth.random_qkv(B, HQ, HKV, n, D, seed=901, device="cuda")
+    layer = cuda_lib.Layer(TABLE, B, HQ, HKV, n, D, "cuda")
+    o_all = torch.empty_like(q)
+    l_all = torch.empty(B, HQ, n, device="cuda")
+    e_all = torch.zeros(B * HQ, dtype=torch.int64, device="cuda")
+    layer.index(q, k)
+    layer.attend(q, k, v, o_all, lse=l_all, edges=e_all)
+    sentinel = torch.full_like(q, 7.0)
+    o = sentinel.clone()
+    lse = torch.full((B, HQ, n), 7.0, device="cuda")
+    edges = torch.zeros(B * HQ, dtype=torch.int64, device="cuda")
+    layer.attend_rows(q, k, v, o, 512, 1024, lse=lse, edges=edges)
+    assert cuda_lib.poll_device_status() == 0
+    assert torch.equal(o[:, :, 512:1024], o_all[:, :, 512:1024])
+    assert torch.equal(o[:, :, :512], sentinel[:, :, :512]) and torch.equal(o[:, :, 1024:], sentinel[:, :, 1024:])
+    for lo, hi in [(1024, n), (0, 512)]:
+        layer.attend_rows(q, k, v, o, lo, hi, lse=lse, edges=edges)
+    assert cuda_lib.poll_device_status() == 0
+    assert torch.equal(o, o_all) and torch.equal(lse, l_all) and torch.equal(edges, e_all)
