@@ -223,6 +223,16 @@ MSA_API msa_status msa_prefill_layer(const msa_shape* shape, const void* q, cons
 MSA_API msa_status msa_merge_attention(int64_t rows, int32_t d_h, const void* o_a, const float* lse_a,
                                        const void* o_b, const float* lse_b, void* o, float* lse, void* stream);
 
+/* Captured dense mass per head (MInference page §5.1: the probability mass
+ * outside the sparse set is dropped and the rest renormalised): for each of
+ * `heads` rows-blocks of n query rows, mass[h] = (1/n) Σ_i e^{lse_sparse - lse_dense}
+ * = the mean over rows of Σ_{j in N(i)} p_ij under the dense causal softmax p.
+ * lse_sparse: [heads, n] LSE of the sparse layer; lse_dense: [heads, n] LSE of
+ * msa_attn_dense on the same inputs; rows whose sparse set is empty count 0.
+ * mass: [heads] fp32.  Deterministic (fixed summation order). */
+MSA_API msa_status msa_captured_mass(int64_t heads, int64_t n, const float* lse_sparse, const float* lse_dense,
+                                     float* mass, void* stream);
+
 /* Chunked prefill (MInference page §5.2: a scheduler may cut a long prefill
  * into chunks so that it does not block short requests): msa_layer_attend
  * restricted to the query rows [row_begin, row_end) of every head; rows

@@ -30,7 +30,7 @@ EXPORTS = ("msa_status_string", "msa_vs_index_workspace", "msa_block_index_works
            "msa_prefill_layer", "msa_layer_index", "msa_layer_attend", "msa_kernel_launches", "msa_layer_indices",
            "msa_vs_expand", "msa_poll_device_status", "msa_build_block_index_static",
            "msa_check_wait_timeout", "msa_attn_dense", "msa_layer_varlen_workspace", "msa_prefill_layer_varlen",
-           "msa_layer_attend_rows", "msa_merge_attention")
+           "msa_layer_attend_rows", "msa_merge_attention", "msa_captured_mass")
 
 
 class MsaError(RuntimeError):
@@ -114,6 +114,8 @@ def load(path: str = LIB_PATH):
             lib.msa_layer_attend_rows.argtypes = [P, P, P, P, P, P, P, P, P, sz, i32, i32, P]
             lib.msa_merge_attention.restype = st
             lib.msa_merge_attention.argtypes = [ctypes.c_int64, i32, P, P, P, P, P, P, P]
+            lib.msa_captured_mass.restype = st
+            lib.msa_captured_mass.argtypes = [ctypes.c_int64, ctypes.c_int64, P, P, P, P]
             lib.msa_build_block_index_static.restype = st
             lib.msa_build_block_index_static.argtypes = [P, P, P, P, i32, i32, i32, P, P, P]
             _lib = lib
@@ -441,6 +443,17 @@ def merge_attention(o_a, lse_a, o_b, lse_b, o=None, lse=None, stream=None):
     _check(load().msa_merge_attention(rows, d, _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o), _ptr(lse),
                                       _stream(stream)), "msa_merge_attention")
     return o, lse
+
+
+def captured_mass(lse_sparse, lse_dense, stream=None):
+    """Per-head share of the dense softmax mass kept by the sparse sets (msa_captured_mass).
+    lse_*: [..., n] with the leading dims flattened into heads; returns [heads] fp32."""
+    n = lse_sparse.shape[-1]
+    heads = lse_sparse.numel() // n
+    mass = torch.empty(heads, dtype=torch.float32, device=lse_sparse.device)
+    _check(load().msa_captured_mass(heads, n, _ptr(lse_sparse), _ptr(lse_dense), _ptr(mass), _stream(stream)),
+           "msa_captured_mass")
+    return mass
 
 
 def kernel_launches() -> int:

@@ -80,3 +80,42 @@ extern "C" msa_status msa_merge_attention(int64_t rows, int32_t d_h, const void*
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
+
+// ------------------------------------------------------------------ captured mass
+// Share of each row's dense softmax mass that the sparse set keeps (MInference
+// page §5.1: the probability outside the candidates is dropped and the rest
+// renormalised): Σ_{j in N(i)} e^{s_ij} / Σ_{j <= i} e^{s_ij} = e^{lse_sparse(i)
+// - lse_dense(i)}.  One CTA per head averages it over the head's rows in a
+// fixed order (deterministic).
+namespace msa {
+namespace {
+__global__ void __launch_bounds__(256) captured_mass_kernel(const float* ls, const float* ld, int64_t n, float* mass) {
+  __shared__ double part[256];
+  const int64_t h = blockIdx.x;
+  double acc = 0.0;
+  for (int64_t i = threadIdx.x; i < n; i += 256) {
+    const float a = ls[h * n + i], b = ld[h * n + i];
+    if (a != -INFINITY && b != -INFINITY) acc += (double)expf(a - b);
+  }
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) part[threadIdx.x] += part[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) mass[h] = (float)(part[0] / (double)n);
+}
+}  // namespace
+}  // namespace msa
+
+extern "C" msa_status msa_captured_mass(int64_t heads, int64_t n, const float* lse_sparse, const float* lse_dense,
+                                        float* mass, void* stream) {
+  if (heads < 0 || n < 1 || !lse_sparse || !lse_dense || !mass) return MSA_ERR_INVALID_ARG;
+  for (const float* p : {lse_sparse, lse_dense, static_cast<const float*>(mass)})
+    if (reinterpret_cast<uintptr_t>(p) % 4) return MSA_ERR_INVALID_ARG;
+  if (heads == 0) return MSA_OK;
+  if (heads > 0x7FFFFFFF) return MSA_ERR_UNSUPPORTED;
+  msa::captured_mass_kernel<<<(unsigned)heads, 256, 0, (cudaStream_t)stream>>>(lse_sparse, lse_dense, n, mass);
+  msa::note_launch();
+  return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}

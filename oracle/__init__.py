@@ -247,6 +247,20 @@ def merge(o_a, lse_a, o_b, lse_b):
     return o, lse
 
 
+def captured_mass(q, k, rows, keysets, scale: float):
+    """Mean over the given rows of the dense causal softmax mass that falls in
+    each row's key set (MInference page §5.1): Σ_{j in set} p_ij with
+    p_ij = e^{s_ij} / Σ_{j' <= i} e^{s_ij'} (fp64, plain loops over rows)."""
+    q, k = np.asarray(q, np.float64), np.asarray(k, np.float64)
+    total = 0.0
+    for i, ks in zip(rows, keysets):
+        s = (k[:i + 1] @ q[i]) * scale
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        total += p[np.asarray(ks, np.int64)].sum() if len(ks) else 0.0
+    return total / len(rows)
+
+
 def _head(cfg: dict) -> _Head:
     return _Head(int(cfg["pattern"]), int(cfg.get("sink", 0)), int(cfg.get("window", 0)),
                  int(cfg.get("block", 64)), int(cfg.get("topk", 0)))

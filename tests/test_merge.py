@@ -116,3 +116,52 @@ def test_vertical_sets_computed_apart_and_merged(cuda_lib):
         ro, rl, _ = oracle.head_rows(dict(pattern=oracle.VS, block=64), qn, kn, vn, np.arange(n), scale_of(d), C=C[h],
                                      D=np.array([], np.int64))
         compare_rows(f32(o[0, h]), f32(lse[0, h]), ro, rl, f"merged verticals h{h}")
+
+
+# ----------------------------------------------------------------- captured mass
+def test_oracle_captured_mass_pins():
+    rng = np.random.default_rng(5)
+    n, d = 120, 8
+    # fp32-representable inputs: oracle.attend takes fp32 tensors, so both paths see the same values
+    q, k = (rng.standard_normal((n, d)).astype(np.float32).astype(np.float64) for _ in range(2))
+    rows = np.arange(n)
+    full = [np.arange(i + 1) for i in rows]
+    assert abs(oracle.captured_mass(q, k, rows, full, 0.3) - 1.0) < 1e-12
+    assert oracle.captured_mass(q, k, rows, [np.array([], np.int64)] * n, 0.3) == 0.0
+    # a set and its complement share the mass; the share is e^(lse_set - lse_dense)
+    sets = [np.flatnonzero(rng.random(i + 1) < 0.4) for i in rows]
+    comp = [np.setdiff1d(np.arange(i + 1), s) for i, s in zip(rows, sets)]
+    a = oracle.captured_mass(q, k, rows, sets, 0.3)
+    b = oracle.captured_mass(q, k, rows, comp, 0.3)
+    assert abs(a + b - 1.0) < 1e-12
+    v = rng.standard_normal((n, d)).astype(np.float32)
+    shares = []
+    for i, s in zip(rows, sets):
+        if len(s) == 0:
+            shares.append(0.0)
+            continue
+        _, ls = oracle.attend(q, k, v, i, s, 0.3)
+        _, ld = oracle.attend(q, k, v, i, np.arange(i + 1), 0.3)
+        shares.append(np.exp(ls - ld))
+    assert abs(np.mean(shares) - a) < 1e-12
+
+
+@pytest.mark.gpu
+def test_captured_mass_of_ashape_heads(cuda_lib):
+    n, d, Hq, Hkv = 2048, 128, 4, 2
+    q, k, v = synth.random_qkv(1, Hq, Hkv, n, d, 61, device="cuda", scale_q=2.0)
+    cfgs = [(4, 64), (0, 256), (64, 512), (0, n)]
+    lse_s = torch.empty(1, Hq, n, device="cuda")
+    for h, (g, w) in enumerate(cfgs):
+        cuda_lib.attn_ashape(q, k, v, [h], g, w, lse=lse_s)
+    lse_d = torch.empty(1, Hq, n, device="cuda")
+    cuda_lib.attn_dense(q, k, v, list(range(Hq)), lse=lse_d)
+    mass = cuda_lib.captured_mass(lse_s, lse_d)
+    assert cuda_lib.poll_device_status() == 0
+    rows = np.arange(n)
+    for h, (g, w) in enumerate(cfgs):
+        qn, kn, _ = head_qkv(q, k, v, 0, h, Hq, Hkv)
+        sets = [np.union1d(np.arange(min(g, i + 1)), np.arange(max(0, i - w + 1), i + 1)) for i in rows]
+        ref = oracle.captured_mass(qn, kn, rows, sets, scale_of(d))
+        assert abs(float(mass[h]) - ref) < 2e-3, (h, float(mass[h]), ref)
+    assert abs(float(mass[3]) - 1.0) < 1e-4
