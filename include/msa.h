@@ -78,7 +78,15 @@ typedef struct {
   int32_t n_slash;    /* Vertical-Slash: s diagonal offsets kept */
   int32_t block;      /* Vertical-Slash / Block-Sparse block size (64) */
   int32_t topk;       /* Block-Sparse: k_b key blocks per query block (>= 1) */
+  int32_t proxy;      /* Vertical-Slash proxy convention, MSA_PROXY_* bits (0: sums) */
 } msa_head_cfg;
+
+/* Vertical-Slash proxy conventions (msa_head_cfg.proxy bits; MInference page
+ * §3.1: a column score may be the maximum over the sampled rows, which keeps a
+ * single strong response, or their sum; §6.2: offset d has only the legal
+ * pairs (i, i-d) of the sampled rows with i >= d, so a slash sum favours short
+ * offsets and a slash mean does not).  0 = column sums and slash sums. */
+enum { MSA_PROXY_COL_MAX = 1, MSA_PROXY_SLASH_MEAN = 2 };
 
 /* Vertical-Slash index of a set of heads (device buffers owned by the caller).
  * For slot s (see conventions), with v_cap = min(n_vertical, n) and

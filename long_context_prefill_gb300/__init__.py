@@ -47,7 +47,7 @@ class Shape(ctypes.Structure):
 class HeadCfg(ctypes.Structure):
     _fields_ = [("pattern", ctypes.c_int32), ("sink", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("last_q", ctypes.c_int32), ("n_vertical", ctypes.c_int32), ("n_slash", ctypes.c_int32),
-                ("block", ctypes.c_int32), ("topk", ctypes.c_int32)]
+                ("block", ctypes.c_int32), ("topk", ctypes.c_int32), ("proxy", ctypes.c_int32)]
 
 
 class VSIndexC(ctypes.Structure):
@@ -157,7 +157,7 @@ def head_cfg(entry: dict) -> HeadCfg:
     pat = PATTERNS[pat] if isinstance(pat, str) else int(pat)
     return HeadCfg(pat, int(entry.get("sink", 0)), int(entry.get("window", 1)), int(entry.get("last_q", 64)),
                    int(entry.get("n_vertical", 0)), int(entry.get("n_slash", 0)), int(entry.get("block", 64)),
-                   int(entry.get("topk", 1)))
+                   int(entry.get("topk", 1)), int(entry.get("proxy", 0)))
 
 
 def table_array(table):
@@ -267,11 +267,12 @@ def attn_block(q, k, v, heads, topk, block_idx, block_cnt, o=None, lse=None, edg
 
 
 # ----------------------------------------------------------------- indices
-def build_vs_index(q, k, heads, last_q, n_vertical, n_slash, index: VSIndex | None = None, scale=None, stream=None):
+def build_vs_index(q, k, heads, last_q, n_vertical, n_slash, index: VSIndex | None = None, scale=None, stream=None,
+                   proxy: int = 0):
     lib = load()
     sh = make_shape(q, k, scale)
     hp, nh = _heads(heads)
-    cfg = HeadCfg(VS, 0, 1, int(last_q), int(n_vertical), int(n_slash), 64, 1)
+    cfg = HeadCfg(VS, 0, 1, int(last_q), int(n_vertical), int(n_slash), 64, 1, int(proxy))
     if index is None:
         index = VSIndex(q.shape[0] * nh, q.shape[2], n_vertical, n_slash, q.device)
     ws_bytes = lib.msa_vs_index_workspace(ctypes.byref(sh), ctypes.byref(cfg), nh)

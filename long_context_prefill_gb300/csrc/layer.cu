@@ -42,6 +42,7 @@ static msa_status check_cfg(const msa_head_cfg& c) {
       return MSA_OK;
     case MSA_VS:
       if (c.last_q < 1 || c.n_vertical < 0 || c.n_slash < 0) return MSA_ERR_INVALID_ARG;
+      if (c.proxy < 0 || c.proxy > 3) return MSA_ERR_INVALID_ARG;
       if (c.block != 64) return MSA_ERR_UNSUPPORTED;
       return MSA_OK;
     case MSA_BLOCK:
@@ -79,7 +80,7 @@ static msa_status plan_layer(const msa_shape& s, const msa_head_cfg* table, void
     } else if (table[h].pattern == MSA_VS) {
       if (!P.vs_heads.empty() &&
           (table[h].last_q != P.vs_cfg.last_q || table[h].n_vertical != P.vs_cfg.n_vertical ||
-           table[h].n_slash != P.vs_cfg.n_slash))
+           table[h].n_slash != P.vs_cfg.n_slash || table[h].proxy != P.vs_cfg.proxy))
         return MSA_ERR_UNSUPPORTED;  // one Vertical-Slash budget per layer
       P.vs_cfg = table[h];
       P.vs_heads.push_back(h);
@@ -151,6 +152,7 @@ msa_status msa_build_vs_index(const msa_shape* shape, const void* q, const void*
   if ((st = check_heads(heads, n_heads, shape->Hq)) != MSA_OK) return st;
   if (!cfg || !out || !q || !k) return MSA_ERR_INVALID_ARG;
   if (cfg->last_q < 1 || cfg->n_vertical < 0 || cfg->n_slash < 0) return MSA_ERR_INVALID_ARG;
+  if (cfg->proxy < 0 || cfg->proxy > 3) return MSA_ERR_INVALID_ARG;
   if (cfg->block != 64) return MSA_ERR_UNSUPPORTED;
   return run_vs_index(*shape, q, k, heads, n_heads, *cfg, *out, ws, ws_bytes, (cudaStream_t)stream);
 }

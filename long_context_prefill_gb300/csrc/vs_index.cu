@@ -71,6 +71,7 @@ struct ProxyArgs {
   float* colsum;       // [slots, n] log2 c_j
   float* rpart;        // [slots, nkb + LB, LB + 1, 32] log2 partial slash sums
   int32_t nkb;         // 4 * ntiles key blocks of 32
+  int32_t mode;        // proxy convention bits (MSA_PROXY_*)
   int* err;
 };
 
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
             bsum[cc] += hs;
             bsum[cc + 1] += ls;
           }
-          col_log[x] = cs > 0.f ? cm + __log2f(cs) : -INFINITY;
+          col_log[x] = (A.mode & MSA_PROXY_COL_MAX) ? cm : (cs > 0.f ? cm + __log2f(cs) : -INFINITY);
 #pragma unroll
           for (int m = 0; m <= LB; ++m) bin_log[x][m] = bsum[m] > 0.f ? bm[m] + __log2f(bsum[m]) : -INFINITY;
         }
@@ -399,7 +400,8 @@ __global__ void proxy_lse_kernel(const float2* part, int nchunks, float* lse2) {
 
 // log2 r_δ = log-sum-exp over the bins (y = n - L - δ) of the key blocks that
 // own them, m = 0..LB in order.
-__global__ void slash_finalize_kernel(const float* rpart, int n, int L, int LB, int nkb, int slots, float* r) {
+__global__ void slash_finalize_kernel(const float* rpart, int n, int L, int LB, int nkb, int slots, int mode,
+                                      float* r) {
   const int64_t total = (int64_t)slots * n;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -419,7 +421,9 @@ __global__ void slash_finalize_kernel(const float* rpart, int n, int L, int LB, 
     float s = 0.f;
     if (mx != -INFINITY)
       for (int m = 0; m <= LB; ++m) s += v[m] != -INFINITY ? exp2f(v[m] - mx) : 0.f;
-    r[slot * n + d] = s > 0.f ? mx + log2f(s) : -INFINITY;
+    float lr = s > 0.f ? mx + log2f(s) : -INFINITY;
+    if ((mode & MSA_PROXY_SLASH_MEAN) && lr != -INFINITY) lr -= log2f((float)min(L, n - d));  // legal pairs of offset d
+    r[slot * n + d] = lr;
   }
 }
 
@@ -918,6 +922,7 @@ msa_status run_vs_index(const msa_shape& s, const void* q, const void* k, const 
   a.Lp = P.Lp;
   a.ntiles = P.ntiles;
   a.nkb = P.nkb;
+  a.mode = cfg.proxy;
   const float scale = s.scale > 0.f ? s.scale : 1.0f / sqrtf((float)s.d_h);
   a.c2 = scale * 1.4426950408889634f;
   a.part = reinterpret_cast<float2*>(w + P.off_part);
@@ -942,7 +947,7 @@ msa_status run_vs_index(const msa_shape& s, const void* q, const void* k, const 
   {
     const int64_t total = (int64_t)P.slots * s.n;
     const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
-    slash_finalize_kernel<<<blocks, 256, 0, stream>>>(a.rpart, s.n, P.L, P.LB, P.nkb, P.slots, slashsum);
+    slash_finalize_kernel<<<blocks, 256, 0, stream>>>(a.rpart, s.n, P.L, P.LB, P.nkb, P.slots, cfg.proxy, slashsum);
     note_launch();
     if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   }

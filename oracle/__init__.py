@@ -63,8 +63,8 @@ def _load():
             lib.ora_bs_set.restype = i64
             lib.ora_bs_set.argtypes = [i64, i64, i64, P, P, i64, P]
             lib.ora_vs_proxy_probs.argtypes = [i64, i64, i64, f64, P, P, P]
-            lib.ora_proxy_aggregate.argtypes = [P, i64, i64, P, P, P]
-            lib.ora_vs_proxy.argtypes = [i64, i64, i64, f64, P, P, P, P]
+            lib.ora_proxy_aggregate.argtypes = [P, i64, i64, P, P, P, ctypes.c_int32]
+            lib.ora_vs_proxy.argtypes = [i64, i64, i64, f64, P, P, P, P, ctypes.c_int32]
             lib.ora_topk.restype = i64
             lib.ora_topk.argtypes = [P, i64, i64, P]
             lib.ora_bs_pool.argtypes = [P, i64, i64, i64, P]
@@ -157,25 +157,31 @@ def vs_proxy_probs(q, k, last_q: int, scale: float) -> np.ndarray:
     return A
 
 
-def proxy_aggregate(A, pos):
+# proxy conventions (bits): column maximum instead of the sum, slash mean instead of the sum
+PROXY_SUM, PROXY_COL_MAX, PROXY_SLASH_MEAN = 0, 1, 2
+
+
+def proxy_aggregate(A, pos, mode: int = PROXY_SUM):
     """MInference page §3.1/§6.2: column sums c_j = Σ_t A[t, j] and slash sums
-    r_d = Σ_t A[t, pos[t] - d] of a proxy matrix whose row t is query pos[t]."""
+    r_d = Σ_t A[t, pos[t] - d] of a proxy matrix whose row t is query pos[t]
+    (mode: PROXY_COL_MAX takes the column maximum, PROXY_SLASH_MEAN divides each
+    slash sum by its number of legal pairs)."""
     A = np.ascontiguousarray(np.asarray(A, dtype=np.float64))
     rows, n = A.shape
     pos = np.ascontiguousarray(np.asarray(pos, dtype=np.int64))
     c = np.empty(n, dtype=np.float64)
     r = np.empty(n, dtype=np.float64)
-    _load().ora_proxy_aggregate(_p(A), rows, n, _p(pos), _p(c), _p(r))
+    _load().ora_proxy_aggregate(_p(A), rows, n, _p(pos), _p(c), _p(r), int(mode))
     return c, r
 
 
-def vs_proxy(q, k, last_q: int, scale: float):
+def vs_proxy(q, k, last_q: int, scale: float, mode: int = PROXY_SUM):
     """Column scores c [n] and slash scores r [n] of one head (fp64)."""
     q, k = _f32(q), _f32(k)
     n, d = k.shape
     c = np.empty(n, dtype=np.float64)
     r = np.empty(n, dtype=np.float64)
-    _load().ora_vs_proxy(n, d, min(int(last_q), n), float(scale), _p(q), _p(k), _p(c), _p(r))
+    _load().ora_vs_proxy(n, d, min(int(last_q), n), float(scale), _p(q), _p(k), _p(c), _p(r), int(mode))
     return c, r
 
 
@@ -187,9 +193,9 @@ def topk(score, k: int) -> np.ndarray:
     return out[:m].copy()
 
 
-def vs_index(q, k, last_q: int, n_vertical: int, n_slash: int, scale: float):
+def vs_index(q, k, last_q: int, n_vertical: int, n_slash: int, scale: float, mode: int = PROXY_SUM):
     """Vertical-Slash index of one head: (C ascending, D descending, c, r)."""
-    c, r = vs_proxy(q, k, last_q, scale)
+    c, r = vs_proxy(q, k, last_q, scale, mode)
     C = np.sort(topk(c, n_vertical))
     D = np.sort(topk(r, n_slash))[::-1].copy()
     return C, D, c, r

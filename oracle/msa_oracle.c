@@ -275,28 +275,46 @@ void ora_vs_proxy_probs(int64_t n, int64_t d, int64_t L, double scale, const flo
 
 /* [MI] §3.1 and §6.2 aggregation of a proxy matrix whose row t is query
  * position pos[t]: column scores c_j = Σ_t A[t][j] and slash scores
- * r_d = Σ_t A[t][pos[t] - d] over the rows with pos[t] - d >= 0. */
-void ora_proxy_aggregate(const double* A, int64_t rows, int64_t n, const int64_t* pos, double* c, double* r) {
+ * r_d = Σ_t A[t][pos[t] - d] over the rows with pos[t] - d >= 0.
+ * mode bit 0: column score = the maximum over the rows instead of the sum
+ * ([MI] §3.1: one strong response kept, sensitive to spikes); mode bit 1:
+ * slash score = the mean over its legal pairs (rows with pos[t] - d >= 0)
+ * instead of the sum ([MI] §6.2: a sum favours short offsets, which have
+ * more pairs); an offset with no legal pair scores 0. */
+void ora_proxy_aggregate(const double* A, int64_t rows, int64_t n, const int64_t* pos, double* c, double* r,
+                         int32_t mode) {
+  int64_t* cnt = (int64_t*)calloc((size_t)n, sizeof(int64_t));
   for (int64_t j = 0; j < n; ++j) c[j] = 0.0;
   for (int64_t dd = 0; dd < n; ++dd) r[dd] = 0.0;
   for (int64_t t = 0; t < rows; ++t) {
     const double* row = A + t * n;
     for (int64_t j = 0; j < n; ++j) {
-      c[j] += row[j];
+      if (mode & 1) {
+        if (row[j] > c[j]) c[j] = row[j];
+      } else {
+        c[j] += row[j];
+      }
       int64_t dd = pos[t] - j; /* the slash through (pos[t], j) */
-      if (dd >= 0 && dd < n) r[dd] += row[j];
+      if (dd >= 0 && dd < n) {
+        r[dd] += row[j];
+        ++cnt[dd];
+      }
     }
   }
+  if (mode & 2)
+    for (int64_t dd = 0; dd < n; ++dd) r[dd] = cnt[dd] ? r[dd] / (double)cnt[dd] : 0.0;
+  free(cnt);
 }
 
 /* Full Vertical-Slash proxy: Ã for rows [n-L, n), then c and r. */
-void ora_vs_proxy(int64_t n, int64_t d, int64_t L, double scale, const float* q, const float* k, double* c, double* r) {
+void ora_vs_proxy(int64_t n, int64_t d, int64_t L, double scale, const float* q, const float* k, double* c, double* r,
+                  int32_t mode) {
   if (L > n) L = n;
   double* A = (double*)malloc(sizeof(double) * (size_t)(L * n));
   int64_t* pos = (int64_t*)malloc(sizeof(int64_t) * (size_t)L);
   ora_vs_proxy_probs(n, d, L, scale, q, k, A);
   for (int64_t t = 0; t < L; ++t) pos[t] = n - L + t;
-  ora_proxy_aggregate(A, L, n, pos, c, r);
+  ora_proxy_aggregate(A, L, n, pos, c, r, mode);
   free(A);
   free(pos);
 }

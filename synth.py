@@ -49,8 +49,9 @@ def ashape(sink, window):
     return dict(pattern="ashape", sink=int(sink), window=int(window))
 
 
-def vslash(last_q, v, s, block=64):
-    return dict(pattern="vs", last_q=int(last_q), n_vertical=int(v), n_slash=int(s), block=int(block))
+def vslash(last_q, v, s, block=64, proxy=0):
+    return dict(pattern="vs", last_q=int(last_q), n_vertical=int(v), n_slash=int(s), block=int(block),
+                proxy=int(proxy))
 
 
 def blocksparse(topk, block=64):

@@ -27,13 +27,13 @@ def check_set(got, want, scores, what):
     return len(got ^ want)
 
 
-def run_vs(msa, q, k, heads, last_q, v, s):
-    idx = msa.build_vs_index(q, k, heads, last_q, v, s)
+def run_vs(msa, q, k, heads, last_q, v, s, proxy=0):
+    idx = msa.build_vs_index(q, k, heads, last_q, v, s, proxy=proxy)
     assert msa.poll_device_status() == 0
     return idx
 
 
-def check_vs_against_oracle(idx, q, k, heads, last_q, v, s, exact=False):
+def check_vs_against_oracle(idx, q, k, heads, last_q, v, s, exact=False, proxy=0):
     B, Hq, n, d = q.shape
     Hkv = k.shape[1]
     scale = 1.0 / np.sqrt(d)
@@ -42,7 +42,7 @@ def check_vs_against_oracle(idx, q, k, heads, last_q, v, s, exact=False):
         for x, h in enumerate(heads):
             slot = b * len(heads) + x
             qn, kn, _ = head_qkv(q, k, k, b, h, Hq, Hkv)
-            C, D, c, r = oracle.vs_index(qn, kn, last_q, v, s, scale)
+            C, D, c, r = oracle.vs_index(qn, kn, last_q, v, s, scale, proxy)
             vc, sc = int(idx.vertical_cnt[slot]), int(idx.slash_cnt[slot])
             gC = idx.vertical[slot, :vc].cpu().numpy()
             gD = idx.slash[slot, :sc].cpu().numpy()
@@ -95,6 +95,28 @@ def test_vs_index_exact_ties(cuda_lib):
     check_vs_against_oracle(idx, q, k, [0, 1], 64, 1000, 3000)
     for slot in range(2):
         assert idx.vertical[slot, :1000].cpu().tolist() == list(range(1000))
+
+
+@pytest.mark.parametrize("proxy", [1, 2, 3])
+@pytest.mark.parametrize("n,d,last_q,Hq,Hkv,heads,v,s", [
+    (1000, 128, 64, 4, 1, [0, 1, 2, 3], 40, 90),
+    (777, 64, 17, 4, 2, [1, 2, 3], 13, 50),
+])
+def test_vs_index_proxy_conventions(cuda_lib, proxy, n, d, last_q, Hq, Hkv, heads, v, s):
+    """Column maximum (bit 1) and slash mean over legal pairs (bit 2) against
+    the oracle's conventions, on random inputs (the 1e-4 rule)."""
+    q, k, _ = synth.random_qkv(1, Hq, Hkv, n, d, seed=n + 7 * proxy, device="cuda")
+    idx = run_vs(cuda_lib, q, k, heads, last_q, v, s, proxy=proxy)
+    check_vs_against_oracle(idx, q, k, heads, last_q, v, s, proxy=proxy)
+
+
+def test_vs_index_proxy_planted(cuda_lib):
+    """The tiny planted head under each convention, against the oracle's
+    index under the same convention."""
+    w = synth.make_workload("tiny", device="cuda")
+    for proxy in (1, 2, 3):
+        idx = run_vs(cuda_lib, w["q"], w["k"], [1], 64, 64, 128, proxy=proxy)
+        check_vs_against_oracle(idx, w["q"], w["k"], [1], 64, 64, 128, proxy=proxy)
 
 
 def test_vs_index_batch(cuda_lib):

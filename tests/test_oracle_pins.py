@@ -81,6 +81,36 @@ def test_proxy_topk_example_eq12():
     assert oracle.topk(c, 1).tolist() == [g["selected_top1"]]
     assert oracle.topk(P.max(axis=0), 1).tolist() == [g["selected_top1"]]
     np.testing.assert_allclose(P.max(axis=0), g["printed_column_max"])
+    # the column-maximum convention reproduces the printed maxima and the same choice
+    cm, _ = oracle.proxy_aggregate(P, [6, 7], oracle.PROXY_COL_MAX)
+    np.testing.assert_allclose(cm, g["printed_column_max"], atol=1e-15)
+    assert oracle.topk(cm, 1).tolist() == [g["selected_top1"]]
+
+
+def test_proxy_slash_mean_counts_legal_pairs():
+    """Slash mean (MInference page §6.2: offset d has fewer legal pairs than a
+    short one): with every proxy probability 1 on the causal part, each legal
+    pair adds 1, so the sum of r_d is the number of legal pairs (rows with
+    pos >= d) and the mean is exactly 1 for every offset that has one, 0 else."""
+    n, pos = 10, [6, 7, 8, 9]
+    A = np.zeros((4, n))
+    for t, i in enumerate(pos):
+        A[t, :i + 1] = 1.0
+    _, rs = oracle.proxy_aggregate(A, pos)
+    assert rs.tolist() == [sum(1 for i in pos if i >= d) for d in range(n)]
+    _, rm = oracle.proxy_aggregate(A, pos, oracle.PROXY_SLASH_MEAN)
+    assert rm.tolist() == [1.0] * n
+    A2 = A.copy()
+    A2[:, 0] = 0.0  # key 0 dropped: offsets d = pos reach only key 0
+    _, rm2 = oracle.proxy_aggregate(A2, pos, oracle.PROXY_SLASH_MEAN)
+    for d in range(n):
+        legal = [i for i in pos if i >= d]
+        want = sum(1.0 for i in legal if i - d != 0) / len(legal)
+        assert rm2[d] == want
+    # column max and sum agree when a single row is sampled
+    c1, _ = oracle.proxy_aggregate(A[:1], pos[:1])
+    cm1, _ = oracle.proxy_aggregate(A[:1], pos[:1], oracle.PROXY_COL_MAX)
+    assert c1.tolist() == cm1.tolist()
 
 
 def test_proxy_slash_indexing_one_hot():
