@@ -59,10 +59,7 @@ struct AttnArgs {
   int32_t nqt;               // 128-row query tiles over n
   int32_t n_bands;           // bands in the unit table
   float scale_log2;  // scale * log2(e)
-  const void* q;     // bf16 [B*Hq, n, d] (rows loaded into TMEM)
-  const void* k;     // bf16 [B*Hkv, n, d] (column gathers)
-  const void* v;
-  void* o;           // bf16 [B*Hq, n, d]
+  void* o;           // bf16 [B*Hq, n, d] (q, k, v are read through the TMA maps)
   float* lse;        // [B*Hq, n] or null
   unsigned long long* edges;  // [B*Hq] or null
   // Vertical-Slash index (slot-indexed)

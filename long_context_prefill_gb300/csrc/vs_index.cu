@@ -14,7 +14,7 @@
 //                 online (max, sum) per row -> partials
 //   proxy_lse     combine the partials into lse per row
 //   proxy_scores  pass 2, tcgen05 S^T = K Q_R^T; thread = key; Ã for every
-//                 (row, key); c_j summed in registers; slash sums gathered
+//                 (row, key); c_j summed in registers; slash sums collected
 //                 along diagonals with warp shuffles into per-key-block bins
 //   slash_finalize  adds each diagonal's bins in a fixed order -> r
 //   topk_select   radix select (threshold), then an index-ordered compaction
