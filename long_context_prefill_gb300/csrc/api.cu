@@ -242,6 +242,9 @@ msa_status attention(const msa_shape& s, const void* q, const void* k, const voi
   a.nqt = ceil_div(s.n, 128);
   a.T = (a.nqt + 1) / 2;
   a.scale_log2 = effective_scale(s) * 1.4426950408889634f;
+  a.q = q;
+  a.k = k;
+  a.v = v;
   a.o = o;
   a.lse = lse;
   a.edges = reinterpret_cast<unsigned long long*>(edges);

@@ -59,7 +59,10 @@ struct AttnArgs {
   int32_t nqt;               // 128-row query tiles over n
   int32_t n_bands;           // bands in the unit table
   float scale_log2;  // scale * log2(e)
-  void* o;           // bf16 [B*Hq, n, d] (q, k, v are read through the TMA maps)
+  const void* q;     // bf16 [B*Hq, n, d] (the kernel reads q, k, v through the TMA maps; the
+  const void* k;     // pointers stay in the arguments: dropping them measured 1.5 % slower
+  const void* v;     // code for the same work)
+  void* o;           // bf16 [B*Hq, n, d]
   float* lse;        // [B*Hq, n] or null
   unsigned long long* edges;  // [B*Hq] or null
   // Vertical-Slash index (slot-indexed)
