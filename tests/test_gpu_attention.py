@@ -178,3 +178,63 @@ def test_dense_causal_matches_sdpa(cuda_lib, n, d):
             torch.from_numpy(vn).double()[None], is_causal=True, scale=scale_of(d))[0].numpy()
         assert np.abs(f32(o[0, h]) - ref).max() <= 1.5e-2
         assert int(edges[h]) == n * (n + 1) // 2
+
+
+@pytest.mark.parametrize("pattern", ["dense", "ashape"])
+def test_extreme_logits(cuda_lib, pattern):
+    """Logits of order ±100 whose scale grows along the key axis, so later
+    key tiles raise each row's running maximum by tens of units and the
+    online rescale of eq.(7)-(8) (MInference page §3.2) drops earlier
+    partial sums to underflow; the result must still be eq.(2) over the set."""
+    n, d, Hq, Hkv = 1000, 128, 2, 1
+    q, k, v = synth.random_qkv(1, Hq, Hkv, n, d, seed=91, device="cuda", scale_q=8.0)
+    ramp = torch.linspace(1.0, 4.0, n, device="cuda")[None, None, :, None]
+    k = (k.float() * ramp).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty(1, Hq, n, device="cuda")
+    if pattern == "dense":
+        cuda_lib.attn_dense(q, k, v, [0, 1], o=o, lse=lse)
+        cfg = dict(pattern=oracle.DENSE)
+    else:
+        cuda_lib.attn_ashape(q, k, v, [0, 1], 16, 300, o=o, lse=lse)
+        cfg = dict(pattern=oracle.ASHAPE, sink=16, window=300)
+    assert cuda_lib.poll_device_status() == 0
+    for h in range(Hq):
+        qn, kn, vn = head_qkv(q, k, v, 0, h, Hq, Hkv)
+        ro, rl, _ = oracle.head_rows(cfg, qn, kn, vn, np.arange(n), scale_of(d))
+        assert rl.max() > 60.0  # the case really reaches large logits
+        compare_rows(f32(o[0, h]), f32(lse[0, h]), ro, rl, f"{pattern} extreme h{h}")
+
+
+@pytest.mark.parametrize("n,topk", [
+    (700, 20),            # k_b above N_b = 11
+    (64 * 520 + 17, 521),  # k_b = N_b = 521: the last rows' lists exceed the 512 entries staged in shared memory
+])
+def test_block_budget_covering_every_key_is_dense(cuda_lib, n, topk):
+    """Block-Sparse with k_b >= N_b (index built on the device, attention on
+    its lists) reduces to dense causal attention, eq.(1)-(2): J_u = {0..u},
+    E = n(n+1)/2.  The long case takes the path that reads lists longer than
+    the shared-memory stage straight from global memory."""
+    d, Hq, Hkv = 128, 2, 1
+    q, k, v = synth.random_qkv(1, Hq, Hkv, n, d, seed=n, device="cuda")
+    bidx, bcnt = cuda_lib.build_block_index(q, k, [1], topk)
+    assert cuda_lib.poll_device_status() == 0
+    nb = (n + 63) // 64
+    cnt = bcnt[0, 0].cpu().numpy()
+    assert (cnt == np.minimum(np.arange(nb) + 1, topk)).all()
+    idx = bidx[0, 0].cpu().numpy()
+    for u in range(nb):
+        assert (idx[u, :u + 1] == np.arange(u + 1)).all(), f"block {u}"
+    o = torch.zeros_like(q)
+    lse = torch.empty(1, Hq, n, device="cuda")
+    edges = torch.zeros(Hq, dtype=torch.int64, device="cuda")
+    cuda_lib.attn_block(q, k, v, [1], topk, bidx, bcnt, o=o, lse=lse, edges=edges)
+    assert cuda_lib.poll_device_status() == 0
+    rows = np.arange(n) if n <= 1000 else synth.sample_rows(n, 96, seed=3)
+    if n > 1000:
+        rows = np.unique(np.concatenate([rows, np.arange(n - 130, n)]))  # the blocks with > 512 entries
+    qn, kn, vn = head_qkv(q, k, v, 0, 1, Hq, Hkv)
+    ro, rl, _ = oracle.head_rows(dict(pattern=oracle.DENSE), qn, kn, vn, rows, scale_of(d))
+    compare_rows(f32(o[0, 1])[rows], f32(lse[0, 1])[rows], ro, rl, f"block dense n{n}")
+    assert int(edges[1]) == n * (n + 1) // 2
+    assert torch.all(o[0, 0] == 0)
