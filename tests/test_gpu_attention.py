@@ -238,3 +238,46 @@ def test_block_budget_covering_every_key_is_dense(cuda_lib, n, topk):
     compare_rows(f32(o[0, 1])[rows], f32(lse[0, 1])[rows], ro, rl, f"block dense n{n}")
     assert int(edges[1]) == n * (n + 1) // 2
     assert torch.all(o[0, 0] == 0)
+
+
+@pytest.mark.parametrize("heads,Hq,Hkv", [
+    ([0, 1], 4, 1),                 # a pair of heads
+    ([2], 4, 2),                    # a single head: its even and odd tiles
+    ([0, 1, 2, 3], 4, 1),           # two pairs of one group
+    ([0, 1, 2, 3, 4, 6], 8, 1),     # three pairs
+    ([7, 1, 2, 0, 5], 8, 1),        # two pairs, then a single
+    ([0, 1, 3, 4, 5, 6, 7], 8, 2),  # a pair and a single in one group, two pairs in the other
+])
+def test_vs_head_groupings(cuda_lib, heads, Hq, Hkv):
+    """Vertical-Slash attention on head subsets that pair into items in every
+    way (each sub-item reads its own head's index); per-head random verticals
+    and slashes, partly shared, so that an item's key stream mixes common and
+    private keys."""
+    n, d = 1000, 128
+    rng = np.random.default_rng(31 + len(heads))
+    q, k, v = synth.random_qkv(1, Hq, Hkv, n, d, seed=17 + len(heads), device="cuda")
+    C0, D0 = rng.choice(n, 30, replace=False), rng.choice(n, 20, replace=False)
+    C, D = [], []
+    index = cuda_lib.VSIndex(len(heads), n, 60, 40, "cuda")
+    for x in range(len(heads)):
+        Cx = np.unique(np.concatenate([C0[:20], rng.choice(n, 25, replace=False)]))
+        Dx = np.unique(np.concatenate([D0[:12], rng.choice(n, 15, replace=False), [0]]))[::-1]
+        C.append(Cx)
+        D.append(Dx)
+        index.vertical_bits[x] = torch.from_numpy(pack_bits(Cx, n)).cuda()
+        index.slash_bits[x] = torch.from_numpy(pack_bits(Dx, n)).cuda()
+        index.slash_cover[x] = torch.from_numpy(cover_bits(Dx, n)).cuda()
+    o = torch.zeros_like(q)
+    lse = torch.empty(1, Hq, n, device="cuda")
+    edges = torch.zeros(Hq, dtype=torch.int64, device="cuda")
+    cuda_lib.attn_vs(q, k, v, heads, index, o=o, lse=lse, edges=edges)
+    assert cuda_lib.poll_device_status() == 0
+    cfg = dict(pattern=oracle.VS, block=64)
+    for x, h in enumerate(heads):
+        qn, kn, vn = head_qkv(q, k, v, 0, h, Hq, Hkv)
+        ro, rl, _ = oracle.head_rows(cfg, qn, kn, vn, np.arange(n), scale_of(d), C=C[x], D=D[x])
+        compare_rows(f32(o[0, h]), f32(lse[0, h]), ro, rl, f"vs h{h}")
+        assert int(edges[h]) == oracle.head_edges(cfg, n, C=C[x], D=D[x])
+    for h in range(Hq):
+        if h not in heads:
+            assert torch.all(o[0, h] == 0)
