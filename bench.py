@@ -272,6 +272,92 @@ def attention_traffic(names, n_override):
     return int(sum(per.values())), per
 
 
+# ----------------------------------------------------------------- curves
+def _timed(fn, reps, flush):
+    """Median CUDA-event time (ms) of fn over reps calls, L2 flushed before each."""
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def curves(kind, local, reps=5):
+    """The curves the MInference page asks for beside the headline (§5.2: the
+    time decomposition eq.(13) and the length where sparse overtakes dense;
+    §6.2: sampled rows vs captured mass vs index time), on the seeded layers:
+
+    crossover: for each layer type and n, T_index + T_sparse of the sparse
+      layer against dense causal attention (msa_attn_dense) of every head on
+      the same inputs; speedup = dense / (index + sparse).
+    lastq: the Vertical-Slash and mixed layers at n = 131072 with last_q =
+      16 .. 128 sampled proxy rows: index time and attention time.
+    proxy: the same layers with each proxy aggregation convention (§3.1,
+      §6.2: column sum or maximum, slash sum or mean over legal pairs).
+    Every point also gives the captured dense mass per head (the mean over
+    rows of e^{lse_sparse - lse_dense}), as its mean and minimum over the heads
+    of each pattern."""
+    import long_context_prefill_gb300 as msa
+    import synth
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    msa.load()
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=device)
+    if kind == "crossover":
+        points = [(wl, n) for wl in ("vs128k", "bs128k", "mixed")
+                  for n in (4096, 8192, 16384, 32768, 65536, 131072)]
+    else:
+        points = [("vs128k", 131072), ("mixed", 131072)]
+    for wl, n in points:
+        w = synth.make_workload(wl, device=device, n=n)
+        sh = w["shape"]
+        q, k, v = w["q"], w["k"], w["v"]
+        o = torch.empty_like(q)
+        lse_d = torch.empty(sh["B"], sh["Hq"], n, device=device)
+        heads = list(range(sh["Hq"]))
+        dense = lambda: msa.attn_dense(q, k, v, heads, o=o, lse=lse_d)
+        dense()
+        t_dense = _timed(dense, reps, flush)
+        variants = {"crossover": [{}], "lastq": [{"last_q": x} for x in (16, 32, 64, 128)],
+                    "proxy": [{"proxy": x} for x in (0, 1, 2, 3)]}[kind]
+        for var in variants:
+            table = [dict(e) for e in w["table"]]
+            for e in table:
+                if e["pattern"] == "vs":
+                    e.update(var)
+            layer = msa.Layer(table, sh["B"], sh["Hq"], sh["Hkv"], n, sh["d"], device)
+            lse_s = torch.empty_like(lse_d)
+            edges = torch.zeros(sh["B"] * sh["Hq"], dtype=torch.int64, device=device)
+            layer(q, k, v, o=o, lse=lse_s, edges=edges)
+            t_idx = _timed(lambda: layer.index(q, k), reps, flush)
+            t_att = _timed(lambda: layer.attend(q, k, v, o, lse=lse_s), reps, flush)
+            assert msa.poll_device_status() == 0
+            E = float(edges.sum().item())
+            rec = {"curve": kind, "workload": wl, "n": n, "heads": sh["Hq"], "kv_heads": sh["Hkv"], "d_h": sh["d"],
+                   "t_index_ms": round(t_idx, 4), "t_sparse_ms": round(t_att, 4), "dense_ms": round(t_dense, 4),
+                   "speedup_vs_dense": round(t_dense / (t_idx + t_att), 3),
+                   "density": round(E / (sh["B"] * sh["Hq"] * n * (n + 1) / 2), 4),
+                   "effective_tflops": round(4.0 * E * sh["d"] / ((t_idx + t_att) * 1e-3) / 1e12, 1),
+                   "l2": "flushed (256 MiB write) before every timed call"}
+            rec.update(var)
+            mass = msa.captured_mass(lse_s, lse_d).cpu().numpy().reshape(sh["B"], sh["Hq"])
+            for pat in ("ashape", "vs", "block"):
+                hs = [h for h, e in enumerate(table) if e["pattern"] == pat]
+                if hs:
+                    rec[f"captured_mass_{pat}"] = {"mean": round(float(mass[:, hs].mean()), 5),
+                                                   "min": round(float(mass[:, hs].min()), 5)}
+            print(json.dumps(rec), flush=True)
+            del layer
+        del w, q, k, v, o
+        torch.cuda.empty_cache()
+
+
 # ----------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -285,12 +371,20 @@ def main():
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-baseline and cold-L2 measurements")
     ap.add_argument("--n", type=int, default=None,
                     help="override the sequence length (scaled-down runs for profiling; not a headline number)")
+    ap.add_argument("--curve", choices=["crossover", "lastq", "proxy"], default=None,
+                    help="instead of the step: the sparse-vs-dense crossover over sequence lengths, the sampled "
+                         "proxy rows sweep, or the proxy aggregation conventions, each with index time and "
+                         "captured mass (one JSON line per point)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     names = [x for x in args.workloads.split(",") if x]
 
     if args.impl == "reference":
         return reference_arm(args, world, rank, local, names)
+    if args.curve:
+        if rank == 0:
+            curves(args.curve, local)
+        return
 
     import long_context_prefill_gb300 as msa
     import synth
