@@ -202,7 +202,11 @@ MSA_API msa_status msa_attn_vs(const msa_shape* shape, const void* q, const void
 
 /* Block-Sparse attention (MInference page eq.(6)): row i of block u attends
  * the keys of blocks v in J_u with j <= i (the diagonal block is causal).
- * block_idx / block_cnt: as written by msa_build_block_index. */
+ * block_idx / block_cnt: as written by msa_build_block_index: for head slot x
+ * and query block u, the first block_cnt[x][u] (clamped to [0, topk]) entries
+ * of block_idx[x][u] are strictly ascending block ids in [0, u].  Entries that
+ * break this are skipped by the kernel and the next msa_poll_device_status
+ * returns MSA_ERR_INDEX (the output is then undefined). */
 MSA_API msa_status msa_attn_block(const msa_shape* shape, const void* q, const void* k, const void* v,
                           const int32_t* heads, int32_t n_heads, int32_t block, int32_t topk,
                           const int32_t* block_idx, const int32_t* block_cnt, void* o, float* lse,
