@@ -171,9 +171,58 @@ def _out_like(q, o):
     return torch.empty_like(q) if o is None else o
 
 
+def _want(t, what, dtype, shape=None, min_numel=None, device=None):
+    """Raise ValueError unless t (None passes) is a contiguous tensor of this
+    dtype and shape (on `device` if given): the library sees only a pointer,
+    so a smaller or strided buffer would be read or written out of bounds."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{what}: a torch.Tensor is required")
+    if t.dtype != dtype:
+        raise ValueError(f"{what}: dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{what}: {t.numel()} elements, at least {min_numel} needed")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{what}: on {t.device}, expected {device}")
+
+
+def _cuda(**tensors):
+    """Raise ValueError for the first given tensor (None passes) not on a CUDA device."""
+    for what, t in tensors.items():
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{what}: must be on a CUDA device")
+
+
+def _check_attn(q, k, v=None, o=None, lse=None, edges=None, dims=None):
+    """Q/O [B,Hq,n,d], K/V [B,Hkv,n,d] bf16, LSE [B,Hq,n] fp32, edges >= B*Hq int64.
+    dims: (B, Hq, Hkv, n, d) the tensors must have (a layer's shape), else taken from q and k."""
+    for t, what in ((q, "q"), (k, "k")):
+        if not isinstance(t, torch.Tensor) or t.dim() != 4:
+            raise ValueError(f"{what}: a 4-d tensor [B, H, n, d] is required")
+    if dims:
+        B, Hq, Hkv, n, d = dims
+    else:
+        B, Hq, n, d = q.shape
+        Hkv = k.shape[1]
+    dev = q.device
+    _want(q, "q", torch.bfloat16, (B, Hq, n, d), device=dev)
+    _want(k, "k", torch.bfloat16, (B, Hkv, n, d), device=dev)
+    _want(v, "v", torch.bfloat16, (B, Hkv, n, d), device=dev)
+    _want(o, "o", torch.bfloat16, (B, Hq, n, d), device=dev)
+    _want(lse, "lse", torch.float32, (B, Hq, n), device=dev)
+    _want(edges, "edges", torch.int64, min_numel=B * Hq, device=dev)
+    _cuda(q=q, k=k, v=v, o=o, lse=lse, edges=edges)
+
+
 # ----------------------------------------------------------------- attention
 def attn_ashape(q, k, v, heads, sink, window, o=None, lse=None, edges=None, scale=None, stream=None):
     """A-shape heads (sink g, window w); returns o."""
+    _check_attn(q, k, v, o, lse, edges)
     lib = load()
     o = _out_like(q, o)
     sh = make_shape(q, k, scale)
@@ -185,6 +234,7 @@ def attn_ashape(q, k, v, heads, sink, window, o=None, lse=None, edges=None, scal
 
 def attn_dense(q, k, v, heads, o=None, lse=None, edges=None, scale=None, stream=None):
     """Dense causal attention of the listed heads on the same engine; returns o."""
+    _check_attn(q, k, v, o, lse, edges)
     lib = load()
     o = _out_like(q, o)
     sh = make_shape(q, k, scale)
@@ -198,6 +248,7 @@ class VSIndex:
     """Device buffers of a Vertical-Slash index (see msa_vs_index in msa.h)."""
 
     def __init__(self, slots: int, n: int, n_vertical: int, n_slash: int, device):
+        self.slots, self.n = int(slots), int(n)
         self.v_cap = max(min(int(n_vertical), n), 0)
         self.s_cap = max(min(int(n_slash), n), 0)
         words = (n + 31) // 32
@@ -209,6 +260,13 @@ class VSIndex:
         self.slash_bits = torch.zeros(slots, words, dtype=torch.int32, device=device)
         self.slash_cover = torch.zeros(slots, (n + 63 + 31) // 32, dtype=torch.int32, device=device)
 
+    def check(self, slots: int, n: int, device=None):
+        """Raise ValueError unless the buffers hold `slots` slots of an n-token index (on `device`)."""
+        if self.n != n or self.slots < slots:
+            raise ValueError(f"VSIndex: {self.slots} slots for n = {self.n}, need {slots} for n = {n}")
+        if device is not None and self.vertical_bits.device != device:
+            raise ValueError(f"VSIndex: on {self.vertical_bits.device}, expected {device}")
+
     def c(self) -> VSIndexC:
         return VSIndexC(self.vertical.data_ptr(), self.vertical_cnt.data_ptr(), self.slash.data_ptr(),
                         self.slash_cnt.data_ptr(), self.vertical_bits.data_ptr(), self.slash_bits.data_ptr(),
@@ -218,6 +276,7 @@ class VSIndex:
     def from_c(c: VSIndexC, slots: int, n: int):
         """Non-owning view of an index that lives in a layer workspace."""
         ix = VSIndex.__new__(VSIndex)
+        ix.slots, ix.n = int(slots), int(n)
         ix.v_cap, ix.s_cap = c.v_cap, c.s_cap
         words = (n + 31) // 32
         ix.vertical = _view_i32(c.vertical, slots * max(c.v_cap, 1)).view(slots, max(c.v_cap, 1))
@@ -246,6 +305,8 @@ def _view_i32(ptr: int, count: int) -> torch.Tensor:
 
 
 def attn_vs(q, k, v, heads, index: VSIndex, o=None, lse=None, edges=None, scale=None, stream=None):
+    _check_attn(q, k, v, o, lse, edges)
+    index.check(q.shape[0] * len(heads), q.shape[2], q.device)
     lib = load()
     o = _out_like(q, o)
     sh = make_shape(q, k, scale)
@@ -257,6 +318,10 @@ def attn_vs(q, k, v, heads, index: VSIndex, o=None, lse=None, edges=None, scale=
 
 
 def attn_block(q, k, v, heads, topk, block_idx, block_cnt, o=None, lse=None, edges=None, scale=None, stream=None):
+    _check_attn(q, k, v, o, lse, edges)
+    B, nb = q.shape[0], (q.shape[2] + 63) // 64
+    _want(block_idx, "block_idx", torch.int32, (B, len(heads), nb, int(topk)), device=q.device)
+    _want(block_cnt, "block_cnt", torch.int32, (B, len(heads), nb), device=q.device)
     lib = load()
     o = _out_like(q, o)
     sh = make_shape(q, k, scale)
@@ -269,12 +334,16 @@ def attn_block(q, k, v, heads, topk, block_idx, block_cnt, o=None, lse=None, edg
 # ----------------------------------------------------------------- indices
 def build_vs_index(q, k, heads, last_q, n_vertical, n_slash, index: VSIndex | None = None, scale=None, stream=None,
                    proxy: int = 0):
+    _check_attn(q, k)
     lib = load()
     sh = make_shape(q, k, scale)
     hp, nh = _heads(heads)
     cfg = HeadCfg(VS, 0, 1, int(last_q), int(n_vertical), int(n_slash), 64, 1, int(proxy))
     if index is None:
         index = VSIndex(q.shape[0] * nh, q.shape[2], n_vertical, n_slash, q.device)
+    index.check(q.shape[0] * nh, q.shape[2], q.device)
+    if index.v_cap < min(int(n_vertical), q.shape[2]) or index.s_cap < min(int(n_slash), q.shape[2]):
+        raise ValueError("VSIndex: list capacity below the requested budgets")
     ws_bytes = lib.msa_vs_index_workspace(ctypes.byref(sh), ctypes.byref(cfg), nh)
     ws = torch.empty(max(int(ws_bytes), 1), dtype=torch.uint8, device=q.device)
     ic = index.c()
@@ -285,6 +354,7 @@ def build_vs_index(q, k, heads, last_q, n_vertical, n_slash, index: VSIndex | No
 
 
 def build_block_index(q, k, heads, topk, block_idx=None, block_cnt=None, scale=None, stream=None):
+    _check_attn(q, k)
     lib = load()
     sh = make_shape(q, k, scale)
     hp, nh = _heads(heads)
@@ -294,6 +364,8 @@ def build_block_index(q, k, heads, topk, block_idx=None, block_cnt=None, scale=N
         block_idx = torch.empty(B, nh, nb, int(topk), dtype=torch.int32, device=q.device)
     if block_cnt is None:
         block_cnt = torch.empty(B, nh, nb, dtype=torch.int32, device=q.device)
+    _want(block_idx, "block_idx", torch.int32, (B, nh, nb, int(topk)), device=q.device)
+    _want(block_cnt, "block_cnt", torch.int32, (B, nh, nb), device=q.device)
     ws_bytes = lib.msa_block_index_workspace(ctypes.byref(sh), 64, nh)
     ws = torch.empty(max(int(ws_bytes), 1), dtype=torch.uint8, device=q.device)
     _check(lib.msa_build_block_index(ctypes.byref(sh), _ptr(q), _ptr(k), hp, nh, 64, int(topk), _ptr(block_idx),
@@ -306,6 +378,7 @@ def build_block_index(q, k, heads, topk, block_idx=None, block_cnt=None, scale=N
 def build_block_index_static(q, k, heads, topk, block_idx=None, block_cnt=None, scale=None, stream=None):
     """msa_build_block_index_static: the Block-Sparse index built in the
     library's own scratch (no workspace); outputs as build_block_index."""
+    _check_attn(q, k)
     lib = load()
     sh = make_shape(q, k, scale)
     hp, nh = _heads(heads)
@@ -315,6 +388,8 @@ def build_block_index_static(q, k, heads, topk, block_idx=None, block_cnt=None, 
         block_idx = torch.empty(B, nh, nb, int(topk), dtype=torch.int32, device=q.device)
     if block_cnt is None:
         block_cnt = torch.empty(B, nh, nb, dtype=torch.int32, device=q.device)
+    _want(block_idx, "block_idx", torch.int32, (B, nh, nb, int(topk)), device=q.device)
+    _want(block_cnt, "block_cnt", torch.int32, (B, nh, nb), device=q.device)
     _check(lib.msa_build_block_index_static(ctypes.byref(sh), _ptr(q), _ptr(k), hp, nh, 64, int(topk),
                                             _ptr(block_idx), _ptr(block_cnt), _stream(stream)),
            "msa_build_block_index_static")
@@ -352,7 +427,12 @@ class Layer:
             raise MsaError(MSA_ERR_INVALID_ARG, "msa_layer_workspace")
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
 
+    def _dims(self):
+        s = self.shape
+        return (s.B, s.Hq, s.Hkv, s.n, s.d_h)
+
     def __call__(self, q, k, v, o=None, lse=None, edges=None, stream=None):
+        _check_attn(q, k, v, o, lse, edges, self._dims())
         lib = load()
         o = _out_like(q, o)
         _check(lib.msa_prefill_layer(ctypes.byref(self.shape), _ptr(q), _ptr(k), _ptr(v), self.tarr, _ptr(o), _ptr(lse),
@@ -361,11 +441,13 @@ class Layer:
 
     def index(self, q, k, stream=None):
         """First half of the layer (T_index): build every online index into the workspace."""
+        _check_attn(q, k, dims=self._dims())
         _check(load().msa_layer_index(ctypes.byref(self.shape), _ptr(q), _ptr(k), self.tarr, _ptr(self.ws),
                                       self.ws_bytes, _stream(stream)), "msa_layer_index")
 
     def attend(self, q, k, v, o, lse=None, edges=None, stream=None):
         """Second half (T_sparse): the single attention launch over the indices in the workspace."""
+        _check_attn(q, k, v, o, lse, edges, self._dims())
         _check(load().msa_layer_attend(ctypes.byref(self.shape), _ptr(q), _ptr(k), _ptr(v), self.tarr, _ptr(o),
                                        _ptr(lse), _ptr(edges), _ptr(self.ws), self.ws_bytes, _stream(stream)),
                "msa_layer_attend")
@@ -373,6 +455,7 @@ class Layer:
 
     def attend_rows(self, q, k, v, o, row_begin, row_end, lse=None, edges=None, stream=None):
         """Chunked T_sparse: the attention of query rows [row_begin, row_end) only (indices from index())."""
+        _check_attn(q, k, v, o, lse, edges, self._dims())
         _check(load().msa_layer_attend_rows(ctypes.byref(self.shape), _ptr(q), _ptr(k), _ptr(v), self.tarr, _ptr(o),
                                             _ptr(lse), _ptr(edges), _ptr(self.ws), self.ws_bytes, int(row_begin),
                                             int(row_end), _stream(stream)), "msa_layer_attend_rows")
@@ -418,6 +501,14 @@ def unpack_varlen(flat: torch.Tensor, H: int, cu_seqlens, d: int):
 def prefill_layer_varlen(q, k, v, table, cu_seqlens, Hq, Hkv, d, o=None, lse=None, edges=None, scale=None,
                          ws=None, stream=None):
     """msa_prefill_layer_varlen on packed buffers (see pack_varlen); returns o."""
+    total = int(cu_seqlens[-1]) if len(cu_seqlens) else 0
+    _want(q, "q", torch.bfloat16, min_numel=Hq * total * d)
+    _want(k, "k", torch.bfloat16, min_numel=Hkv * total * d, device=q.device)
+    _want(v, "v", torch.bfloat16, min_numel=Hkv * total * d, device=q.device)
+    _want(o, "o", torch.bfloat16, tuple(q.shape), device=q.device)
+    _want(lse, "lse", torch.float32, min_numel=Hq * total, device=q.device)
+    _want(edges, "edges", torch.int64, min_numel=(len(cu_seqlens) - 1) * Hq, device=q.device)
+    _cuda(q=q)
     lib = load()
     cu = (ctypes.c_int32 * len(cu_seqlens))(*[int(x) for x in cu_seqlens])
     shape = Shape(1, Hq, Hkv, max(1, max(int(cu_seqlens[s + 1]) - int(cu_seqlens[s]) for s in range(len(cu_seqlens) - 1))),
@@ -437,8 +528,15 @@ def prefill_layer_varlen(q, k, v, table, cu_seqlens, Hq, Hkv, d, o=None, lse=Non
 
 def merge_attention(o_a, lse_a, o_b, lse_b, o=None, lse=None, stream=None):
     """Combine two attention results over disjoint key sets (msa_merge_attention); returns (o, lse)."""
+    if not isinstance(o_a, torch.Tensor) or o_a.dim() < 1:
+        raise ValueError("o_a: a tensor [..., d] is required")
     d = o_a.shape[-1]
     rows = o_a.numel() // d
+    for t, what in ((o_a, "o_a"), (o_b, "o_b"), (o, "o")):
+        _want(t, what, torch.bfloat16, tuple(o_a.shape), device=o_a.device)
+    for t, what in ((lse_a, "lse_a"), (lse_b, "lse_b"), (lse, "lse")):
+        _want(t, what, torch.float32, tuple(o_a.shape[:-1]), device=o_a.device)
+    _cuda(o_a=o_a)
     o = torch.empty_like(o_a) if o is None else o
     lse = torch.empty_like(lse_a) if lse is None else lse
     _check(load().msa_merge_attention(rows, d, _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o), _ptr(lse),
@@ -449,6 +547,11 @@ def merge_attention(o_a, lse_a, o_b, lse_b, o=None, lse=None, stream=None):
 def captured_mass(lse_sparse, lse_dense, stream=None):
     """Per-head share of the dense softmax mass kept by the sparse sets (msa_captured_mass).
     lse_*: [..., n] with the leading dims flattened into heads; returns [heads] fp32."""
+    if not isinstance(lse_sparse, torch.Tensor) or lse_sparse.dim() < 1:
+        raise ValueError("lse_sparse: a tensor [..., n] is required")
+    _want(lse_sparse, "lse_sparse", torch.float32, device=lse_sparse.device)
+    _want(lse_dense, "lse_dense", torch.float32, tuple(lse_sparse.shape), device=lse_sparse.device)
+    _cuda(lse_sparse=lse_sparse)
     n = lse_sparse.shape[-1]
     heads = lse_sparse.numel() // n
     mass = torch.empty(heads, dtype=torch.float32, device=lse_sparse.device)

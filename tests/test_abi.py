@@ -117,3 +117,37 @@ def test_missing_library_fails_loudly(tmp_path):
             mod.load(str(tmp_path / "nope.so"))
     finally:
         mod._lib = saved
+
+
+def test_binding_validates_tensors():
+    """The binding refuses tensors whose dtype, shape, layout or device would
+    make the library read or write outside them (the C ABI sees pointers only);
+    the checks run before the library is called, so CPU tensors exercise them."""
+    import torch
+    bf = torch.bfloat16
+    q = torch.zeros(1, 2, 64, 128, dtype=bf)
+    k = torch.zeros(1, 1, 64, 128, dtype=bf)
+    cases = [
+        (lambda: msa.attn_ashape(q, k, torch.zeros(1, 1, 32, 128, dtype=bf), [0], 4, 16), "v: shape"),
+        (lambda: msa.attn_ashape(q, k, k, [0], 4, 16, o=torch.zeros(1, 2, 64, 128)), "o: dtype"),
+        (lambda: msa.attn_ashape(q, k, k, [0], 4, 16, o=torch.zeros(1, 2, 128, 64, dtype=bf).transpose(2, 3)),
+         "o: must be contiguous"),
+        (lambda: msa.attn_ashape(q, k, k, [0], 4, 16, lse=torch.zeros(1, 2, 63)), "lse: shape"),
+        (lambda: msa.attn_ashape(q, k, k, [0], 4, 16, edges=torch.zeros(1, dtype=torch.int64)), "edges: 1 elements"),
+        (lambda: msa.attn_ashape(q.float(), k, k, [0], 4, 16), "q: dtype"),
+        (lambda: msa.attn_ashape(q, k, k, [0], 4, 16), "q: must be on a CUDA device"),
+        (lambda: msa.attn_block(q, k, k, [0], 4, torch.zeros(1, 1, 1, 4, dtype=torch.int32),
+                                torch.zeros(1, 1, 1, dtype=torch.int32)), "q: must be on a CUDA device"),
+        (lambda: msa.merge_attention(torch.zeros(8, 128, dtype=bf), torch.zeros(8), torch.zeros(8, 64, dtype=bf),
+                                     torch.zeros(8)), "o_b: shape"),
+        (lambda: msa.captured_mass(torch.zeros(2, 64), torch.zeros(2, 65)), "lse_dense: shape"),
+        (lambda: msa.prefill_layer_varlen(torch.zeros(100, dtype=bf), k, k, [dict(pattern="ashape", sink=4, window=8)],
+                                          [0, 64], 2, 1, 128), "q: 100 elements"),
+    ]
+    for call, msg in cases:
+        with pytest.raises(ValueError, match=msg):
+            call()
+    ix = msa.VSIndex.__new__(msa.VSIndex)
+    ix.slots, ix.n = 1, 64
+    with pytest.raises(ValueError, match="VSIndex"):
+        ix.check(2, 64)

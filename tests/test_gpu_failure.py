@@ -53,11 +53,13 @@ def test_bad_block_index_reports_index_error(cuda_lib):
     bad[10, :3] = bad[10, :3][::-1].copy()  # descending: out of order
     o = torch.empty_like(q)
     lse = torch.empty(1, 2, n, device="cuda")
-    cuda_lib.attn_block(q, k, v, [0], topk, torch.from_numpy(bad[None]).cuda(), torch.from_numpy(C[None]).cuda(),
+    cuda_lib.attn_block(q, k, v, [0], topk, torch.from_numpy(bad[None, None]).cuda(),
+                        torch.from_numpy(C[None, None]).cuda(),
                         o=o, lse=lse)
     assert cuda_lib.poll_device_status() == MSA_ERR_INDEX
     assert cuda_lib.poll_device_status() == 0
-    cuda_lib.attn_block(q, k, v, [0], topk, torch.from_numpy(J[None]).cuda(), torch.from_numpy(C[None]).cuda(),
+    cuda_lib.attn_block(q, k, v, [0], topk, torch.from_numpy(J[None, None]).cuda(),
+                        torch.from_numpy(C[None, None]).cuda(),
                         o=o, lse=lse)
     assert cuda_lib.poll_device_status() == 0
     cfg = dict(pattern=oracle.BLOCK, block=64, topk=topk)
