@@ -273,32 +273,25 @@ class VSIndex:
                         self.slash_cover.data_ptr(), self.v_cap, self.s_cap)
 
     @staticmethod
-    def from_c(c: VSIndexC, slots: int, n: int):
-        """Non-owning view of an index that lives in a layer workspace."""
+    def from_c(c: VSIndexC, slots: int, n: int, ws: torch.Tensor):
+        """View of an index that lives in the layer workspace `ws` (the views keep it alive)."""
         ix = VSIndex.__new__(VSIndex)
         ix.slots, ix.n = int(slots), int(n)
         ix.v_cap, ix.s_cap = c.v_cap, c.s_cap
         words = (n + 31) // 32
-        ix.vertical = _view_i32(c.vertical, slots * max(c.v_cap, 1)).view(slots, max(c.v_cap, 1))
-        ix.vertical_cnt = _view_i32(c.vertical_cnt, slots)
-        ix.slash = _view_i32(c.slash, slots * max(c.s_cap, 1)).view(slots, max(c.s_cap, 1))
-        ix.slash_cnt = _view_i32(c.slash_cnt, slots)
-        ix.vertical_bits = _view_i32(c.vertical_bits, slots * words).view(slots, words)
-        ix.slash_bits = _view_i32(c.slash_bits, slots * words).view(slots, words)
+        ix.vertical = _view_i32(ws, c.vertical, slots * max(c.v_cap, 1)).view(slots, max(c.v_cap, 1))
+        ix.vertical_cnt = _view_i32(ws, c.vertical_cnt, slots)
+        ix.slash = _view_i32(ws, c.slash, slots * max(c.s_cap, 1)).view(slots, max(c.s_cap, 1))
+        ix.slash_cnt = _view_i32(ws, c.slash_cnt, slots)
+        ix.vertical_bits = _view_i32(ws, c.vertical_bits, slots * words).view(slots, words)
+        ix.slash_bits = _view_i32(ws, c.slash_bits, slots * words).view(slots, words)
         cw = (n + 63 + 31) // 32
-        ix.slash_cover = _view_i32(c.slash_cover, slots * cw).view(slots, cw)
+        ix.slash_cover = _view_i32(ws, c.slash_cover, slots * cw).view(slots, cw)
         return ix
 
 
-_views = {}
-
-
-def _view_i32(ptr: int, count: int) -> torch.Tensor:
-    """A torch int32 view of `count` elements at device address `ptr` (inside a live workspace)."""
-    key = (ptr, count)
-    base = _views.get("ws")
-    if base is None:
-        raise RuntimeError("no workspace registered for index views")
+def _view_i32(base: torch.Tensor, ptr: int, count: int) -> torch.Tensor:
+    """A torch int32 view of `count` elements at device address `ptr` inside the uint8 workspace `base`."""
     off = ptr - base.data_ptr()
     assert off % 4 == 0 and 0 <= off and off + 4 * count <= base.numel()
     return base[off:off + 4 * count].view(torch.int32)
@@ -469,17 +462,16 @@ class Layer:
         bc = ctypes.c_void_p()
         _check(lib.msa_layer_indices(ctypes.byref(self.shape), self.tarr, _ptr(self.ws), ctypes.byref(vc),
                                      ctypes.byref(bi), ctypes.byref(bc)), "msa_layer_indices")
-        _views["ws"] = self.ws
         B, n = self.shape.B, self.shape.n
         nvs = sum(1 for e in self.table if head_cfg(e).pattern == VS)
         nbs = [e for e in self.table if head_cfg(e).pattern == BLOCK]
-        vs = VSIndex.from_c(vc, B * nvs, n) if nvs else None
+        vs = VSIndex.from_c(vc, B * nvs, n, self.ws) if nvs else None
         blk = cnt = None
         if nbs:
             nb = (n + 63) // 64
             topk = head_cfg(nbs[0]).topk
-            blk = _view_i32(bi.value, B * len(nbs) * nb * topk).view(B, len(nbs), nb, topk)
-            cnt = _view_i32(bc.value, B * len(nbs) * nb).view(B, len(nbs), nb)
+            blk = _view_i32(self.ws, bi.value, B * len(nbs) * nb * topk).view(B, len(nbs), nb, topk)
+            cnt = _view_i32(self.ws, bc.value, B * len(nbs) * nb).view(B, len(nbs), nb)
         return vs, blk, cnt
 
 
