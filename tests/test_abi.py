@@ -151,3 +151,21 @@ def test_binding_validates_tensors():
     ix.slots, ix.n = 1, 64
     with pytest.raises(ValueError, match="VSIndex"):
         ix.check(2, 64)
+
+
+def test_empty_inputs_are_no_ops(lib):
+    """Valid calls with nothing to do return MSA_OK before touching the
+    device (so they run here without one): a merge of zero rows, the captured
+    mass of zero heads, and a varlen batch whose sequences are all empty."""
+    P = ctypes.c_void_p
+    a, b, la, lb = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
+    assert lib.msa_merge_attention(0, 128, a, la, b, lb, a, None, None) == msa.MSA_OK
+    assert lib.msa_captured_mass(0, 16, la, lb, P(0x50000), None) == msa.MSA_OK
+    table = msa.table_array([dict(pattern="ashape", sink=4, window=64),
+                             dict(pattern="vs", last_q=64, n_vertical=10, n_slash=20)])
+    cu = (ctypes.c_int32 * 3)(0, 0, 0)
+    sh = msa.Shape(1, 2, 1, 1, 128, 0.0)
+    need = lib.msa_layer_varlen_workspace(ctypes.byref(sh), table, cu, 2)
+    assert need > 0
+    assert lib.msa_prefill_layer_varlen(ctypes.byref(sh), cu, 2, a, a, a, table, a, None, None, a, need,
+                                        None) == msa.MSA_OK
