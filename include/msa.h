@@ -112,10 +112,11 @@ typedef struct {
   int32_t s_cap;
 } msa_vs_index;
 
-/* Status as text (static storage). */
+/* Status as text (static storage; no counterpart in the pages). */
 MSA_API const char* msa_status_string(msa_status s);
 
-/* Workspace bytes msa_build_vs_index needs for n_heads heads with budgets cfg
+/* Workspace sizing (no counterpart in the pages: the caller owns all memory).
+ * Workspace bytes msa_build_vs_index needs for n_heads heads with budgets cfg
  * (0 on invalid arguments). */
 MSA_API size_t msa_vs_index_workspace(const msa_shape* shape, const msa_head_cfg* cfg, int32_t n_heads);
 
@@ -301,10 +302,11 @@ MSA_API msa_status msa_layer_attend(const msa_shape* shape, const void* q, const
 MSA_API msa_status msa_check_wait_timeout(int32_t limit_ms, void* stream);
 
 /* Number of kernels this process has launched through the library so far
- * (all devices).  Lets a caller count the launches inside a region. */
+ * (all devices; no counterpart in the pages).  Lets a caller count the launches inside a region. */
 MSA_API uint64_t msa_kernel_launches(void);
 
-/* Pointers into a msa_prefill_layer workspace: where that call left the
+/* Inspection (no counterpart in the pages).  Pointers into a
+ * msa_prefill_layer workspace: where that call left the
  * Vertical-Slash index (slot = b * n_vs + rank of the head among the table's
  * VS heads) and the Block-Sparse index (likewise among BS heads).  Any
  * output pointer may be NULL.  Valid until the workspace is reused. */
@@ -323,8 +325,8 @@ MSA_API msa_status msa_vs_expand(const msa_shape* shape, const msa_vs_index* ind
                          int32_t u_count, int32_t range_cap, int32_t col_cap, int32_t* range_cnt,
                          int32_t* ranges, int32_t* col_cnt, int32_t* cols, void* stream);
 
-/* Synchronise `stream`, read and clear the device error word of the current
- * device.  Returns MSA_OK, MSA_ERR_DEVICE_TIMEOUT, MSA_ERR_INDEX or
+/* Failure detection (no counterpart in the pages).  Synchronise `stream`,
+ * read and clear the device error word of the current device.  Returns MSA_OK, MSA_ERR_DEVICE_TIMEOUT, MSA_ERR_INDEX or
  * MSA_ERR_CUDA. */
 MSA_API msa_status msa_poll_device_status(void* stream);
 
