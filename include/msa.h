@@ -163,15 +163,20 @@ MSA_API msa_status msa_build_block_index(const msa_shape* shape, const void* q, 
  * counterpart in the MInference pages; it exists for callers that hold device
  * tensors from another runtime and have no allocator of their own (or must not
  * call cudaMalloc on their path).
- * Limit: msa_block_index_workspace(shape, 64, n_heads) must not exceed
- * MSA_STATIC_SCRATCH_BYTES, else MSA_ERR_WORKSPACE_TOO_SMALL is returned and
- * nothing is launched (for d_h = 128 and one KV head per listed head: up
- * to 31 heads at n = 16384, 12 at n = 32768, 4 at n = 65536).
+ * Limit: the scratch these heads need must not exceed MSA_STATIC_SCRATCH_BYTES,
+ * else MSA_ERR_WORKSPACE_TOO_SMALL is returned and nothing is launched.  The
+ * need counts each KV head the listed heads read once, so it is at most
+ * msa_block_index_workspace(shape, 64, n_heads) (which assumes one KV head per
+ * listed head: for d_h = 128 up to 31 heads at n = 16384, 12 at n = 32768,
+ * 4 at n = 65536; with four query heads per KV head, 16 heads at n = 32768 fit).
  * The scratch is shared by all calls on a device: calls that overlap in time
  * (unordered streams, several host threads) race on it and must be ordered.
  * The first call on a device looks up the scratch address (a runtime call),
  * so make one call on each device before the work that must be free of
- * set-up calls.  Arguments and outputs as for msa_build_block_index. */
+ * set-up calls.  The looked-up address is cached per device ordinal and is
+ * not refreshed: after cudaDeviceReset in the same process, do not call this
+ * entry point on that device again.  Arguments and outputs as for
+ * msa_build_block_index. */
 MSA_API msa_status msa_build_block_index_static(const msa_shape* shape, const void* q, const void* k,
                                                 const int32_t* heads, int32_t n_heads, int32_t block, int32_t topk,
                                                 int32_t* block_idx, int32_t* block_cnt, void* stream);
@@ -270,17 +275,28 @@ MSA_API msa_status msa_layer_attend_rows(const msa_shape* shape, const void* q, 
  * lse likewise as [Hq, n_s] blocks at Hq * cu_seqlens[s]; edges: [n_seqs, Hq]
  * counters (ADDED to).  shape gives Hq, Hkv, d_h and scale for every sequence
  * (its B and n are ignored).  Every sequence runs as msa_prefill_layer with
- * B = 1 and n = n_s on its own segment, in order on `stream`, reusing `ws`:
- * its own online indices, its own attention, no key of another sequence.
- * Requires ws_bytes >= msa_layer_varlen_workspace(...).  Errors: invalid
- * cu_seqlens -> MSA_ERR_INVALID_ARG before anything is launched; otherwise
- * the first failing sequence's status (earlier sequences have been queued). */
+ * B = 1 and n = n_s on its own segment, in order on `stream`, in its own
+ * region of `ws`: its own online indices, its own attention, no key of another
+ * sequence.  Requires ws_bytes >= msa_layer_varlen_workspace(...) (the sum of
+ * the sequences' layer workspaces).  Errors: invalid cu_seqlens ->
+ * MSA_ERR_INVALID_ARG before anything is launched; otherwise the first
+ * failing sequence's status (earlier sequences have been queued). */
 MSA_API size_t msa_layer_varlen_workspace(const msa_shape* shape, const msa_head_cfg* table,
                                           const int32_t* cu_seqlens, int32_t n_seqs);
 MSA_API msa_status msa_prefill_layer_varlen(const msa_shape* shape, const int32_t* cu_seqlens, int32_t n_seqs,
                                             const void* q, const void* k, const void* v, const msa_head_cfg* table,
                                             void* o, float* lse, int64_t* edges, void* ws, size_t ws_bytes,
                                             void* stream);
+
+/* Inspection (no counterpart in the pages): msa_layer_indices for sequence
+ * `seq` of a msa_prefill_layer_varlen workspace (same shape, table and
+ * cu_seqlens): where that call left the sequence's Vertical-Slash index (slot
+ * = rank of the head among the table's VS heads) and Block-Sparse index
+ * ([n_bs, ceil(n_s/64), topk] and counts).  MSA_ERR_INVALID_ARG for an empty
+ * or out-of-range sequence.  Valid until the workspace is reused. */
+MSA_API msa_status msa_layer_varlen_indices(const msa_shape* shape, const msa_head_cfg* table,
+                                            const int32_t* cu_seqlens, int32_t n_seqs, void* ws, int32_t seq,
+                                            msa_vs_index* vs, int32_t** block_idx, int32_t** block_cnt);
 
 /* The two halves of msa_prefill_layer, in order (the time decomposition
  * T = T_index + T_sparse of the MInference page eq.(13)): msa_layer_index

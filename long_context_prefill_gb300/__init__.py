@@ -30,7 +30,7 @@ EXPORTS = ("msa_status_string", "msa_vs_index_workspace", "msa_block_index_works
            "msa_prefill_layer", "msa_layer_index", "msa_layer_attend", "msa_kernel_launches", "msa_layer_indices",
            "msa_vs_expand", "msa_poll_device_status", "msa_build_block_index_static",
            "msa_check_wait_timeout", "msa_attn_dense", "msa_layer_varlen_workspace", "msa_prefill_layer_varlen",
-           "msa_layer_attend_rows", "msa_merge_attention", "msa_captured_mass")
+           "msa_layer_attend_rows", "msa_merge_attention", "msa_captured_mass", "msa_layer_varlen_indices")
 
 
 class MsaError(RuntimeError):
@@ -110,6 +110,8 @@ def load(path: str = LIB_PATH):
             lib.msa_layer_varlen_workspace.argtypes = [P, P, P, i32]
             lib.msa_prefill_layer_varlen.restype = st
             lib.msa_prefill_layer_varlen.argtypes = [P, P, i32, P, P, P, P, P, P, P, P, sz, P]
+            lib.msa_layer_varlen_indices.restype = st
+            lib.msa_layer_varlen_indices.argtypes = [P, P, P, i32, P, i32, P, P, P]
             lib.msa_layer_attend_rows.restype = st
             lib.msa_layer_attend_rows.argtypes = [P, P, P, P, P, P, P, P, P, sz, i32, i32, P]
             lib.msa_merge_attention.restype = st
@@ -490,9 +492,59 @@ def unpack_varlen(flat: torch.Tensor, H: int, cu_seqlens, d: int):
     return out
 
 
-def prefill_layer_varlen(q, k, v, table, cu_seqlens, Hq, Hkv, d, o=None, lse=None, edges=None, scale=None,
-                         ws=None, stream=None):
-    """msa_prefill_layer_varlen on packed buffers (see pack_varlen); returns o."""
+class VarlenLayer:
+    """A varlen batch (cumulative lengths cu_seqlens) of one layer's table plus
+    its workspace; call() runs msa_prefill_layer_varlen on packed buffers (see
+    pack_varlen) and indices(seq) views what it left for one sequence."""
+
+    def __init__(self, table, cu_seqlens, Hq, Hkv, d, device, scale=None):
+        self.table = list(table)
+        if len(self.table) != int(Hq):
+            raise ValueError(f"table: {len(self.table)} entries, expected Hq = {int(Hq)}")
+        self.cu_list = [int(x) for x in cu_seqlens]
+        self.n_seqs = len(self.cu_list) - 1
+        self.cu = (ctypes.c_int32 * len(self.cu_list))(*self.cu_list)
+        lens = [self.cu_list[s + 1] - self.cu_list[s] for s in range(self.n_seqs)]
+        self.Hq, self.Hkv, self.d = int(Hq), int(Hkv), int(d)
+        self.shape = Shape(1, self.Hq, self.Hkv, max([1] + lens), self.d, float(scale) if scale else 0.0)
+        self.tarr = table_array(self.table)
+        lib = load()
+        self.ws_bytes = int(lib.msa_layer_varlen_workspace(ctypes.byref(self.shape), self.tarr, self.cu, self.n_seqs))
+        if self.ws_bytes == 0:
+            raise MsaError(MSA_ERR_INVALID_ARG, "msa_layer_varlen_workspace")
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, q, k, v, o=None, lse=None, edges=None, stream=None):
+        _check_varlen(q, k, v, o, lse, edges, self.cu_list, self.Hq, self.Hkv, self.d)
+        o = torch.empty_like(q) if o is None else o
+        _check(load().msa_prefill_layer_varlen(ctypes.byref(self.shape), self.cu, self.n_seqs, _ptr(q), _ptr(k),
+                                               _ptr(v), self.tarr, _ptr(o), _ptr(lse), _ptr(edges), _ptr(self.ws),
+                                               self.ws_bytes, _stream(stream)), "msa_prefill_layer_varlen")
+        return o
+
+    def indices(self, seq: int):
+        """(VSIndex view, block_idx [n_bs, N_b, topk], block_cnt [n_bs, N_b]) of sequence seq."""
+        lib = load()
+        vc = VSIndexC()
+        bi = ctypes.c_void_p()
+        bc = ctypes.c_void_p()
+        _check(lib.msa_layer_varlen_indices(ctypes.byref(self.shape), self.tarr, self.cu, self.n_seqs,
+                                            _ptr(self.ws), int(seq), ctypes.byref(vc), ctypes.byref(bi),
+                                            ctypes.byref(bc)), "msa_layer_varlen_indices")
+        n = self.cu_list[seq + 1] - self.cu_list[seq]
+        nvs = sum(1 for e in self.table if head_cfg(e).pattern == VS)
+        nbs = [e for e in self.table if head_cfg(e).pattern == BLOCK]
+        vs = VSIndex.from_c(vc, nvs, n, self.ws) if nvs else None
+        blk = cnt = None
+        if nbs:
+            nb = (n + 63) // 64
+            topk = head_cfg(nbs[0]).topk
+            blk = _view_i32(self.ws, bi.value, len(nbs) * nb * topk).view(len(nbs), nb, topk)
+            cnt = _view_i32(self.ws, bc.value, len(nbs) * nb).view(len(nbs), nb)
+        return vs, blk, cnt
+
+
+def _check_varlen(q, k, v, o, lse, edges, cu_seqlens, Hq, Hkv, d):
     total = int(cu_seqlens[-1]) if len(cu_seqlens) else 0
     _want(q, "q", torch.bfloat16, min_numel=Hq * total * d)
     _want(k, "k", torch.bfloat16, min_numel=Hkv * total * d, device=q.device)
@@ -501,21 +553,14 @@ def prefill_layer_varlen(q, k, v, table, cu_seqlens, Hq, Hkv, d, o=None, lse=Non
     _want(lse, "lse", torch.float32, min_numel=Hq * total, device=q.device)
     _want(edges, "edges", torch.int64, min_numel=(len(cu_seqlens) - 1) * Hq, device=q.device)
     _cuda(q=q)
-    lib = load()
-    cu = (ctypes.c_int32 * len(cu_seqlens))(*[int(x) for x in cu_seqlens])
-    shape = Shape(1, Hq, Hkv, max(1, max(int(cu_seqlens[s + 1]) - int(cu_seqlens[s]) for s in range(len(cu_seqlens) - 1))),
-                  d, float(scale) if scale else 0.0)
-    tarr = table_array(table)
-    need = int(lib.msa_layer_varlen_workspace(ctypes.byref(shape), tarr, cu, len(cu_seqlens) - 1))
-    if need == 0:
-        raise MsaError(MSA_ERR_INVALID_ARG, "msa_layer_varlen_workspace")
-    if ws is None or ws.numel() < need:
-        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
-    o = torch.empty_like(q) if o is None else o
-    _check(lib.msa_prefill_layer_varlen(ctypes.byref(shape), cu, len(cu_seqlens) - 1, _ptr(q), _ptr(k), _ptr(v), tarr,
-                                        _ptr(o), _ptr(lse), _ptr(edges), _ptr(ws), ws.numel(), _stream(stream)),
-           "msa_prefill_layer_varlen")
-    return o
+
+
+def prefill_layer_varlen(q, k, v, table, cu_seqlens, Hq, Hkv, d, o=None, lse=None, edges=None, scale=None,
+                         stream=None):
+    """msa_prefill_layer_varlen on packed buffers (see pack_varlen); returns o."""
+    _check_varlen(q, k, v, o, lse, edges, cu_seqlens, Hq, Hkv, d)
+    layer = VarlenLayer(table, cu_seqlens, Hq, Hkv, d, q.device, scale=scale)
+    return layer(q, k, v, o=o, lse=lse, edges=edges, stream=stream)
 
 
 def merge_attention(o_a, lse_a, o_b, lse_b, o=None, lse=None, stream=None):

@@ -505,14 +505,19 @@ msa_status run_bs(const msa_shape& s, const void* q, const void* k, const BSPlan
 }  // namespace
 
 size_t block_index_ws_bytes(const msa_shape& s, int32_t n_heads) { return plan_bs(s, nullptr, n_heads).total + 256; }
+size_t block_index_ws_bytes_exact(const msa_shape& s, const int32_t* heads, int32_t n_heads) {
+  return plan_bs(s, heads, n_heads).total + 256;
+}
 
 msa_status run_block_index(const msa_shape& s, const void* q, const void* k, const int32_t* heads,
                            int32_t n_heads, int32_t topk, int32_t* block_idx, int32_t* block_cnt, void* ws,
                            size_t ws_bytes, cudaStream_t stream) {
-  if (!ws || ws_bytes < block_index_ws_bytes(s, n_heads)) return MSA_ERR_WORKSPACE_TOO_SMALL;
   const int nb = ceil_div(s.n, 64);
   if ((int64_t)nb * (nb + 1) / 2 > ((int64_t)1 << 40)) return MSA_ERR_UNSUPPORTED;
   BSPlan P = plan_bs(s, heads, n_heads);
+  // the workspace query is the worst case (one KV head per listed head); what
+  // this call needs counts the KV heads the listed heads actually read
+  if (!ws || ws_bytes < P.total + 256) return MSA_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~(uintptr_t)255);
   if (s.d_h == 128) return run_bs<128>(s, q, k, P, topk, block_idx, block_cnt, w, stream);
   return run_bs<64>(s, q, k, P, topk, block_idx, block_cnt, w, stream);

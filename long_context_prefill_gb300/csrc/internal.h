@@ -103,6 +103,8 @@ msa_status run_block_index(const msa_shape& s, const void* q, const void* k, con
                            int32_t n_heads, int32_t topk, int32_t* block_idx, int32_t* block_cnt, void* ws,
                            size_t ws_bytes, cudaStream_t stream);
 size_t block_index_ws_bytes(const msa_shape& s, int32_t n_heads);
+// Bytes the listed heads need (their KV heads counted once; <= block_index_ws_bytes).
+size_t block_index_ws_bytes_exact(const msa_shape& s, const int32_t* heads, int32_t n_heads);
 
 inline int32_t ceil_div(int64_t a, int64_t b) { return (int32_t)((a + b - 1) / b); }
 

@@ -293,6 +293,15 @@ static msa_status check_cu_seqlens(const int32_t* cu, int32_t n_seqs) {
   return MSA_OK;
 }
 
+// Each sequence owns its own region of the workspace (sequence-major), so the
+// indices of every sequence are still there after the call.
+static size_t varlen_region(const msa_shape* shape, const msa_head_cfg* table, int32_t len) {
+  msa_shape ss = *shape;
+  ss.B = 1;
+  ss.n = len;
+  return (msa_layer_workspace(&ss, table) + 255) & ~(size_t)255;
+}
+
 size_t msa_layer_varlen_workspace(const msa_shape* shape, const msa_head_cfg* table, const int32_t* cu_seqlens,
                                   int32_t n_seqs) {
   if (!shape || !table || check_cu_seqlens(cu_seqlens, n_seqs) != MSA_OK) return 0;
@@ -300,12 +309,9 @@ size_t msa_layer_varlen_workspace(const msa_shape* shape, const msa_head_cfg* ta
   for (int32_t x = 0; x < n_seqs; ++x) {
     const int32_t len = cu_seqlens[x + 1] - cu_seqlens[x];
     if (len == 0) continue;
-    msa_shape ss = *shape;
-    ss.B = 1;
-    ss.n = len;
-    const size_t w = msa_layer_workspace(&ss, table);
+    const size_t w = varlen_region(shape, table, len);
     if (w == 0) return 0;
-    need = w > need ? w : need;
+    need += w;
   }
   return need;
 }
@@ -316,24 +322,49 @@ msa_status msa_prefill_layer_varlen(const msa_shape* shape, const int32_t* cu_se
   if (!shape || !q || !k || !v || !o || !table) return MSA_ERR_INVALID_ARG;
   msa_status st = check_cu_seqlens(cu_seqlens, n_seqs);
   if (st != MSA_OK) return st;
-  if (ws_bytes < msa_layer_varlen_workspace(shape, table, cu_seqlens, n_seqs)) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  const size_t need = msa_layer_varlen_workspace(shape, table, cu_seqlens, n_seqs);
+  if (need == 0) return MSA_ERR_INVALID_ARG;
+  if (ws_bytes < need || !ws) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~(uintptr_t)255);
   const int64_t hq = shape->Hq, hkv = shape->Hkv, d = shape->d_h;
+  size_t off = 0;
   for (int32_t x = 0; x < n_seqs; ++x) {
     const int32_t len = cu_seqlens[x + 1] - cu_seqlens[x];
     if (len == 0) continue;
     msa_shape ss = *shape;
     ss.B = 1;
     ss.n = len;
+    const size_t region = varlen_region(shape, table, len);
     const int64_t t0 = cu_seqlens[x];
     const char* qb = static_cast<const char*>(q) + hq * t0 * d * 2;
     const char* kb = static_cast<const char*>(k) + hkv * t0 * d * 2;
     const char* vb = static_cast<const char*>(v) + hkv * t0 * d * 2;
     char* ob = static_cast<char*>(o) + hq * t0 * d * 2;
     if ((st = msa_prefill_layer(&ss, qb, kb, vb, table, ob, lse ? lse + hq * t0 : nullptr,
-                                edges ? edges + (int64_t)x * hq : nullptr, ws, ws_bytes, stream)) != MSA_OK)
+                                edges ? edges + (int64_t)x * hq : nullptr, base + off, region, stream)) != MSA_OK)
       return st;
+    off += region;
   }
   return MSA_OK;
+}
+
+msa_status msa_layer_varlen_indices(const msa_shape* shape, const msa_head_cfg* table, const int32_t* cu_seqlens,
+                                    int32_t n_seqs, void* ws, int32_t seq, msa_vs_index* vs, int32_t** block_idx,
+                                    int32_t** block_cnt) {
+  if (!shape || !table || !ws) return MSA_ERR_INVALID_ARG;
+  msa_status st = check_cu_seqlens(cu_seqlens, n_seqs);
+  if (st != MSA_OK) return st;
+  if (seq < 0 || seq >= n_seqs || cu_seqlens[seq + 1] == cu_seqlens[seq]) return MSA_ERR_INVALID_ARG;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~(uintptr_t)255);
+  size_t off = 0;
+  for (int32_t x = 0; x < seq; ++x) {
+    const int32_t len = cu_seqlens[x + 1] - cu_seqlens[x];
+    if (len) off += varlen_region(shape, table, len);
+  }
+  msa_shape ss = *shape;
+  ss.B = 1;
+  ss.n = cu_seqlens[seq + 1] - cu_seqlens[seq];
+  return msa_layer_indices(&ss, table, base + off, vs, block_idx, block_cnt);
 }
 
 msa_status msa_layer_attend_rows(const msa_shape* shape, const void* q, const void* k, const void* v,

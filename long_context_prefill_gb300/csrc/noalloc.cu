@@ -27,7 +27,10 @@ static std::atomic<void*> g_scratch_addr[kMaxDevices];
 // Device address of the scratch on the current device, looked up once per
 // device (with that device current).  The first call on a device performs the
 // lookup, so it should come before any work a caller wants free of runtime
-// set-up calls.
+// set-up calls.  The cache is keyed by device ordinal only: after a
+// cudaDeviceReset (or any teardown of the device's primary context) in the
+// same process the cached address is stale, and this entry point must not be
+// called again on that device.
 static void* scratch_address() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -57,7 +60,8 @@ msa_status msa_build_block_index_static(const msa_shape* shape, const void* q, c
   if (!q || !k || !block_idx || !block_cnt) return MSA_ERR_INVALID_ARG;
   if (topk < 1) return MSA_ERR_INVALID_ARG;
   if (block != 64) return MSA_ERR_UNSUPPORTED;
-  const size_t need = block_index_ws_bytes(*shape, n_heads);
+  // what these heads need: each KV head they read is pooled once
+  const size_t need = block_index_ws_bytes_exact(*shape, heads, n_heads);
   if (need > (size_t)MSA_STATIC_SCRATCH_BYTES) return MSA_ERR_WORKSPACE_TOO_SMALL;
   void* ws = scratch_address();
   if (!ws) return MSA_ERR_CUDA;

@@ -1,4 +1,13 @@
-"""Shared test helpers: tolerances, oracle marshalling, bitmap packing."""
+"""Shared test helpers: tolerances, oracle marshalling, bitmap packing, and
+the index-set comparison rule.
+
+Index sets (a top-k of fp64 oracle scores against the device's fp32 scores):
+- where the oracle's k-th and (k+1)-th scores are separated by more than
+  MARGIN (relative), the structure is well separated and the sets must be
+  equal;
+- otherwise a member may differ only if its oracle score lies within REL
+  (relative) of the oracle's k-th score, for both the missing and the extra
+  member (fp32 device scores against fp64)."""
 import math
 
 import numpy as np
@@ -78,3 +87,57 @@ def oracle_cfg(entry: dict) -> dict:
 
 def scale_of(d):
     return 1.0 / math.sqrt(d)
+
+
+REL = 1e-4      # a differing member's oracle score must lie this close to the k-th score
+MARGIN = 1e-3   # k-th vs (k+1)-th gap above which the sets must be equal
+
+
+def topk_margin(scores, k: int) -> float:
+    """Relative gap between the k-th and (k+1)-th largest oracle scores
+    (inf when k takes every candidate or none)."""
+    s = np.asarray(scores, dtype=np.float64).reshape(-1)
+    if k <= 0 or k >= s.size:
+        return float("inf")
+    part = -np.partition(-s, (k - 1, k))
+    kth, nxt = part[k - 1], part[k]
+    if kth == nxt:
+        return 0.0
+    return float((kth - nxt) / abs(kth)) if kth != 0 else float("inf")
+
+
+def check_topk_set(got, want, scores, k: int, what: str) -> int:
+    """The index-set rule above; returns the number of differing members."""
+    got, want = set(int(x) for x in got), set(int(x) for x in want)
+    assert len(got) == len(want), f"{what}: {len(got)} vs {len(want)} members"
+    if got == want:
+        return 0
+    margin = topk_margin(scores, k)
+    assert margin <= MARGIN, f"{what}: sets differ although the oracle's top-{k} is separated by {margin:.2e}"
+    sc = np.asarray(scores, dtype=np.float64)
+    kth = min(sc[x] for x in want)
+    for x in got ^ want:
+        assert abs(sc[x] - kth) <= REL * abs(kth), f"{what}: member {x} score {sc[x]!r} vs k-th {kth!r}"
+    return len(got ^ want)
+
+
+def check_block_index(Jg, Cg, Jo, Co, qb, kb, topk: int, what: str) -> int:
+    """Every row of a Block-Sparse index against the oracle's: counts equal,
+    each row strictly ascending, ending with its own (diagonal) block, -1
+    padded; rows that differ follow the index-set rule on the block scores
+    Q̄_u . K̄_v (v < u; the diagonal is forced).  Returns the differing rows."""
+    Jg, Cg, Jo, Co = (np.asarray(x) for x in (Jg, Cg, Jo, Co))
+    nb = Jo.shape[0]
+    assert np.array_equal(Cg, Co), f"{what}: block counts"
+    cols = np.arange(Jg.shape[1])[None, :]
+    inside = cols < Cg[:, None]
+    assert np.all(Jg[~inside] == -1), f"{what}: padding"
+    steps = np.diff(Jg, axis=1) > 0
+    assert np.all(steps | ~inside[:, 1:]), f"{what}: rows not strictly ascending"
+    assert np.array_equal(Jg[np.arange(nb), Cg - 1], np.arange(nb)), f"{what}: diagonal block"
+    bad = np.nonzero(~np.all(Jg == Jo, axis=1))[0]
+    for u in bad:
+        sc = qb[u] @ kb[:u].T
+        check_topk_set([v for v in Jg[u, :Cg[u]] if v != u], [v for v in Jo[u, :Co[u]] if v != u], sc,
+                       min(topk - 1, int(u)), f"{what} u{u}")
+    return int(bad.size)

@@ -1,27 +1,41 @@
 """Parity at the benchmark's full sizes, through the same layer call bench.py
 times (msa_layer_index + msa_layer_attend on one workspace).
 
-At these sizes the oracle cannot evaluate every row, so for a few heads of
-each pattern it rebuilds the online index at full length (compared by the
-same rule as the small cases) and evaluates eq.(2) on seeded sampled query
-rows (always including rows 0, 63, 64 and n-1) over the GPU's own index sets;
-the per-head edge count E_h is compared exactly on the GPU's sets."""
+For EVERY head of each layer:
+- the online index against the oracle's, rebuilt at full length: the
+  Vertical-Slash lists C and D, and every row of the Block-Sparse J, under the
+  index-set rule (exact where the oracle's k-th and (k+1)-th scores are
+  separated by more than 1e-3, else the 1e-4 rule);
+- the edge count E_h exactly, computed by the oracle on the device's sets;
+- eq.(2) on seeded query rows over the device's own sets (rows 0, 63, 64 and
+  n-1 always included): 512 rows per head at 32K and 128K, 4096 per head at
+  1,048,576; on the mixed 32K layer every row of the first head of each
+  pattern.
+"""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
-from helpers import compare_rows, f32, head_qkv, oracle_cfg
-from test_gpu_index import check_set
+from helpers import check_block_index, check_topk_set, compare_rows, oracle_cfg
 
 pytestmark = pytest.mark.gpu
 
 
-def _check_layer(msa, name, n=None, heads_per_pattern=2, rows=40, check_edges=True):
-    w = synth.make_workload(name, device="cuda", n=n)
+def _host(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy()
+
+
+def _rows_of(t: torch.Tensor, rows: np.ndarray) -> np.ndarray:
+    return t[torch.as_tensor(rows, device=t.device)].float().cpu().numpy()
+
+
+def _check_layer(msa, name, rows_per_head, all_rows_first_of_pattern=False):
+    w = synth.make_workload(name, device="cuda")
     q, k, v, table, sh = w["q"], w["k"], w["v"], w["table"], w["shape"]
     B, Hq, Hkv, n, d = sh["B"], sh["Hq"], sh["Hkv"], sh["n"], sh["d"]
+    g = Hq // Hkv
     layer = msa.Layer(table, B, Hq, Hkv, n, d, q.device)
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, n, device=q.device)
@@ -32,14 +46,18 @@ def _check_layer(msa, name, n=None, heads_per_pattern=2, rows=40, check_edges=Tr
     vs, bidx, bcnt = layer.indices()
     vs_heads = [h for h, e in enumerate(table) if e["pattern"] == "vs"]
     bs_heads = [h for h, e in enumerate(table) if e["pattern"] == "block"]
-    picked = []
-    for pat in ("ashape", "vs", "block"):
-        hs = [h for h, e in enumerate(table) if e["pattern"] == pat]
-        picked += sorted({hs[0], hs[-1]})[:heads_per_pattern] if hs else []
-    sample = synth.sample_rows(n, rows, seed=n + 17)
-    for h in picked:
+    first = {}
+    for h, e in enumerate(table):
+        first.setdefault(e["pattern"], h)
+    diffs = {"vertical": 0, "slash": 0, "block rows": 0}
+    kv_cache = {}
+    for h in range(Hq):
         entry = table[h]
-        qn, kn, vn = head_qkv(q, k, v, 0, h, Hq, Hkv)
+        if h // g not in kv_cache:
+            kv_cache.clear()
+            kv_cache[h // g] = (_host(k[0, h // g]), _host(v[0, h // g]))
+        kn, vn = kv_cache[h // g]
+        qn = _host(q[0, h])
         cfg = oracle_cfg(entry)
         idx = {}
         if entry["pattern"] == "vs":
@@ -47,34 +65,40 @@ def _check_layer(msa, name, n=None, heads_per_pattern=2, rows=40, check_edges=Tr
             C = vs.vertical[slot, :int(vs.vertical_cnt[slot])].cpu().numpy()
             D = vs.slash[slot, :int(vs.slash_cnt[slot])].cpu().numpy()
             Co, Do, c, r = oracle.vs_index(qn, kn, entry["last_q"], entry["n_vertical"], entry["n_slash"], sh["scale"])
-            check_set(C, Co, c, f"{name} vertical h{h}")
-            check_set(D, Do, r, f"{name} slash h{h}")
+            diffs["vertical"] += check_topk_set(C, Co, c, min(entry["n_vertical"], n), f"{name} vertical h{h}")
+            diffs["slash"] += check_topk_set(D, Do, r, min(entry["n_slash"], n), f"{name} slash h{h}")
             idx = dict(C=C, D=D)
         elif entry["pattern"] == "block":
             x = bs_heads.index(h)
             J, cnt = bidx[0, x].cpu().numpy(), bcnt[0, x].cpu().numpy()
             Jo, co = oracle.bs_index(qn, kn, 64, entry["topk"])
-            assert np.array_equal(cnt, co), f"{name} block counts h{h}"
             qb, kb = oracle.bs_pool(qn, 64), oracle.bs_pool(kn, 64)
-            for u in np.random.default_rng(h).choice(len(cnt), size=min(64, len(cnt)), replace=False):
-                g = J[u, :cnt[u]]
-                assert np.all(np.diff(g) > 0) and g[-1] == u
-                sc = qb[u] @ kb[:u].T if u else np.zeros(0)
-                check_set([t for t in g if t != u], [t for t in Jo[u, :co[u]] if t != u], sc, f"{name} blocks h{h} u{u}")
+            diffs["block rows"] += check_block_index(J, cnt, Jo, co, qb, kb, entry["topk"], f"{name} blocks h{h}")
             idx = dict(J=J, cnt=cnt)
-        ro, rl, _ = oracle.head_rows(cfg, qn, kn, vn, sample, sh["scale"], **idx)
-        compare_rows(f32(o[0, h])[sample], f32(lse[0, h])[sample], ro, rl, f"{name} h{h} {entry['pattern']}")
-        if check_edges:
-            assert int(edges[h]) == oracle.head_edges(cfg, n, **idx), f"{name} edges h{h}"
+        if all_rows_first_of_pattern and first[entry["pattern"]] == h:
+            rows = np.arange(n, dtype=np.int64)
+        else:
+            rows = synth.sample_rows(n, rows_per_head, seed=n + 17 + h)
+        ro, rl, _ = oracle.head_rows(cfg, qn, kn, vn, rows, sh["scale"], **idx)
+        compare_rows(_rows_of(o[0, h], rows), _rows_of(lse[0, h], rows), ro, rl,
+                     f"{name} h{h} {entry['pattern']} ({rows.size} rows)")
+        assert int(edges[h]) == oracle.head_edges(cfg, n, **idx), f"{name} edges h{h}"
+    print(f"{name}: differing members within the 1e-4 rule: {diffs}")
 
 
 @pytest.mark.timeout(900)
-@pytest.mark.parametrize("name", ["mixed", "vs128k", "bs128k"])
-def test_bench_layers_full_size(cuda_lib, name):
-    _check_layer(cuda_lib, name)
+def test_mixed_layer_full_size(cuda_lib):
+    """Mixed 32K layer: every head, every row of the first head of each pattern."""
+    _check_layer(cuda_lib, "mixed", 512, all_rows_first_of_pattern=True)
 
 
-@pytest.mark.timeout(1500)
+@pytest.mark.timeout(900)
+@pytest.mark.parametrize("name", ["vs128k", "bs128k"])
+def test_128k_layers_full_size(cuda_lib, name):
+    _check_layer(cuda_lib, name, 512)
+
+
+@pytest.mark.timeout(1800)
 def test_million_token_layer(cuda_lib):
-    """The mixed table at n = 1,048,576: one head per pattern, sampled rows."""
-    _check_layer(cuda_lib, "million", heads_per_pattern=1, rows=12)
+    """The mixed table at n = 1,048,576: every head's full index and 4096 rows."""
+    _check_layer(cuda_lib, "million", 4096)

@@ -161,7 +161,7 @@ def test_captured_mass_of_ashape_heads(cuda_lib):
     rows = np.arange(n)
     for h, (g, w) in enumerate(cfgs):
         qn, kn, _ = head_qkv(q, k, v, 0, h, Hq, Hkv)
-        sets = [np.union1d(np.arange(min(g, i + 1)), np.arange(max(0, i - w + 1), i + 1)) for i in rows]
+        sets = [oracle.ashape_set(i, g, w) for i in rows]
         ref = oracle.captured_mass(qn, kn, rows, sets, scale_of(d))
         assert abs(float(mass[h]) - ref) < 2e-3, (h, float(mass[h]), ref)
     assert abs(float(mass[3]) - 1.0) < 1e-4

@@ -1,10 +1,14 @@
 """Varlen prefill (msa_prefill_layer_varlen): sequences of different lengths
-packed without padding, each with its own online indices and attention.
+packed without padding, each with its own online indices and attention
+(cost-model page §2.2: no window, index or tile reaches a neighbour's tokens).
 
 CPU: the host checks of cu_seqlens and the workspace rule (no launch).  GPU:
 every sequence's output, LSE and edge counts equal those of msa_prefill_layer
-run on that sequence alone (the same kernels, so bit for bit), and A-shape
-heads match the fp64 oracle directly."""
+run on that sequence alone (bit for bit), and every head of every packed
+sequence matches the fp64 oracle: its online index against the oracle's index
+of that sequence alone, its rows on the packed layout against eq.(2) over the
+device's sets, and its edge count exactly.  Chunked prefill (MInference page
+§5.2): each row chunk's attention against the oracle on the index built once."""
 import ctypes
 
 import numpy as np
@@ -14,7 +18,7 @@ import torch
 import long_context_prefill_gb300 as msa
 import oracle
 import synth
-from helpers import compare_rows, f32, oracle_cfg
+from helpers import check_block_index, check_topk_set, compare_rows, f32, oracle_cfg
 
 TABLE = [synth.ashape(16, 100), synth.vslash(64, 20, 50), synth.blocksparse(4), synth.vslash(64, 20, 50)]
 HQ, HKV, D = 4, 2, 128
@@ -50,11 +54,15 @@ def test_varlen_rejects_bad_cu_seqlens(lib, cu):
     assert st == msa.MSA_ERR_INVALID_ARG
 
 
-def test_varlen_workspace_is_the_largest_sequence(lib):
+def test_varlen_workspace_is_the_sum_of_the_sequences(lib):
+    """Each sequence owns a region of the workspace (so its indices survive the
+    call): the requirement is the sum of the sequences' layer workspaces,
+    each rounded up to 256 bytes, plus 256 for alignment."""
     cu = _cu(LENS)
     arr = (ctypes.c_int32 * len(cu))(*cu)
     tarr = msa.table_array(TABLE)
-    want = max(lib.msa_layer_workspace(ctypes.byref(msa.Shape(1, HQ, HKV, n, D, 0.0)), tarr) for n in LENS if n)
+    want = 256 + sum((lib.msa_layer_workspace(ctypes.byref(msa.Shape(1, HQ, HKV, n, D, 0.0)), tarr) + 255) // 256 * 256
+                     for n in LENS if n)
     assert lib.msa_layer_varlen_workspace(ctypes.byref(_shape()), tarr, arr, len(LENS)) == want
 
 
@@ -92,27 +100,81 @@ def test_varlen_equals_each_sequence_alone(cuda_lib):
         assert torch.equal(edges[s * HQ:(s + 1) * HQ], e1), f"sequence {s}: edges"
 
 
-@pytest.mark.gpu
-def test_varlen_ashape_heads_against_oracle(cuda_lib):
-    seqs = _sequences("cuda")
-    cu = _cu(LENS)
+def check_sequence_against_oracle(layer, s, n, q, k, v, outs, lses, edges, table, rows=None, what=""):
+    """Every head of packed sequence s against the oracle run on that sequence
+    alone (q, k, v: its [1, H, n, d] tensors)."""
+    vs, bidx, bcnt = layer.indices(s)
+    vs_heads = [h for h, e in enumerate(table) if e["pattern"] == "vs"]
+    bs_heads = [h for h, e in enumerate(table) if e["pattern"] == "block"]
+    g = HQ // HKV
+    rows = np.arange(n) if rows is None else rows
+    scale = D ** -0.5
+    for h, entry in enumerate(table):
+        qn, kn, vn = f32(q[0, h]), f32(k[0, h // g]), f32(v[0, h // g])
+        cfg = oracle_cfg(entry)
+        idx = {}
+        if entry["pattern"] == "vs":
+            x = vs_heads.index(h)
+            C = vs.vertical[x, :int(vs.vertical_cnt[x])].cpu().numpy()
+            Dl = vs.slash[x, :int(vs.slash_cnt[x])].cpu().numpy()
+            Co, Do, c, r = oracle.vs_index(qn, kn, entry["last_q"], entry["n_vertical"], entry["n_slash"], scale)
+            check_topk_set(C, Co, c, min(entry["n_vertical"], n), f"{what} seq {s} vertical h{h}")
+            check_topk_set(Dl, Do, r, min(entry["n_slash"], n), f"{what} seq {s} slash h{h}")
+            idx = dict(C=C, D=Dl)
+        elif entry["pattern"] == "block":
+            x = bs_heads.index(h)
+            J, cnt = bidx[x].cpu().numpy(), bcnt[x].cpu().numpy()
+            Jo, co = oracle.bs_index(qn, kn, 64, entry["topk"])
+            check_block_index(J, cnt, Jo, co, oracle.bs_pool(qn, 64), oracle.bs_pool(kn, 64), entry["topk"],
+                              f"{what} seq {s} blocks h{h}")
+            idx = dict(J=J, cnt=cnt)
+        ro, rl, _ = oracle.head_rows(cfg, qn, kn, vn, rows, scale, **idx)
+        compare_rows(f32(outs[s][h])[rows], f32(lses[s][h])[rows], ro, rl, f"{what} seq {s} h{h} {entry['pattern']}")
+        assert int(edges[s * HQ + h]) == oracle.head_edges(cfg, n, **idx), f"{what} seq {s} edges h{h}"
+
+
+def _run_varlen(cuda_lib, seqs, lens, table):
+    cu = _cu(lens)
     empty = torch.empty(0, dtype=torch.bfloat16, device="cuda")
     q = cuda_lib.pack_varlen([x[0][0] if x else empty for x in seqs])
     k = cuda_lib.pack_varlen([x[1][0] if x else empty for x in seqs])
     v = cuda_lib.pack_varlen([x[2][0] if x else empty for x in seqs])
     lse = torch.empty(HQ * cu[-1], device="cuda")
-    o = cuda_lib.prefill_layer_varlen(q, k, v, TABLE, cu, HQ, HKV, D, lse=lse)
+    edges = torch.zeros(len(lens) * HQ, dtype=torch.int64, device="cuda")
+    layer = cuda_lib.VarlenLayer(table, cu, HQ, HKV, D, "cuda")
+    o = layer(q, k, v, lse=lse, edges=edges)
     assert cuda_lib.poll_device_status() == 0
     outs = cuda_lib.unpack_varlen(o, HQ, cu, D)
-    cfg = oracle_cfg(TABLE[0])
+    lses = [lse[HQ * cu[s]:HQ * cu[s + 1]].view(HQ, -1) for s in range(len(lens))]
+    return layer, outs, lses, edges
+
+
+@pytest.mark.gpu
+def test_varlen_every_head_against_oracle(cuda_lib):
+    """All rows of every head of every sequence of the packed batch."""
+    seqs = _sequences("cuda")
+    layer, outs, lses, edges = _run_varlen(cuda_lib, seqs, LENS, TABLE)
     for s, n in enumerate(LENS):
-        if not n:
-            continue
-        qs, ks, vs = seqs[s]
-        rows = synth.sample_rows(n, 150, seed=n)
-        ro, rl, _ = oracle.head_rows(cfg, f32(qs[0, 0]), f32(ks[0, 0]), f32(vs[0, 0]), rows, D ** -0.5)
-        lh = lse[HQ * cu[s]:HQ * cu[s + 1]].view(HQ, n)
-        compare_rows(f32(outs[s][0])[rows], f32(lh[0])[rows], ro, rl, f"sequence {s} A-shape head")
+        if n:
+            check_sequence_against_oracle(layer, s, n, *seqs[s], outs, lses, edges, TABLE)
+
+
+@pytest.mark.gpu
+@pytest.mark.timeout(900)
+def test_varlen_many_sequences_against_oracle(cuda_lib):
+    """72 sequences of mixed lengths (empty, a single row, ragged tails, up to
+    5000 tokens): every head's index against the oracle and 96 seeded rows per
+    head and sequence (rows 0, 63, 64 and n-1 included)."""
+    rng = np.random.default_rng(4242)
+    lens = [int(x) for x in rng.integers(1, 5000, size=68)] + [0, 1, 64, 129]
+    rng.shuffle(lens)
+    seqs = [synth.random_qkv(1, HQ, HKV, n, D, seed=7000 + s, device="cuda") if n else None
+            for s, n in enumerate(lens)]
+    layer, outs, lses, edges = _run_varlen(cuda_lib, seqs, lens, TABLE)
+    for s, n in enumerate(lens):
+        if n:
+            check_sequence_against_oracle(layer, s, n, *seqs[s], outs, lses, edges, TABLE,
+                                          rows=synth.sample_rows(n, 96, seed=s), what="batch of 72")
 
 
 # ----------------------------------------------------------------- chunked rows
@@ -149,3 +211,49 @@ def test_chunked_rows_reproduce_the_whole_layer(cuda_lib):
         layer.attend_rows(q, k, v, o, lo, hi, lse=lse, edges=edges)
     assert cuda_lib.poll_device_status() == 0
     assert torch.equal(o, o_all) and torch.equal(lse, l_all) and torch.equal(edges, e_all)
+
+
+@pytest.mark.gpu
+def test_chunked_rows_against_oracle(cuda_lib):
+    """Chunked prefill: indices built once over the whole sequence, then the
+    attention run chunk by chunk (out of order); every row of every head of
+    each chunk equals eq.(2) over the once-built sets (fp64 oracle)."""
+    n, B = 1300, 2
+    q, k, v = synth.random_qkv(B, HQ, HKV, n, D, seed=903, device="cuda")
+    layer = cuda_lib.Layer(TABLE, B, HQ, HKV, n, D, "cuda")
+    layer.index(q, k)
+    o = torch.zeros_like(q)
+    lse = torch.empty(B, HQ, n, device="cuda")
+    edges = torch.zeros(B * HQ, dtype=torch.int64, device="cuda")
+    vs, bidx, bcnt = layer.indices()
+    vs_heads = [h for h, e in enumerate(TABLE) if e["pattern"] == "vs"]
+    bs_heads = [h for h, e in enumerate(TABLE) if e["pattern"] == "block"]
+    g = HQ // HKV
+    for lo, hi in [(768, n), (0, 256), (256, 768)]:
+        layer.attend_rows(q, k, v, o, lo, hi, lse=lse, edges=edges)
+        assert cuda_lib.poll_device_status() == 0
+        rows = np.arange(lo, hi)
+        for b in range(B):
+            for h, entry in enumerate(TABLE):
+                qn, kn, vn = f32(q[b, h]), f32(k[b, h // g]), f32(v[b, h // g])
+                idx = {}
+                if entry["pattern"] == "vs":
+                    x = b * len(vs_heads) + vs_heads.index(h)
+                    idx = dict(C=vs.vertical[x, :int(vs.vertical_cnt[x])].cpu().numpy(),
+                               D=vs.slash[x, :int(vs.slash_cnt[x])].cpu().numpy())
+                elif entry["pattern"] == "block":
+                    x = bs_heads.index(h)
+                    idx = dict(J=bidx[b, x].cpu().numpy(), cnt=bcnt[b, x].cpu().numpy())
+                ro, rl, _ = oracle.head_rows(oracle_cfg(entry), qn, kn, vn, rows, D ** -0.5, **idx)
+                compare_rows(f32(o[b, h])[rows], f32(lse[b, h])[rows], ro, rl, f"rows [{lo}, {hi}) b{b} h{h}")
+    for b in range(B):
+        for h, entry in enumerate(TABLE):
+            idx = {}
+            if entry["pattern"] == "vs":
+                x = b * len(vs_heads) + vs_heads.index(h)
+                idx = dict(C=vs.vertical[x, :int(vs.vertical_cnt[x])].cpu().numpy(),
+                           D=vs.slash[x, :int(vs.slash_cnt[x])].cpu().numpy())
+            elif entry["pattern"] == "block":
+                x = bs_heads.index(h)
+                idx = dict(J=bidx[b, x].cpu().numpy(), cnt=bcnt[b, x].cpu().numpy())
+            assert int(edges[b * HQ + h]) == oracle.head_edges(oracle_cfg(entry), n, **idx), f"edges b{b} h{h}"

@@ -24,6 +24,22 @@ def test_static_scratch_matches_workspace_path(cuda_lib, n, d, Hq, Hkv, heads, t
         assert torch.equal(J, J_ws)
 
 
+def test_static_scratch_counts_each_kv_head_once(cuda_lib):
+    """16 query heads reading 4 KV heads at n = 32768, d_h = 128: pooled once
+    per KV head the request needs about 15.5 MiB and fits, although the
+    worst-case workspace query (one KV head per listed head, about 20 MiB)
+    does not."""
+    q, k, _ = synth.random_qkv(1, 16, 4, 32768, 128, seed=77, device="cuda")
+    heads = list(range(16))
+    J_ws, C_ws = cuda_lib.build_block_index(q, k, heads, 16)
+    assert cuda_lib.poll_device_status() == 0
+    for _ in range(2):
+        J, C = cuda_lib.build_block_index_static(q, k, heads, 16)
+        assert cuda_lib.poll_device_status() == 0
+        assert torch.equal(C, C_ws)
+        assert torch.equal(J, J_ws)
+
+
 def test_static_scratch_rejects_oversize(cuda_lib):
     """A request whose scratch would exceed MSA_STATIC_SCRATCH_BYTES is refused
     on the host with MSA_ERR_WORKSPACE_TOO_SMALL (3) and launches nothing."""
