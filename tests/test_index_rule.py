@@ -64,3 +64,19 @@ def test_block_rows_equal_pass_and_broken_rows_fail():
     swapped[u, :cnt[u]] = np.sort(swapped[u, :cnt[u]])
     with pytest.raises(AssertionError):
         check_block_index(swapped, cnt, J, cnt, qb, kb, topk, "wrong member")
+
+
+def test_output_tolerance_allows_bf16_storage_rounding_only():
+    """compare_rows: a bf16 output may sit half a bf16 step from the exact
+    value on top of the arithmetic tolerance, and no more."""
+    from helpers import BF16_U, O_MAX_ABS, compare_rows
+    import torch
+    ref = np.full((1, 16), 0.5, dtype=np.float64)
+    ref[0, 0] = 4.0 + 0.0155                                     # rounds to 4.0 in bf16: error 0.0155
+    got = torch.tensor(ref).to(torch.bfloat16).double().numpy()
+    assert np.abs(got - ref).max() > O_MAX_ABS
+    compare_rows(got, None, ref, None, "bf16 rounding of 4.0155")
+    bad = ref.copy()
+    bad[0, 0] += O_MAX_ABS + BF16_U * abs(ref[0, 0]) + 1e-4
+    with pytest.raises(AssertionError, match="exceeds"):
+        compare_rows(bad, None, ref, None, "beyond the storage rounding")
