@@ -19,8 +19,8 @@
 //   slash_finalize  adds each diagonal's bins in a fixed order -> r
 //   topk_select   radix select (threshold), then an index-ordered compaction
 //                 that writes the sorted lists and the bitmaps
-// K is streamed once per pass per group of query heads sharing a KV head; the
-// second pass mostly hits L2.
+// K is streamed once per pass per group of query heads sharing a KV head (at
+// 128K the second pass reads it from DRAM again: K of all groups exceeds L2).
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -311,12 +311,23 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
             tmem_ld_wait();
             float xv[32];
             float mx = -INFINITY;
+            // every (row, key) of this chunk valid (warp-uniform): all 32 rows are
+            // proxy rows and every key lies at or before the chunk's first row
+            const bool chunk_valid = cc * 32 + 31 < A.L && kb0 + 31 <= n - A.L + cc * 32;
+            if (chunk_valid) {
 #pragma unroll
-            for (int tp = 0; tp < 32; ++tp) {
-              const int t = cc * 32 + tp;
-              const bool valid = t < A.L && key <= n - A.L + t && key < n;
-              xv[tp] = valid ? fmaf(__uint_as_float(sraw[tp]), c2, -sLse[r0 + tp]) : -INFINITY;
-              mx = fmaxf(mx, xv[tp]);
+              for (int tp = 0; tp < 32; ++tp) {
+                xv[tp] = fmaf(__uint_as_float(sraw[tp]), c2, -sLse[r0 + tp]);
+                mx = fmaxf(mx, xv[tp]);
+              }
+            } else {
+#pragma unroll
+              for (int tp = 0; tp < 32; ++tp) {
+                const int t = cc * 32 + tp;
+                const bool valid = t < A.L && key <= n - A.L + t && key < n;
+                xv[tp] = valid ? fmaf(__uint_as_float(sraw[tp]), c2, -sLse[r0 + tp]) : -INFINITY;
+                mx = fmaxf(mx, xv[tp]);
+              }
             }
             // column: running log-sum-exp over the head's rows
             const float nm = fmaxf(cm, mx);
@@ -344,12 +355,22 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
               if (b != -INFINITY) { bsum[cc + 1] *= ex2f(bm[cc + 1] - b); bm[cc + 1] = b; }
             }
             float hs = 0.f, ls = 0.f;
+            if (chunk_valid) {  // every term finite, so is every bin maximum
 #pragma unroll
-            for (int tp = 0; tp < 32; ++tp) {
-              const bool hi = lane + tp < 32;
-              const float e = vsh[tp] != -INFINITY ? ex2f(vsh[tp] - (hi ? bm[cc] : bm[cc + 1])) : 0.f;
-              if (hi) hs += e;
-              else ls += e;
+              for (int tp = 0; tp < 32; ++tp) {
+                const bool hi = lane + tp < 32;
+                const float e = ex2f(vsh[tp] - (hi ? bm[cc] : bm[cc + 1]));
+                if (hi) hs += e;
+                else ls += e;
+              }
+            } else {
+#pragma unroll
+              for (int tp = 0; tp < 32; ++tp) {
+                const bool hi = lane + tp < 32;
+                const float e = vsh[tp] != -INFINITY ? ex2f(vsh[tp] - (hi ? bm[cc] : bm[cc + 1])) : 0.f;
+                if (hi) hs += e;
+                else ls += e;
+              }
             }
             bsum[cc] += hs;
             bsum[cc + 1] += ls;
@@ -437,32 +458,6 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 constexpr int kTopkThreads = 512;
 constexpr int kTopkCluster = 8;  // CTAs per score vector
 
-__device__ int block_excl_scan(int v, int* sh, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sh[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
-      if (lane >= o) w += y;
-    }
-    sh[lane] = w;  // inclusive prefix of warp totals
-  }
-  __syncthreads();
-  const int before = (warp > 0 ? sh[warp - 1] : 0) + x - v;
-  total = sh[(blockDim.x >> 5) - 1];
-  __syncthreads();
-  return before;
-}
-
 struct TopkJob {
   const float* vals;
   int32_t* list;   // [cap]
@@ -504,31 +499,41 @@ __device__ __forceinline__ TopkJob topk_job(const TopkArgs& a, int n, int vec) {
 }
 
 // One cluster of kTopkCluster CTAs per score vector (cluster c: vector c, as
-// in topk_job); CTA r owns words [r cw, (r+1) cw) of the n values.
+// in topk_job); CTA r owns words [r cw, (r+1) cw) of the n values, and warp
+// w of a CTA a contiguous run of those words, so (CTA, warp, word, lane) is
+// index order.  Every pass reads the values with coalesced loads.
 //  1. the cluster's min and max order keys fix the bits all keys share;
 //  2. radix select, 8 bits per pass from the highest differing bit down: each
 //     CTA histograms its keys that match the prefix chosen so far (one
 //     histogram per warp, summed), the cluster adds the CTAs' histograms
-//     through distributed shared memory, and every CTA picks the same digit;
+//     through distributed shared memory, and every CTA picks
+//     the same digit.  When the chosen bin holds exactly the keys still needed,
+//     every key at or above it is taken and the search stops early; otherwise
 //     the k-th largest key T and the number `need` of keys equal to T to keep
 //     come out;
-//  3. each CTA counts its keys above T and equal to T; from the counts of the
-//     CTAs before it (index order) it knows where its selected keys go, and
-//     writes the bitmap words and the sorted list (ties: lower index first).
-__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
+//  3. each warp counts its keys above / equal to T with ballots; from the
+//     counts of the warps and CTAs before it (index order) it knows where its
+//     selected keys go, and writes the bitmap words and the sorted list (ties:
+//     lower index first).
+constexpr int kDigitBits = 8;
+constexpr int kBins = 1 << kDigitBits;
+constexpr int kTopkWarps = kTopkThreads / 32;
+static_assert(kBins <= kTopkThreads && kBins % 32 == 0, "one bin per thread");
+
+__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, 2)
     topk_kernel(const TopkArgs args, int n) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const TopkJob J = topk_job(args, n, (int)(blockIdx.x / kTopkCluster));
-  __shared__ int whist[kTopkThreads / 32][256];
-  __shared__ int chist[256];     // this CTA's histogram of the current pass (read cluster-wide)
-  __shared__ int ghist[256];     // the cluster's histogram
-  __shared__ uint32_t s_mm[2];   // this CTA's min / max key (read cluster-wide)
-  __shared__ int s_cnt[2];       // this CTA's keys above / equal to T (read cluster-wide)
-  __shared__ int sh[32];
+  __shared__ int whist[kTopkWarps][kBins];  // per-warp histograms of the current pass
+  __shared__ int hist[kBins];        // this CTA's histogram of the current pass (read cluster-wide)
+  __shared__ int ghist[kBins];       // the cluster's histogram
+  __shared__ uint32_t s_mm[2];       // this CTA's min / max key (read cluster-wide)
+  __shared__ int s_cnt[2];           // this CTA's keys above / equal to T (read cluster-wide)
+  __shared__ int wcnt[kTopkWarps][2];
   __shared__ uint32_t s_u[2];
-  __shared__ int s_i[2];
+  __shared__ int s_i[3];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int words = (n + 31) / 32;
   const int cw = (words + kTopkCluster - 1) / kTopkCluster;
@@ -548,11 +553,11 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     }
     mn = __reduce_min_sync(0xFFFFFFFFu, mn);
     mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-    if (lane == 0) { whist[warp][0] = (int)mn; whist[warp][1] = (int)mx; }
+    if (lane == 0) { wcnt[warp][0] = (int)mn; wcnt[warp][1] = (int)mx; }
     __syncthreads();
     if (warp == 0) {
       uint32_t a = 0xFFFFFFFFu, b = 0u;
-      if (lane < kTopkThreads / 32) { a = (uint32_t)whist[lane][0]; b = (uint32_t)whist[lane][1]; }
+      if (lane < kTopkWarps) { a = (uint32_t)wcnt[lane][0]; b = (uint32_t)wcnt[lane][1]; }
       a = __reduce_min_sync(0xFFFFFFFFu, a);
       b = __reduce_max_sync(0xFFFFFFFFu, b);
       if (lane == 0) { s_mm[0] = a; s_mm[1] = b; }
@@ -578,35 +583,36 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
       int lo = 32 - __clz(gmin ^ gmax);  // bits [0, lo) still open
       uint32_t pmask = lo == 32 ? 0u : ~((1u << lo) - 1u);
       uint32_t prefix = gmin & pmask;
+      bool exact = false;
       while (lo > 0) {
-        const int width = lo < 8 ? lo : 8, sft = lo - width;
+        const int width = lo < kDigitBits ? lo : kDigitBits, sft = lo - width;
         const uint32_t dmask = (1u << width) - 1u;
-        for (int b = lane; b < 256; b += 32) whist[warp][b] = 0;
-        __syncthreads();
+        for (int b = lane; b < kBins; b += 32) whist[warp][b] = 0;
+        __syncwarp();
         for (int x = x0 + tid; x < x1; x += kTopkThreads) {
           const uint32_t key = order_key(J.vals[x]);
           if ((key & pmask) == prefix) atomicAdd(&whist[warp][(key >> sft) & dmask], 1);
         }
         __syncthreads();
-        if (tid < 256) {
+        if (tid < kBins) {
           int v = 0;
 #pragma unroll
-          for (int w = 0; w < kTopkThreads / 32; ++w) v += whist[w][tid];
-          chist[tid] = v;
+          for (int w = 0; w < kTopkWarps; ++w) v += whist[w][tid];
+          hist[tid] = v;
         }
-        cluster.sync();
-        if (tid < 256) {
+        cluster.sync();  // every CTA's histogram is complete
+        if (tid < kBins) {
           int v = 0;
 #pragma unroll
-          for (int r = 0; r < kTopkCluster; ++r) v += cluster.map_shared_rank(chist, r)[tid];
+          for (int r = 0; r < kTopkCluster; ++r) v += cluster.map_shared_rank(hist, r)[tid];
           ghist[tid] = v;
         }
         __syncthreads();
         if (warp == 0) {
-          // digit of the need-th largest: suffix sums, 8 bins per lane (higher lanes hold higher bins)
+          // digit of the need-th largest: suffix sums, kBins / 32 bins per lane (higher lanes hold higher bins)
+          constexpr int kPer = kBins / 32;
           int mine = 0;
-#pragma unroll
-          for (int b = 0; b < 8; ++b) mine += ghist[8 * lane + b];
+          for (int b = 0; b < kPer; ++b) mine += ghist[kPer * lane + b];
           int suf = mine;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
@@ -617,14 +623,15 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
           const unsigned who = __ballot_sync(0xFFFFFFFFu, excl < need && suf >= need);
           const int src = __ffs(who) - 1;
           if (lane == src) {
-            int cum = excl, d = 8 * lane;
-            for (int b = 7; b >= 0; --b) {
-              const int c = ghist[8 * lane + b];
-              if (cum + c >= need) { d = 8 * lane + b; break; }
+            int cum = excl, d = kPer * lane;
+            for (int b = kPer - 1; b >= 0; --b) {
+              const int c = ghist[kPer * lane + b];
+              if (cum + c >= need) { d = kPer * lane + b; break; }
               cum += c;
             }
             s_i[0] = d;
             s_i[1] = cum;
+            s_i[2] = ghist[d];
           }
         }
         cluster.sync();  // every CTA has read the histograms of this pass
@@ -632,75 +639,83 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
         prefix |= (uint32_t)s_i[0] << sft;
         pmask |= dmask << sft;
         lo = sft;
+        if (s_i[2] == need && prefix != 0u) {  // the whole bin is taken: every key >= prefix
+          exact = true;
+          break;
+        }
       }
-      T = prefix;
+      if (exact) {
+        T = prefix - 1u;
+        need = 0;
+      } else {
+        T = prefix;
+      }
     }
   }
-  // ---- 3. counts, then placement in index order
-  auto word_bits = [&](int w, uint32_t& gt, uint32_t& eq) {
-    gt = eq = 0u;
-    for (int b = 0; b < 32; ++b) {
-      const int x = 32 * w + b;
-      if (x >= n) break;
-      const uint32_t key = order_key(J.vals[x]);
-      if (all || (!none && key > T)) gt |= 1u << b;
-      else if (!none && key == T) eq |= 1u << b;
+  // ---- 3. counts, then placement in index order (warp w: words [ww0, ww1))
+  const int pw = (w1 - w0 + kTopkWarps - 1) / kTopkWarps;
+  const int ww0 = min(w1, w0 + warp * pw), ww1 = min(w1, ww0 + pw);
+  auto word_masks = [&](int wi, unsigned& gt, unsigned& eq) {
+    const int x = 32 * wi + lane;
+    bool g = false, e = false;
+    if (x < n) {
+      if (all) {
+        g = true;
+      } else if (!none) {
+        const uint32_t key = order_key(J.vals[x]);
+        g = key > T;
+        e = key == T;
+      }
     }
+    gt = __ballot_sync(0xFFFFFFFFu, g);
+    eq = __ballot_sync(0xFFFFFFFFu, e);
   };
-  int cnt_gt = 0, cnt_eq = 0;
-  for (int w = w0 + tid; w < w1; w += kTopkThreads) {
-    uint32_t gt, eq;
-    word_bits(w, gt, eq);
-    cnt_gt += __popc(gt);
-    cnt_eq += __popc(eq);
+  int cgt = 0, ceq = 0;
+  for (int wi = ww0; wi < ww1; ++wi) {
+    unsigned gt, eq;
+    word_masks(wi, gt, eq);
+    cgt += __popc(gt);
+    ceq += __popc(eq);
   }
-  {
-    int tg, te;
-    block_excl_scan(cnt_gt, sh, tg);
-    block_excl_scan(cnt_eq, sh, te);
-    if (tid == 0) { s_cnt[0] = tg; s_cnt[1] = te; }
+  if (lane == 0) { wcnt[warp][0] = cgt; wcnt[warp][1] = ceq; }
+  __syncthreads();
+  if (tid == 0) {
+    int tg = 0, te = 0;
+    for (int w = 0; w < kTopkWarps; ++w) { tg += wcnt[w][0]; te += wcnt[w][1]; }
+    s_cnt[0] = tg;
+    s_cnt[1] = te;
   }
   cluster.sync();
-  int base_sel = 0, base_eq = 0, total_sel = 0, eq_run = 0;  // eq_run: equal keys of the CTAs before r
+  int gt_before = 0, eq_before = 0, total_gt = 0, total_eq = 0;
   for (int r = 0; r < kTopkCluster; ++r) {
     const int* c = cluster.map_shared_rank(s_cnt, r);
-    const int g = c[0], e = c[1];
-    const int take = min(max(need - eq_run, 0), e);
-    if (r == rank) { base_sel = total_sel; base_eq = eq_run; }
-    total_sel += g + take;
-    eq_run += e;
+    if (r < rank) { gt_before += c[0]; eq_before += c[1]; }
+    total_gt += c[0];
+    total_eq += c[1];
   }
   cluster.sync();  // the counts have been read: no CTA may exit before that
-  for (int wb = w0; wb < w1; wb += kTopkThreads) {
-    const int w = wb + tid;
-    uint32_t gt = 0u, eq = 0u;
-    if (w < w1) word_bits(w, gt, eq);
-    int eq_total;
-    const int eq_before = block_excl_scan(__popc(eq), sh, eq_total) + base_eq;
-    uint32_t take = 0u;
-    int rk = eq_before;
-    for (int b = 0; b < 32; ++b)
-      if ((eq >> b) & 1u) {
-        if (rk < need) take |= 1u << b;
-        ++rk;
-      }
-    const uint32_t sel = gt | take;
-    int sel_total;
-    const int pos = block_excl_scan(__popc(sel), sh, sel_total) + base_sel;
-    if (w < w1) {
-      J.bits[w] = sel;
-      int p = pos;
-      for (int b = 0; b < 32; ++b)
-        if ((sel >> b) & 1u) {
-          const int outp = J.descending ? (k - 1 - p) : p;
-          if (outp >= 0 && outp < k) J.list[outp] = 32 * w + b;
-          ++p;
-        }
+  for (int w = 0; w < warp; ++w) { gt_before += wcnt[w][0]; eq_before += wcnt[w][1]; }
+  const unsigned lt = (1u << lane) - 1u;
+  for (int wi = ww0; wi < ww1; ++wi) {
+    unsigned gt, eq;
+    word_masks(wi, gt, eq);
+    // selected: every key above T, and the keys equal to T of rank < need
+    const int eq_rank = eq_before + __popc(eq & lt);
+    const bool take = ((gt >> lane) & 1u) || (((eq >> lane) & 1u) && eq_rank < need);
+    const unsigned sel = __ballot_sync(0xFFFFFFFFu, take);
+    if (take) {
+      const int pos = gt_before + __popc(gt & lt) + min(eq_rank, need);
+      const int outp = J.descending ? (k - 1 - pos) : pos;
+      if (outp >= 0 && outp < k) J.list[outp] = 32 * wi + lane;
     }
-    base_sel += sel_total;
-    base_eq += eq_total;
+    if (lane == 0) J.bits[wi] = sel;
+    gt_before += __popc(gt);
+    eq_before += __popc(eq);
   }
-  if (rank == 0 && tid == 0) *J.cnt = total_sel < k ? total_sel : k;
+  if (rank == 0 && tid == 0) {
+    const int total = total_gt + min(total_eq, need);
+    *J.cnt = total < k ? total : k;
+  }
 }
 
 // Dilated slash coverage: bit z = any offset of D in [n-1-z, n+62-z], z < n+63.
