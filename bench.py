@@ -165,6 +165,18 @@ def algorithmic_index_bytes(w) -> int:
     return total
 
 
+def logical_edges(n: int, C, D) -> int:
+    """Edge count of eq.(5)'s logical Vertical-Slash sets over all rows,
+    Σ_i |{j in C : j <= i} ∪ {i - δ : δ in D, δ <= i}|: each column c is
+    attended by the n - c rows i >= c, each offset δ by the n - δ rows i >= δ,
+    and a pair (c, δ) with c + δ <= n - 1 names the same (row, key) twice."""
+    C = np.unique(np.asarray(C, dtype=np.int64))
+    D = np.unique(np.asarray(D, dtype=np.int64))
+    C, D = C[(C >= 0) & (C < n)], D[(D >= 0) & (D < n)]
+    both = int(np.searchsorted(D, n - 1 - C, side="right").sum())
+    return int((n - C).sum() + (n - D).sum() - both)
+
+
 class LayerRun:
     def __init__(self, name, device, msa, synth, n=None):
         self.name = name
@@ -174,11 +186,31 @@ class LayerRun:
         self.layer = msa.Layer(self.w["table"], sh["B"], sh["Hq"], sh["Hkv"], sh["n"], sh["d"], device)
         self.o = torch.empty_like(self.w["q"])
         self.lse = torch.empty(sh["B"], sh["Hq"], sh["n"], device=device)
+        # untimed counting pass: attended edges E_h and 64-row x 128-key tiles per head
         edges = torch.zeros(sh["B"] * sh["Hq"], dtype=torch.int64, device=device)
-        self.layer(self.w["q"], self.w["k"], self.w["v"], o=self.o, lse=self.lse, edges=edges)
+        tiles = torch.zeros(sh["B"] * sh["Hq"], dtype=torch.int64, device=device)
+        self.layer.index(self.w["q"], self.w["k"])
+        self.layer.attend_stats(self.w["q"], self.w["k"], self.w["v"], self.o, lse=self.lse, edges=edges, tiles=tiles)
         torch.cuda.synchronize()
         self.edges = edges.cpu().numpy()
+        self.tiles = tiles.cpu().numpy()
         self.flops = float(4.0 * self.edges.sum() * sh["d"])
+        # Vertical-Slash heads: physical edges (the tile-expanded sets attended) against eq.(5)'s logical sets
+        table = self.w["table"]
+        vs_heads = [h for h, e in enumerate(table) if e["pattern"] == "vs"]
+        self.vs_edges = None
+        if vs_heads:
+            vs, _, _ = self.layer.indices()
+            logical = 0
+            for b in range(sh["B"]):
+                for x, h in enumerate(vs_heads):
+                    slot = b * len(vs_heads) + x
+                    C = vs.vertical[slot, :int(vs.vertical_cnt[slot])].cpu().numpy()
+                    D = vs.slash[slot, :int(vs.slash_cnt[slot])].cpu().numpy()
+                    logical += logical_edges(sh["n"], C, D)
+            phys = int(sum(self.edges[b * sh["Hq"] + h] for b in range(sh["B"]) for h in vs_heads))
+            self.vs_edges = {"heads": len(vs_heads) * sh["B"], "physical": phys, "logical": logical,
+                             "physical_over_logical": round(phys / max(logical, 1), 4)}
         self.index_bytes = algorithmic_index_bytes(self.w)
         self.bytes_in = sum(t.numel() * t.element_size() for t in (self.w["q"], self.w["k"], self.w["v"]))
         self.bytes_out = self.o.numel() * self.o.element_size()
@@ -369,6 +401,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-baseline and cold-L2 measurements")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the per-config lines outside the step (A-shape-only 128K layer, 1M-token layer)")
     ap.add_argument("--n", type=int, default=None,
                     help="override the sequence length (scaled-down runs for profiling; not a headline number)")
     ap.add_argument("--curve", choices=["crossover", "lastq", "proxy"], default=None,
@@ -447,20 +481,30 @@ def main():
             "index_gbs": round(r.index_bytes / (idx_ms * 1e-3) / 1e9, 1) if idx_ms > 0 else None,
             "index_bytes": r.index_bytes,
             "density": round(float(r.edges.sum()) / (r.sh["Hq"] * r.sh["n"] * (r.sh["n"] + 1) / 2), 4),
+            "tiles_64x128": int(r.tiles.sum()),
+            "tile_fill": round(float(r.edges.sum()) / max(float(r.tiles.sum()) * 64 * 128, 1.0), 4),
         }
+        if r.vs_edges:
+            per_layer[r.name]["vs_edges"] = r.vs_edges
     if not args.no_dense:
         dense_and_cold(runs, msa, per_layer, stream)
     pk, pk_src = peaks()
     achieved = attn_flops_sum / (attn_ms_sum * 1e-3) / 1e12
-    peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    burst = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    clocks = clk.summary()
+    # the burst peak unless the clock record shows the power cap throttling the timed region
+    capped = bool(clocks) and "sw_power_cap" in clocks.get("reasons", [])
+    peak = sustained if capped else burst
     traffic, traffic_per = attention_traffic([r.name for r in runs], args.n)
     roofline = {"bound": "tensor", "kernel": "sparse_attn_kernel", "achieved": round(achieved, 2), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "traffic_note": "DRAM bytes (read + write) of the attention launches of one step, one per layer, from "
                                 "the committed ncu capture; null once the kernel source differs from the captured one",
                 "traffic_per_launch": traffic_per,
-                "peak_source": f"{pk_src} bf16 sustained (kernel timed inside a long step)",
-                "frac_of_burst": round(achieved / float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])), 4),
+                "peak_source": (f"{pk_src} bf16 " + ("sustained (the clock record shows sw_power_cap)" if capped else
+                                                     "burst (no power cap in the clock record of the timed region)")),
+                "frac_of_burst": round(achieved / burst, 4), "frac_of_sustained": round(achieved / sustained, 4),
                 "flops_per_launch": {r.name: r.flops for r in runs},
                 "launch_ms": {r.name: per_layer[r.name]["t_sparse_ms"] for r in runs}}
     idx_bytes = sum(r.index_bytes for r in runs)
@@ -480,8 +524,10 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "index_gbs_total": round(idx_bytes / (idx_ms * 1e-3) / 1e9, 1),
                    "index_frac_of_hbm": round(idx_bytes / (idx_ms * 1e-3) / 1e9 / float(pk.get("hbm_gbs", 6800.0)), 4)},
-        "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk.summary(),
+        "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
     }
+    if not args.no_extra and args.n is None:
+        line["extra_layers"] = extra_layers(msa, synth, device, stream)
     if rank == 0 and world == 1 and not args.no_cpu:
         v, secs, fl, desc = oracle_sample(runs)
         import oracle
@@ -489,6 +535,47 @@ def main():
                                 "sample": desc, "seconds": round(secs, 2)}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def extra_layers(msa, synth, device, stream, names=("ashape128k", "million"), reps=3):
+    """Per-config figures outside the headline step (their own runs, after it):
+    the A-shape pattern alone at n = 131072 and the mixed table at n =
+    1,048,576 (the MInference page §5.2 million-token bucket).  Each layer is
+    timed over `reps` calls after one warm-up; inputs exceed L2."""
+    out = {}
+    for nm in names:
+        r = LayerRun(nm, device, msa, synth)
+        r.index()
+        r.attend()
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        idx, att = [], []
+        for _ in range(reps):
+            a.record(stream)
+            r.index()
+            b.record(stream)
+            r.attend()
+            c.record(stream)
+            torch.cuda.synchronize()
+            idx.append(a.elapsed_time(b))
+            att.append(b.elapsed_time(c))
+        assert msa.poll_device_status() == 0
+        ti, ta = statistics.median(idx), statistics.median(att)
+        sh = r.sh
+        rec = {"n": sh["n"], "heads": sh["Hq"], "kv_heads": sh["Hkv"], "d_h": sh["d"],
+               "patterns": {p: sum(1 for e in r.w["table"] if e["pattern"] == p) for p in ("ashape", "vs", "block")},
+               "ms_per_layer": round(ti + ta, 4), "t_index_ms": round(ti, 4), "t_sparse_ms": round(ta, 4),
+               "edges": int(r.edges.sum()), "effective_tflops": round(r.flops / ((ti + ta) * 1e-3) / 1e12, 2),
+               "attention_tflops": round(r.flops / (ta * 1e-3) / 1e12, 2),
+               "index_gbs": round(r.index_bytes / (ti * 1e-3) / 1e9, 1) if ti > 0 and r.index_bytes else None,
+               "density": round(float(r.edges.sum()) / (sh["Hq"] * sh["n"] * (sh["n"] + 1) / 2), 5),
+               "tiles_64x128": int(r.tiles.sum()),
+               "tile_fill": round(float(r.edges.sum()) / max(float(r.tiles.sum()) * 64 * 128, 1.0), 4)}
+        if r.vs_edges:
+            rec["vs_edges"] = r.vs_edges
+        out[nm] = rec
+        del r
+        torch.cuda.empty_cache()
+    return out
 
 
 def dense_and_cold(runs, msa, per_layer, stream, reps=2):

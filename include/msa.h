@@ -310,6 +310,16 @@ MSA_API msa_status msa_layer_attend(const msa_shape* shape, const void* q, const
                                     const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
                                     size_t ws_bytes, void* stream);
 
+/* msa_layer_attend with work counters (measurement; no counterpart in the
+ * pages beyond the tile-padding accounting of the cost-model page §3): edges
+ * as for msa_layer_attend, and tiles (nullable, [B*Hq] int64 device counters,
+ * ADDED to): the number of 64-row x 128-key tiles each query head's rows were
+ * processed in, so tiles * 8192 is the (row, key) area the tensor cores
+ * covered for that head and E_h / (tiles * 8192) its useful fraction. */
+MSA_API msa_status msa_layer_attend_stats(const msa_shape* shape, const void* q, const void* k, const void* v,
+                                          const msa_head_cfg* table, void* o, float* lse, int64_t* edges,
+                                          int64_t* tiles, void* ws, size_t ws_bytes, void* stream);
+
 /* Failure-detection check (no counterpart in the pages): launches one thread
  * that waits on a barrier nothing arrives at, with the same bounded wait the
  * pipelines use but a limit of limit_ms (1..2000) milliseconds, so that the

@@ -30,7 +30,8 @@ EXPORTS = ("msa_status_string", "msa_vs_index_workspace", "msa_block_index_works
            "msa_prefill_layer", "msa_layer_index", "msa_layer_attend", "msa_kernel_launches", "msa_layer_indices",
            "msa_vs_expand", "msa_poll_device_status", "msa_build_block_index_static",
            "msa_check_wait_timeout", "msa_attn_dense", "msa_layer_varlen_workspace", "msa_prefill_layer_varlen",
-           "msa_layer_attend_rows", "msa_merge_attention", "msa_captured_mass", "msa_layer_varlen_indices")
+           "msa_layer_attend_rows", "msa_merge_attention", "msa_captured_mass", "msa_layer_varlen_indices",
+           "msa_layer_attend_stats")
 
 
 class MsaError(RuntimeError):
@@ -110,6 +111,8 @@ def load(path: str = LIB_PATH):
             lib.msa_layer_varlen_workspace.argtypes = [P, P, P, i32]
             lib.msa_prefill_layer_varlen.restype = st
             lib.msa_prefill_layer_varlen.argtypes = [P, P, i32, P, P, P, P, P, P, P, P, sz, P]
+            lib.msa_layer_attend_stats.restype = st
+            lib.msa_layer_attend_stats.argtypes = [P, P, P, P, P, P, P, P, P, P, sz, P]
             lib.msa_layer_varlen_indices.restype = st
             lib.msa_layer_varlen_indices.argtypes = [P, P, P, i32, P, i32, P, P, P]
             lib.msa_layer_attend_rows.restype = st
@@ -446,6 +449,17 @@ class Layer:
         _check(load().msa_layer_attend(ctypes.byref(self.shape), _ptr(q), _ptr(k), _ptr(v), self.tarr, _ptr(o),
                                        _ptr(lse), _ptr(edges), _ptr(self.ws), self.ws_bytes, _stream(stream)),
                "msa_layer_attend")
+        return o
+
+    def attend_stats(self, q, k, v, o, lse=None, edges=None, tiles=None, stream=None):
+        """attend() with work counters: edges (E_h) and tiles (64-row x 128-key tiles per query head),
+        both [B*Hq] int64 device tensors that are ADDED to."""
+        _check_attn(q, k, v, o, lse, edges, self._dims())
+        if tiles is not None:
+            _want(tiles, "tiles", torch.int64, (self.shape.B * self.shape.Hq,), device=q.device)
+        _check(load().msa_layer_attend_stats(ctypes.byref(self.shape), _ptr(q), _ptr(k), _ptr(v), self.tarr, _ptr(o),
+                                             _ptr(lse), _ptr(edges), _ptr(tiles), _ptr(self.ws), self.ws_bytes,
+                                             _stream(stream)), "msa_layer_attend_stats")
         return o
 
     def attend_rows(self, q, k, v, o, row_begin, row_end, lse=None, edges=None, stream=None):

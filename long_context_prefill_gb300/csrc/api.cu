@@ -228,7 +228,7 @@ __global__ void wait_timeout_check_kernel(uint64_t limit_ns, int* err) {
 
 msa_status attention(const msa_shape& s, const void* q, const void* k, const void* v, void* o, float* lse,
                      int64_t* edges, const std::vector<Unit>& units, const AttnArgs& idx, cudaStream_t stream,
-                     int32_t row_lo = 0, int32_t row_hi = 0x7FFFFFFF) {
+                     int32_t row_lo = 0, int32_t row_hi = 0x7FFFFFFF, int64_t* tiles = nullptr) {
   AttnMaps maps;
   if (!make_bf16_map(&maps.q, q, (int64_t)s.B * s.Hq, s.n, s.d_h, 64) ||
       !make_bf16_map(&maps.k, k, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64) ||
@@ -248,6 +248,7 @@ msa_status attention(const msa_shape& s, const void* q, const void* k, const voi
   a.o = o;
   a.lse = lse;
   a.edges = reinterpret_cast<unsigned long long*>(edges);
+  a.tiles = reinterpret_cast<unsigned long long*>(tiles);
   a.row_lo = row_lo;
   a.row_hi = row_hi;
   a.err = device_error_word();

@@ -934,6 +934,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
       if (lane == 0 && c) atomicAdd(A.edges + qh, c);
     }
+    // every tile of this sub-item is a 64-row x 128-key tile of each of its halves (counted by the half's first warp)
+    if (kCount && A.tiles && (quarter & 1) == 0 && lane == 0 && G.ex[hh] && mine > 0)
+      atomicAdd(A.tiles + qh, (unsigned long long)mine);
   }
 
   tc_fence_before();
@@ -975,7 +978,7 @@ msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Un
     a.n_units = cnt;
     a.n_bands = nb;
     msa_status st;
-    const bool count = args.edges != nullptr;
+    const bool count = args.edges != nullptr || args.tiles != nullptr;
     if (args.d == 128)
       st = count ? launch_impl<128, true>(maps, a, ut, stream) : launch_impl<128, false>(maps, a, ut, stream);
     else

@@ -65,6 +65,7 @@ struct AttnArgs {
   void* o;           // bf16 [B*Hq, n, d]
   float* lse;        // [B*Hq, n] or null
   unsigned long long* edges;  // [B*Hq] or null
+  unsigned long long* tiles;  // [B*Hq] or null: 64-row x 128-key tiles each query head was processed in
   // Vertical-Slash index (slot-indexed)
   const uint32_t* vs_dbits;  // [slots, words] bit δ of D
   const uint32_t* vs_cbits;  // [slots, words] bit j of C

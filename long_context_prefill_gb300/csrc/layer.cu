@@ -19,7 +19,7 @@ void block_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t s
                  std::vector<Unit>& out);
 msa_status attention(const msa_shape& s, const void* q, const void* k, const void* v, void* o, float* lse,
                      int64_t* edges, const std::vector<Unit>& units, const AttnArgs& idx, cudaStream_t stream,
-                     int32_t row_lo = 0, int32_t row_hi = 0x7FFFFFFF);
+                     int32_t row_lo = 0, int32_t row_hi = 0x7FFFFFFF, int64_t* tiles = nullptr);
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -207,7 +207,8 @@ static msa_status layer_index(const msa_shape& s, const void* q, const void* k, 
 
 static msa_status layer_attend(const msa_shape& s, const void* q, const void* k, const void* v,
                                const msa_head_cfg* table, void* o, float* lse, int64_t* edges, const LayerPlan& W,
-                               cudaStream_t strm, int32_t row_lo = 0, int32_t row_hi = 0x7FFFFFFF) {
+                               cudaStream_t strm, int32_t row_lo = 0, int32_t row_hi = 0x7FFFFFFF,
+                               int64_t* tiles = nullptr) {
   std::vector<Unit> units;
   if (!W.a_heads.empty()) {
     std::vector<int32_t> sinks, windows;
@@ -240,7 +241,7 @@ static msa_status layer_attend(const msa_shape& s, const void* q, const void* k,
   a.bs_cnt = W.bs_cnt;
   a.bs_topk = W.bs_heads.empty() ? 1 : W.bs_cfg.topk;
   a.bs_nb = W.nb;
-  return attention(s, q, k, v, o, lse, edges, ordered, a, strm, row_lo, row_hi);
+  return attention(s, q, k, v, o, lse, edges, ordered, a, strm, row_lo, row_hi, tiles);
 }
 
 }  // namespace msa
@@ -263,6 +264,17 @@ msa_status msa_layer_attend(const msa_shape* shape, const void* q, const void* k
   msa_status st = layer_prepare(shape, q, k, v, o, lse, edges, table, ws, ws_bytes, W);
   if (st != MSA_OK) return st;
   return layer_attend(*shape, q, k, v, table, o, lse, edges, W, (cudaStream_t)stream);
+}
+
+msa_status msa_layer_attend_stats(const msa_shape* shape, const void* q, const void* k, const void* v,
+                                  const msa_head_cfg* table, void* o, float* lse, int64_t* edges, int64_t* tiles,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  if (!v || !o) return MSA_ERR_INVALID_ARG;
+  if (tiles && reinterpret_cast<uintptr_t>(tiles) % 8) return MSA_ERR_INVALID_ARG;
+  LayerPlan W;
+  msa_status st = layer_prepare(shape, q, k, v, o, lse, edges, table, ws, ws_bytes, W);
+  if (st != MSA_OK) return st;
+  return layer_attend(*shape, q, k, v, table, o, lse, edges, W, (cudaStream_t)stream, 0, 0x7FFFFFFF, tiles);
 }
 
 msa_status msa_prefill_layer(const msa_shape* shape, const void* q, const void* k, const void* v,

@@ -421,27 +421,32 @@ __global__ void proxy_lse_kernel(const float2* part, int nchunks, float* lse2) {
 
 // log2 r_δ = log-sum-exp over the bins (y = n - L - δ) of the key blocks that
 // own them, m = 0..LB in order.
+// One thread per offset d of a slot (slots along the grid's y dimension).
 __global__ void slash_finalize_kernel(const float* rpart, int n, int L, int LB, int nkb, int slots, int mode,
                                       float* r) {
-  const int64_t total = (int64_t)slots * n;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t slot = idx / n;
-    const int d = (int)(idx % n);
+  for (int64_t slot = blockIdx.y; slot < slots; slot += gridDim.y)
+  for (int d = blockIdx.x * blockDim.x + threadIdx.x; d < n; d += gridDim.x * blockDim.x) {
     const int y = n - L - d;
     const int beta = (y >= 0) ? (y >> 5) : -((31 - y) >> 5);  // floor(y / 32)
     const int ln = y - 32 * beta;
+    const float* src = rpart + ((slot * (nkb + LB) + (beta + LB)) * (LB + 1)) * 32 + ln;
     float v[5];
     float mx = -INFINITY;
-    for (int m = 0; m <= LB; ++m) {
+#pragma unroll
+    for (int m = 0; m < 5; ++m) {
+      if (m > LB) break;
       const int kb = beta + m;
-      v[m] = (kb < 0 || kb >= nkb) ? -INFINITY
-                                   : rpart[((slot * (nkb + LB) + (beta + LB)) * (LB + 1) + m) * 32 + ln];
+      v[m] = (kb < 0 || kb >= nkb) ? -INFINITY : __ldg(src + m * 32);
       mx = fmaxf(mx, v[m]);
     }
     float s = 0.f;
-    if (mx != -INFINITY)
-      for (int m = 0; m <= LB; ++m) s += v[m] != -INFINITY ? exp2f(v[m] - mx) : 0.f;
+    if (mx != -INFINITY) {
+#pragma unroll
+      for (int m = 0; m < 5; ++m) {
+        if (m > LB) break;
+        s += v[m] != -INFINITY ? exp2f(v[m] - mx) : 0.f;
+      }
+    }
     float lr = s > 0.f ? mx + log2f(s) : -INFINITY;
     if ((mode & MSA_PROXY_SLASH_MEAN) && lr != -INFINITY) lr -= log2f((float)min(L, n - d));  // legal pairs of offset d
     r[slot * n + d] = lr;
@@ -722,26 +727,25 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
 // One thread per output bit, words assembled with a warp ballot.
 __global__ void slash_cover_kernel(const uint32_t* dbits, int n, int words, int cover_words, int slots,
                                    uint32_t* cover) {
-  const int64_t total = (int64_t)slots * cover_words * 32;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t slot = idx / ((int64_t)cover_words * 32);
-    const int z = (int)(idx % ((int64_t)cover_words * 32));
+  const int zt = cover_words * 32;  // a multiple of 32: the ballot below sees whole warps
+  for (int64_t slot = blockIdx.y; slot < slots; slot += gridDim.y) {
     const uint32_t* D = dbits + slot * words;
-    bool any = false;
-    if (z < n + 63) {
-      int lo = n - 1 - z, hi = n + 62 - z;
-      lo = lo < 0 ? 0 : lo;
-      hi = hi > n - 1 ? n - 1 : hi;
-      for (int w = lo >> 5; w <= (hi >> 5) && lo <= hi; ++w) {
-        uint32_t x = D[w];
-        if (w == (lo >> 5)) x &= 0xFFFFFFFFu << (lo & 31);
-        if (w == (hi >> 5)) x &= 0xFFFFFFFFu >> (31 - (hi & 31));
-        if (x) { any = true; break; }
+    for (int z = blockIdx.x * blockDim.x + threadIdx.x; z < zt; z += gridDim.x * blockDim.x) {
+      bool any = false;
+      if (z < n + 63) {
+        int lo = n - 1 - z, hi = n + 62 - z;
+        lo = lo < 0 ? 0 : lo;
+        hi = hi > n - 1 ? n - 1 : hi;
+        for (int w = lo >> 5; w <= (hi >> 5) && lo <= hi; ++w) {
+          uint32_t x = __ldg(D + w);
+          if (w == (lo >> 5)) x &= 0xFFFFFFFFu << (lo & 31);
+          if (w == (hi >> 5)) x &= 0xFFFFFFFFu >> (31 - (hi & 31));
+          if (x) { any = true; break; }
+        }
       }
+      const unsigned b = __ballot_sync(0xFFFFFFFFu, any);
+      if ((threadIdx.x & 31) == 0) cover[slot * cover_words + z / 32] = b;
     }
-    const unsigned b = __ballot_sync(0xFFFFFFFFu, any);
-    if ((threadIdx.x & 31) == 0) cover[slot * cover_words + z / 32] = b;
   }
 }
 
@@ -960,9 +964,10 @@ msa_status run_vs_index(const msa_shape& s, const void* q, const void* k, const 
                     : launch_scores<64>(P.Lp, tk, a, P.packs, P.nchunks2, stream);
   if (st != MSA_OK) return st;
   {
-    const int64_t total = (int64_t)P.slots * s.n;
-    const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
-    slash_finalize_kernel<<<blocks, 256, 0, stream>>>(a.rpart, s.n, P.L, P.LB, P.nkb, P.slots, cfg.proxy, slashsum);
+    const int bx = (s.n + 255) / 256 < 1024 ? (s.n + 255) / 256 : 1024;
+    const int by = P.slots < 65535 ? P.slots : 65535;
+    slash_finalize_kernel<<<dim3((unsigned)bx, (unsigned)by), 256, 0, stream>>>(a.rpart, s.n, P.L, P.LB, P.nkb, P.slots,
+                                                                               cfg.proxy, slashsum);
     note_launch();
     if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   }
@@ -979,9 +984,10 @@ msa_status run_vs_index(const msa_shape& s, const void* q, const void* k, const 
   {
     const int words = ceil_div(s.n, 32);
     const int cw = ceil_div(s.n + 63, 32);
-    const int64_t threads = (int64_t)P.slots * cw * 32;
-    const int blocks = (int)((threads + 255) / 256 < 8192 ? (threads + 255) / 256 : 8192);
-    slash_cover_kernel<<<blocks, 256, 0, stream>>>(out.slash_bits, s.n, words, cw, P.slots, out.slash_cover);
+    const int bx = (cw * 32 + 255) / 256 < 1024 ? (cw * 32 + 255) / 256 : 1024;
+    const int by = P.slots < 65535 ? P.slots : 65535;
+    slash_cover_kernel<<<dim3((unsigned)bx, (unsigned)by), 256, 0, stream>>>(out.slash_bits, s.n, words, cw, P.slots,
+                                                                            out.slash_cover);
     note_launch();
   }
   if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;

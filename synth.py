@@ -23,6 +23,8 @@ Workloads (B = 1 throughout; Q [B,Hq,n,d], K/V [B,Hkv,n,d], bf16):
   query head of the group, plus N(0,1) noise; V ~ N(0,1); every head
   Block-Sparse (block 64, top-k 100).
 * ``million`` the ``mixed`` generator and table at n = 1,048,576.
+* ``ashape128k`` the ``vs128k`` generator at n = 131072 with every head
+  A-shape (sink 128, window 1024): the A-shape pattern measured on its own.
 
 rot(u, p) rotates dimension pairs (2k, 2k+1) of u by the angle
 p * 10000^(-2k/d) (a RoPE-style rotation), so rot(u,p).rot(u,p') depends only
@@ -41,8 +43,9 @@ WORKLOADS = {
     "vs128k": dict(B=1, Hq=32, Hkv=8, n=131072, d=128),
     "bs128k": dict(B=1, Hq=32, Hkv=8, n=131072, d=128),
     "million": dict(B=1, Hq=32, Hkv=8, n=1048576, d=128),
+    "ashape128k": dict(B=1, Hq=32, Hkv=8, n=131072, d=128),
 }
-SEEDS = {"tiny": 1001, "mixed": 1002, "vs128k": 1003, "bs128k": 1004, "million": 1005}
+SEEDS = {"tiny": 1001, "mixed": 1002, "vs128k": 1003, "bs128k": 1004, "million": 1005, "ashape128k": 1006}
 
 
 def ashape(sink, window):
@@ -74,6 +77,8 @@ def table_for(name: str, Hq: int, seed: int):
         return [vslash(64, 1000, 6096) for _ in range(Hq)]
     if name == "bs128k":
         return [blocksparse(100) for _ in range(Hq)]
+    if name == "ashape128k":
+        return [ashape(128, 1024) for _ in range(Hq)]
     raise KeyError(name)
 
 
@@ -150,7 +155,7 @@ def make_workload(name: str, device="cpu", n: int | None = None, seed: int | Non
                 offs = [min(o, n_ - 1) for o in offs]
                 ss = float(rng.uniform(1.5, 3.0))
                 _plant_vs(qf, kf, kvh, g, gen, n_, d_, cols, vs_, offs, ss)
-            elif name == "vs128k":
+            elif name in ("vs128k", "ashape128k"):
                 cols = rng.choice(n_, size=min(50, n_), replace=False)
                 offs = [int(math.exp(rng.uniform(0.0, math.log(n_)))) - 1 for _ in range(16)]
                 _plant_vs(qf, kf, kvh, g, gen, n_, d_, cols, 3.0, offs, 2.0)

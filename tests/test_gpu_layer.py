@@ -80,3 +80,25 @@ def test_layer_one_group_pairings(cuda_lib):
              synth.ashape(0, 300), synth.blocksparse(5), synth.vslash(32, 30, 40), synth.blocksparse(5)]
     w = dict(q=q, k=k, v=v, table=table, shape=dict(B=1, Hq=8, Hkv=1, n=1000, d=64, scale=64 ** -0.5))
     run_layer(cuda_lib, w)
+
+
+def test_attend_stats_counts(cuda_lib):
+    """msa_layer_attend_stats: the same output and edge counts as
+    msa_layer_attend, and per head a tile count whose (row, key) area covers
+    the head's attended edges."""
+    w = synth.make_workload("mixed", device="cuda", n=3000, Hq=8, Hkv=2)
+    q, k, v, table, sh = w["q"], w["k"], w["v"], w["table"], w["shape"]
+    layer = cuda_lib.Layer(table, 1, sh["Hq"], sh["Hkv"], sh["n"], sh["d"], "cuda")
+    layer.index(q, k)
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    e1 = torch.zeros(sh["Hq"], dtype=torch.int64, device="cuda")
+    e2 = torch.zeros_like(e1)
+    tiles = torch.zeros_like(e1)
+    layer.attend(q, k, v, o1, edges=e1)
+    layer.attend_stats(q, k, v, o2, edges=e2, tiles=tiles)
+    assert cuda_lib.poll_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(e1, e2)
+    t, e = tiles.cpu().numpy(), e1.cpu().numpy()
+    assert np.all(t * 64 * 128 >= e) and np.all(t > 0)
+    # every query block of a head is processed in at least one tile
+    assert np.all(t >= (sh["n"] + 63) // 64)
