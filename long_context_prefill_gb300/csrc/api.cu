@@ -151,67 +151,63 @@ static std::vector<std::vector<int>> kv_groups(const msa_shape& s, const int32_t
 // two units (even and odd tiles), a single head one unit.  slot[x] is the
 // index slot of position x in batch 0; batch b adds b * slots_per_batch.
 static void head_units(const msa_shape& s, int32_t pattern, const int32_t* heads, int32_t nh, const int32_t* sink,
-                       const int32_t* window, const int32_t* slot, int32_t slots_per_batch, std::vector<Unit>& out) {
+                       const int32_t* window, const int32_t* slot, std::vector<Unit>& out) {
   const auto G = kv_groups(s, heads, nh);
-  for (int b = 0; b < s.B; ++b)
-    for (int kv = 0; kv < s.Hkv; ++kv) {
-      const std::vector<int>& P = G[(size_t)kv];
-      const int32_t kvh = b * s.Hkv + kv;
-      auto sub = [&](int x, int offset) {
-        const int32_t qh = b * s.Hq + heads[x];
-        const int32_t sl = slot ? b * slots_per_batch + slot[x] : 0;
-        return sub_unit(qh, qh, 0, 64, sl, sl, offset, sink ? sink[x] : 0, window ? window[x] : 0);
-      };
-      size_t p = 0;
-      for (; p + 1 < P.size(); p += 2)
-        for (int o = 0; o < 2; ++o) push_unit(out, pattern, kvh, sub(P[p], o), sub(P[p + 1], o));
-      if (p < P.size()) push_unit(out, pattern, kvh, sub(P[p], 0), sub(P[p], 1));
-    }
+  for (int kv = 0; kv < s.Hkv; ++kv) {
+    const std::vector<int>& P = G[(size_t)kv];
+    auto sub = [&](int x, int offset) {
+      const int32_t qh = heads[x];
+      const int32_t sl = slot ? slot[x] : 0;
+      return sub_unit(qh, qh, 0, 64, sl, sl, offset, sink ? sink[x] : 0, window ? window[x] : 0);
+    };
+    size_t p = 0;
+    for (; p + 1 < P.size(); p += 2)
+      for (int o = 0; o < 2; ++o) push_unit(out, pattern, kv, sub(P[p], o), sub(P[p + 1], o));
+    if (p < P.size()) push_unit(out, pattern, kv, sub(P[p], 0), sub(P[p], 1));
+  }
 }
 
 void ashape_units(const msa_shape& s, const int32_t* heads, int32_t nh, const int32_t* sink, const int32_t* window,
                   std::vector<Unit>& out) {
-  head_units(s, kUnitAshape, heads, nh, sink, window, nullptr, 0, out);
+  head_units(s, kUnitAshape, heads, nh, sink, window, nullptr, out);
 }
 
-void vs_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t slot_base_per_batch,
-              int32_t slots_per_batch, std::vector<Unit>& out) {
+// slot of heads[x] = x (its rank among the sequence's Vertical-Slash slots)
+void vs_units(const msa_shape& s, const int32_t* heads, int32_t nh, std::vector<Unit>& out) {
   std::vector<int32_t> slot((size_t)nh);
-  for (int x = 0; x < nh; ++x) slot[(size_t)x] = slot_base_per_batch + x;
-  head_units(s, kUnitVS, heads, nh, nullptr, nullptr, slot.data(), slots_per_batch, out);
+  for (int x = 0; x < nh; ++x) slot[(size_t)x] = x;
+  head_units(s, kUnitVS, heads, nh, nullptr, nullptr, slot.data(), out);
 }
 
 // Block-Sparse units: a half is one 64-row query block of one head.  Four
 // heads of a KV group at the same query block form one item (their block
 // lists tend to coincide); two heads take both blocks of a tile; a single
 // head takes both blocks of its even and of its odd tile.
-void block_units(const msa_shape& s, const int32_t* heads, int32_t nh, int32_t slots_per_batch,
-                 std::vector<Unit>& out) {
+void block_units(const msa_shape& s, const int32_t* heads, int32_t nh, std::vector<Unit>& out) {
   const auto G = kv_groups(s, heads, nh);
-  for (int b = 0; b < s.B; ++b)
-    for (int kv = 0; kv < s.Hkv; ++kv) {
-      const std::vector<int>& P = G[(size_t)kv];
-      const int32_t kvh = b * s.Hkv + kv;
-      auto qh = [&](int x) { return b * s.Hq + heads[P[(size_t)x]]; };
-      auto sl = [&](int x) { return b * slots_per_batch + P[(size_t)x]; };
-      int p = 0;
-      const int m = (int)P.size();
-      for (; p + 3 < m; p += 4)
-        for (int par = 0; par < 2; ++par)
-          for (int o = 0; o < 2; ++o)
-            push_unit(out, kUnitBlock, kvh,
-                      sub_unit(qh(p), qh(p + 1), 64 * par, 64 * par, sl(p), sl(p + 1), o, 0, 0),
-                      sub_unit(qh(p + 2), qh(p + 3), 64 * par, 64 * par, sl(p + 2), sl(p + 3), o, 0, 0));
-      if (p + 1 < m) {
+  for (int kv = 0; kv < s.Hkv; ++kv) {
+    const std::vector<int>& P = G[(size_t)kv];
+    const int32_t kvh = kv;
+    auto qh = [&](int x) { return heads[P[(size_t)x]]; };
+    auto sl = [&](int x) { return P[(size_t)x]; };
+    int p = 0;
+    const int m = (int)P.size();
+    for (; p + 3 < m; p += 4)
+      for (int par = 0; par < 2; ++par)
         for (int o = 0; o < 2; ++o)
-          push_unit(out, kUnitBlock, kvh, sub_unit(qh(p), qh(p + 1), 0, 0, sl(p), sl(p + 1), o, 0, 0),
-                    sub_unit(qh(p), qh(p + 1), 64, 64, sl(p), sl(p + 1), o, 0, 0));
-        p += 2;
-      }
-      if (p < m)
-        push_unit(out, kUnitBlock, kvh, sub_unit(qh(p), qh(p), 0, 64, sl(p), sl(p), 0, 0, 0),
-                  sub_unit(qh(p), qh(p), 0, 64, sl(p), sl(p), 1, 0, 0));
+          push_unit(out, kUnitBlock, kvh,
+                    sub_unit(qh(p), qh(p + 1), 64 * par, 64 * par, sl(p), sl(p + 1), o, 0, 0),
+                    sub_unit(qh(p + 2), qh(p + 3), 64 * par, 64 * par, sl(p + 2), sl(p + 3), o, 0, 0));
+    if (p + 1 < m) {
+      for (int o = 0; o < 2; ++o)
+        push_unit(out, kUnitBlock, kvh, sub_unit(qh(p), qh(p + 1), 0, 0, sl(p), sl(p + 1), o, 0, 0),
+                  sub_unit(qh(p), qh(p + 1), 64, 64, sl(p), sl(p + 1), o, 0, 0));
+      p += 2;
     }
+    if (p < m)
+      push_unit(out, kUnitBlock, kvh, sub_unit(qh(p), qh(p), 0, 64, sl(p), sl(p), 0, 0, 0),
+                sub_unit(qh(p), qh(p), 0, 64, sl(p), sl(p), 1, 0, 0));
+  }
 }
 
 // Failure-detection check: one thread waits on an mbarrier that nothing
@@ -226,21 +222,66 @@ __global__ void wait_timeout_check_kernel(uint64_t limit_ns, int* err) {
   }
 }
 
+// Sequences (in token order) with their prefix sums; lens[x] tokens each.
+// LB: diagonal-bin rows of the Vertical-Slash scores pass (0 when unused).
+std::vector<SeqInfo> build_seqs(const int32_t* lens, int n_seqs, int LB) {
+  std::vector<SeqInfo> out;
+  int64_t tok = 0, word = 0, cword = 0, nb = 0, kb = 0, tri = 0;
+  for (int x = 0; x < n_seqs; ++x) {
+    SeqInfo si;
+    memset(&si, 0, sizeof(si));
+    si.n = lens[x];
+    si.tok0 = (int32_t)tok;
+    si.word0 = (int32_t)word;
+    si.cword0 = (int32_t)cword;
+    si.nb0 = (int32_t)nb;
+    si.kb0 = (int32_t)kb;
+    si.tri0 = tri;
+    si.seq = x;
+    out.push_back(si);
+    tok += lens[x];
+    word += n_words(lens[x]);
+    cword += n_cover_words(lens[x]);
+    const int64_t b = n_blocks(lens[x]);
+    nb += b;
+    kb += 4 * n_tiles(lens[x]) + LB;
+    tri += b * (b + 1) / 2;
+  }
+  return out;
+}
+
+std::vector<SeqInfo> uniform_seqs(const msa_shape& s, int LB) {
+  std::vector<int32_t> lens((size_t)s.B, s.n);
+  return build_seqs(lens.data(), s.B, LB);
+}
+
+// Rows of the [rows, d] views (H * total tokens, plus a tile past the end)
+// must fit the int32 coordinates of TMA.
+bool rows_fit(int64_t H, const std::vector<SeqInfo>& seqs) {
+  int64_t tokens = 0;
+  for (const SeqInfo& x : seqs) tokens += x.n;
+  return H * tokens + 256 < ((int64_t)1 << 31);
+}
+
 msa_status attention(const msa_shape& s, const void* q, const void* k, const void* v, void* o, float* lse,
                      int64_t* edges, const std::vector<Unit>& units, const AttnArgs& idx, cudaStream_t stream,
-                     int32_t row_lo = 0, int32_t row_hi = 0x7FFFFFFF, int64_t* tiles = nullptr) {
+                     int32_t row_lo, int32_t row_hi, int64_t* tiles, const std::vector<SeqInfo>* seq_list) {
+  const std::vector<SeqInfo> own = seq_list ? std::vector<SeqInfo>() : uniform_seqs(s, 0);
+  const std::vector<SeqInfo>& seqs = seq_list ? *seq_list : own;
+  int64_t tokens = 0;
+  for (const SeqInfo& x : seqs) tokens += x.n;
+  if (!rows_fit(s.Hq, seqs)) return MSA_ERR_UNSUPPORTED;
   AttnMaps maps;
-  if (!make_bf16_map(&maps.q, q, (int64_t)s.B * s.Hq, s.n, s.d_h, 64) ||
-      !make_bf16_map(&maps.k, k, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64) ||
-      !make_bf16_map(&maps.v, v, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64) ||
-      !make_bf16_map(&maps.k16, k, (int64_t)s.B * s.Hkv, s.n, s.d_h, 16) ||
-      !make_bf16_map(&maps.v16, v, (int64_t)s.B * s.Hkv, s.n, s.d_h, 16))
+  if (!make_bf16_map(&maps.q, q, 1, (int64_t)s.Hq * tokens, s.d_h, 64) ||
+      !make_bf16_map(&maps.k, k, 1, (int64_t)s.Hkv * tokens, s.d_h, 64) ||
+      !make_bf16_map(&maps.v, v, 1, (int64_t)s.Hkv * tokens, s.d_h, 64) ||
+      !make_bf16_map(&maps.k16, k, 1, (int64_t)s.Hkv * tokens, s.d_h, 16) ||
+      !make_bf16_map(&maps.v16, v, 1, (int64_t)s.Hkv * tokens, s.d_h, 16))
     return MSA_ERR_CUDA;
   AttnArgs a = idx;
-  a.n = s.n;
   a.d = s.d_h;
-  a.nqt = ceil_div(s.n, 128);
-  a.T = (a.nqt + 1) / 2;
+  a.Hq = s.Hq;
+  a.Hkv = s.Hkv;
   a.scale_log2 = effective_scale(s) * 1.4426950408889634f;
   a.q = q;
   a.k = k;
@@ -253,7 +294,20 @@ msa_status attention(const msa_shape& s, const void* q, const void* k, const voi
   a.row_hi = row_hi;
   a.err = device_error_word();
   if (!a.err) return MSA_ERR_CUDA;
-  return launch_attention(maps, a, units.data(), (int)units.size(), stream);
+  // longest sequences first (their items are the heaviest), at most kMaxSeqs per launch
+  std::vector<SeqInfo> order;
+  for (const SeqInfo& x : seqs)
+    if (x.n > 0) order.push_back(x);
+  std::stable_sort(order.begin(), order.end(), [](const SeqInfo& p, const SeqInfo& q) { return p.n > q.n; });
+  for (size_t b = 0; b < order.size(); b += kMaxSeqs) {
+    SeqTable st;
+    memset(&st, 0, sizeof(st));
+    st.count = (int32_t)(order.size() - b < (size_t)kMaxSeqs ? order.size() - b : (size_t)kMaxSeqs);
+    for (int x = 0; x < st.count; ++x) st.s[x] = order[b + x];
+    msa_status r = launch_attention(maps, a, units.data(), (int)units.size(), st, stream);
+    if (r != MSA_OK) return r;
+  }
+  return MSA_OK;
 }
 
 }  // namespace msa
@@ -313,14 +367,13 @@ msa_status msa_attn_vs(const msa_shape* shape, const void* q, const void* k, con
   MSA_TRY(check_ptr4(index->slash_bits, true));
   MSA_TRY(check_ptr4(index->slash_cover, true));
   std::vector<Unit> units;
-  vs_units(*shape, heads, n_heads, 0, n_heads, units);
+  vs_units(*shape, heads, n_heads, units);
   AttnArgs a;
   memset(&a, 0, sizeof(a));
   a.vs_dbits = index->slash_bits;
   a.vs_cbits = index->vertical_bits;
   a.vs_cover = index->slash_cover;
-  a.vs_words = ceil_div(shape->n, 32);
-  a.vs_cover_words = ceil_div(shape->n + 63, 32);
+  a.vs_nslots = n_heads;
   return attention(*shape, q, k, v, o, lse, edges, units, a, (cudaStream_t)stream);
 }
 
@@ -338,13 +391,13 @@ msa_status msa_attn_block(const msa_shape* shape, const void* q, const void* k, 
   MSA_TRY(check_ptr4(block_idx, true));
   MSA_TRY(check_ptr4(block_cnt, true));
   std::vector<Unit> units;
-  block_units(*shape, heads, n_heads, n_heads, units);
+  block_units(*shape, heads, n_heads, units);
   AttnArgs a;
   memset(&a, 0, sizeof(a));
   a.bs_idx = block_idx;
   a.bs_cnt = block_cnt;
   a.bs_topk = topk;
-  a.bs_nb = ceil_div(shape->n, 64);
+  a.bs_nslots = n_heads;
   return attention(*shape, q, k, v, o, lse, edges, units, a, (cudaStream_t)stream);
 }
 

@@ -248,8 +248,10 @@ struct BlockSeg {
   int cnt[4], u[4], p[4];
   int last;
   int pend[4], pendb[4];  // per class (1: sub-item 0 only, 2: sub-item 1 only, 3: both): a block waiting for a partner
-  __device__ void init(const Unit& U, const Geo& G, const AttnArgs& a, int lane, int* sblk) {
+  __device__ void init(const Unit& U, const Geo& G, const AttnArgs& a, const SeqInfo& S, int lane, int* sblk) {
     bool fits = true;
+    const int nbs = n_blocks(S.n);
+    const int64_t base = (int64_t)a.bs_nslots * S.nb0;
     for (int hh = 0; hh < 4; ++hh) {
       const int X = hh >> 1, h = hh & 1;
       u[hh] = G.row0[hh] / 64;
@@ -257,7 +259,7 @@ struct BlockSeg {
       L[hh] = nullptr;
       p[hh] = 0;
       if (G.ex[hh]) {
-        const int64_t off = (int64_t)U.sub[X].slot[h] * a.bs_nb + u[hh];
+        const int64_t off = base + (int64_t)U.sub[X].slot[h] * nbs + u[hh];
         L[hh] = a.bs_idx + off * a.bs_topk;
         const int c = __ldg(a.bs_cnt + off);
         cnt[hh] = c < 0 ? 0 : (c > a.bs_topk ? a.bs_topk : c);
@@ -346,15 +348,16 @@ struct VSSeg {
   int grp;           // first block of the current 32-block group
   uint32_t m[4][2];  // this lane's block: attend masks per half
   uint32_t qm;       // this lane's block: 16-key quarters with attended keys, not yet placed
-  __device__ void init(const Unit& U, const Geo& G, const AttnArgs& A) {
-    cw = A.vs_cover_words;
-    nw = A.vs_words;
+  __device__ void init(const Unit& U, const Geo& G, const AttnArgs& A, const SeqInfo& S) {
+    cw = n_cover_words(S.n);
+    nw = n_words(S.n);
+    const int64_t wbase = (int64_t)A.vs_nslots * S.word0, cbase = (int64_t)A.vs_nslots * S.cword0;
 #pragma unroll
     for (int X = 0; X < 2; ++X) {
       const int slot = U.sub[X].slot[0];
-      dbits[X] = A.vs_dbits + (int64_t)slot * A.vs_words;
-      cbits[X] = A.vs_cbits + (int64_t)slot * A.vs_words;
-      cover[X] = A.vs_cover + (int64_t)slot * A.vs_cover_words;
+      dbits[X] = A.vs_dbits + wbase + (int64_t)slot * nw;
+      cbits[X] = A.vs_cbits + wbase + (int64_t)slot * nw;
+      cover[X] = A.vs_cover + cbase + (int64_t)slot * cw;
     }
     two = U.has1 && U.sub[1].slot[0] != U.sub[0].slot[0];
     hi_key = max(G.hi_key[0], G.hi_key[1]);
@@ -461,7 +464,7 @@ struct VSSeg {
 template <int D, bool kCount>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ AttnMaps M, const AttnArgs A,
-                       const __grid_constant__ UnitTable UT) {
+                       const __grid_constant__ UnitTable UT, const __grid_constant__ SeqTable ST) {
   using Ly = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -471,16 +474,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + Ly::kMisc);  // [0] tmem, [2] abort
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int rem = blockIdx.x, band = 0;
-  while (band + 1 < A.n_bands && rem >= (UT.band[band + 1] - UT.band[band]) * A.T) {
-    rem -= (UT.band[band + 1] - UT.band[band]) * A.T;
+  // sequence of this item (entries ordered by their first item), then band, t and unit within it
+  const SeqInfo& SI = ST.s[seq_search(ST.count, [&](int x) { return ST.s[x].item0; }, (int64_t)blockIdx.x)];
+  int rem = (int)blockIdx.x - SI.item0, band = 0;
+  while (band + 1 < A.n_bands && rem >= (UT.band[band + 1] - UT.band[band]) * SI.T) {
+    rem -= (UT.band[band + 1] - UT.band[band]) * SI.T;
     ++band;
   }
   const int band_units = UT.band[band + 1] - UT.band[band];
-  const int t = A.T - 1 - rem / band_units;
+  const int t = SI.T - 1 - rem / band_units;
   const Unit& U = UT.u[UT.band[band] + rem % band_units];
-  const int n = A.n;
-  const Geo G = make_geo(U, t, n, A.nqt);
+  const int n = SI.n;
+  const Geo G = make_geo(U, t, n, n_tiles(n));
+  // rows of the [rows, d] views: token i of head h of this sequence is row H * tok0 + h * n + i
+  const int32_t qrow0 = A.Hq * SI.tok0, krow0 = A.Hkv * SI.tok0 + U.kvh * n;
   {  // a row range (chunked attention) skips the items outside it; the whole CTA agrees
     bool in_range = false;
 #pragma unroll
@@ -530,8 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     BlockSeg bs;
     VSSeg vw;
     if (U.pattern == kUnitAshape) as.init(U, G, n);
-    else if (U.pattern == kUnitBlock) bs.init(U, G, A, lane, sblk);
-    else vw.init(U, G, A);
+    else if (U.pattern == kUnitBlock) bs.init(U, G, A, SI, lane, sblk);
+    else vw.init(U, G, A, SI);
     bool ok = true;
     for (int j = 0;; ++j) {
       if (misc[2]) { ok = false; break; }
@@ -623,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (G.ex[hh])
           for (int c = 0; c < D / 64; ++c)
             tma_load_3d(sQ + (hh >> 1) * Ly::kTile + c * 16384 + (hh & 1) * 8192, &M.q, &bars[kBarQ], 64 * c,
-                        G.row0[hh], U.sub[hh >> 1].qh[hh & 1]);
+                        qrow0 + U.sub[hh >> 1].qh[hh & 1] * n + G.row0[hh], 0);
     }
     // K(j) into slot 2j, V(j) into 2j+1 (mod kSlots): the MMA releases them in that order
     auto load = [&](int j, bool is_v) -> bool {
@@ -638,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const CUtensorMap* map = is_v ? &M.v : &M.k;
           mbar_arrive_expect_tx(full, Ly::kTile);
           for (int s = 0; s < 2; ++s)
-            for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384 + s * 8192, map, full, 64 * c, d.seg[s], U.kvh);
+            for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384 + s * 8192, map, full, 64 * c, krow0 + d.seg[s], 0);
         }
       } else {
         // eight 16-key segments (lane 8c + x: segment x, columns 64c..): a run
@@ -650,9 +657,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s0 = d.seg[h4];
           const bool run = d.seg[h4 + 1] == s0 + 16 && d.seg[h4 + 2] == s0 + 32 && d.seg[h4 + 3] == s0 + 48;
           if (!run)
-            tma_load_3d(dst + c * 16384 + x * 2048, is_v ? &M.v16 : &M.k16, full, 64 * c, d.seg[x], U.kvh);
+            tma_load_3d(dst + c * 16384 + x * 2048, is_v ? &M.v16 : &M.k16, full, 64 * c, krow0 + d.seg[x], 0);
           else if (x == h4)
-            tma_load_3d(dst + c * 16384 + x * 2048, is_v ? &M.v : &M.k, full, 64 * c, s0, U.kvh);
+            tma_load_3d(dst + c * 16384 + x * 2048, is_v ? &M.v : &M.k, full, 64 * c, krow0 + s0, 0);
         }
       }
       return true;
@@ -906,7 +913,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool empty = !(m_used > -INFINITY);  // no attended key in any tile: o = 0
     const float inv_l = (!empty && l > 0.f) ? 1.f / l : 0.f;
     const bool have = ok && mine > 0;  // warp-uniform: tcgen05.ld below is warp-collective
-    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(A.o) + ((int64_t)qh * n + i) * D;
+    const int64_t orow_idx = (int64_t)qrow0 + (int64_t)qh * n + i;
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(A.o) + orow_idx * D;
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -928,15 +936,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (row_ok && A.lse)
-      A.lse[(int64_t)qh * n + i] = (!empty && l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      A.lse[orow_idx] = (!empty && l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     if (kCount && A.edges) {  // the 32 rows of a warp lie in one half, so in one head
       unsigned long long c = count;
       for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
-      if (lane == 0 && c) atomicAdd(A.edges + qh, c);
+      if (lane == 0 && c) atomicAdd(A.edges + (int64_t)SI.seq * A.Hq + qh, c);
     }
     // every tile of this sub-item is a 64-row x 128-key tile of each of its halves (counted by the half's first warp)
     if (kCount && A.tiles && (quarter & 1) == 0 && lane == 0 && G.ex[hh] && mine > 0)
-      atomicAdd(A.tiles + qh, (unsigned long long)mine);
+      atomicAdd(A.tiles + (int64_t)SI.seq * A.Hq + qh, (unsigned long long)mine);
   }
 
   tc_fence_before();
@@ -948,15 +956,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, bool kCount>
-msa_status launch_impl(const AttnMaps& maps, const AttnArgs& a, const UnitTable& ut, cudaStream_t stream) {
+msa_status launch_impl(const AttnMaps& maps, const AttnArgs& a, const UnitTable& ut, const SeqTable& st,
+                       int64_t items, cudaStream_t stream) {
   auto kern = sparse_attn_kernel<D, kCount>;
   const int smem = Layout<D>::kAlloc;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return MSA_ERR_CUDA;
-  const int64_t items = (int64_t)a.T * a.n_units;
   if (items <= 0) return MSA_OK;
   if (items > 0x7FFFFFFF) return MSA_ERR_UNSUPPORTED;
-  kern<<<(unsigned)items, kThreads, smem, stream>>>(maps, a, ut);
+  kern<<<(unsigned)items, kThreads, smem, stream>>>(maps, a, ut, st);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
@@ -964,7 +972,7 @@ msa_status launch_impl(const AttnMaps& maps, const AttnArgs& a, const UnitTable&
 }  // namespace
 
 msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Unit* units, int n_units,
-                            cudaStream_t stream) {
+                            SeqTable& seqs, cudaStream_t stream) {
   for (int base = 0; base < n_units; base += kMaxUnits) {
     UnitTable ut;
     const int cnt = n_units - base < kMaxUnits ? n_units - base : kMaxUnits;
@@ -974,15 +982,24 @@ msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Un
     for (int x = 0; x < cnt; ++x)
       if (x == 0 || ut.u[x].kvh != ut.u[x - 1].kvh) ut.band[nb++] = x;
     ut.band[nb] = cnt;
+    // items: every unit for every sequence, the sequences in table order
+    int64_t items = 0;
+    for (int x = 0; x < seqs.count; ++x) {
+      seqs.s[x].T = (n_tiles(seqs.s[x].n) + 1) / 2;
+      seqs.s[x].item0 = (int32_t)items;
+      items += (int64_t)seqs.s[x].T * cnt;
+    }
     AttnArgs a = args;
     a.n_units = cnt;
     a.n_bands = nb;
     msa_status st;
     const bool count = args.edges != nullptr || args.tiles != nullptr;
     if (args.d == 128)
-      st = count ? launch_impl<128, true>(maps, a, ut, stream) : launch_impl<128, false>(maps, a, ut, stream);
+      st = count ? launch_impl<128, true>(maps, a, ut, seqs, items, stream)
+                 : launch_impl<128, false>(maps, a, ut, seqs, items, stream);
     else
-      st = count ? launch_impl<64, true>(maps, a, ut, stream) : launch_impl<64, false>(maps, a, ut, stream);
+      st = count ? launch_impl<64, true>(maps, a, ut, seqs, items, stream)
+                 : launch_impl<64, false>(maps, a, ut, seqs, items, stream);
     if (st != MSA_OK) return st;
   }
   return MSA_OK;

@@ -34,20 +34,25 @@ struct HeadMap {
   int32_t row_head[kMaxSlots];  // pooled head -> b*H + h of the source tensor
 };
 
-// Mean of each 64-row block of `src` heads listed in `map`, written as three
-// bf16 planes whose sum is the fp32 mean to about 2^-24 (out [nh, 3, nb, D]:
+// Mean of each 64-row block of the `src` heads listed in `map`, for every
+// sequence of the launch, written as three bf16 planes whose sum is the fp32
+// mean to about 2^-24 (per sequence and head [3, nb, D], sequence-major:
 // hi = bf16(m), mid = bf16(m - hi), lo = bf16(m - hi - mid)), so the score
 // products can run on the bf16 tensor cores at fp32-like accuracy.
 template <int D>
-__global__ void __launch_bounds__(128) block_pool_kernel(const __nv_bfloat16* src, int n, int nb,
+__global__ void __launch_bounds__(128) block_pool_kernel(const __nv_bfloat16* src, int H, int n_pool,
+                                                         const __grid_constant__ SeqTable ST,
                                                          const __grid_constant__ HeadMap map, __nv_bfloat16* out) {
   constexpr int kTPR = D / 8;            // threads per row (8 columns each, 16-byte loads)
   constexpr int kGroups = 128 / kTPR;    // rows handled in parallel
   __shared__ float part[kGroups][D];
-  const int u = blockIdx.x, hx = blockIdx.y;
+  // block u of pooled head hx of one sequence of the launch (blocks of all sequences along x)
+  const SeqInfo& S = ST.s[seq_search(ST.count, [&](int x) { return ST.s[x].blk0; }, (int64_t)blockIdx.x)];
+  const int u = (int)blockIdx.x - S.blk0, hx = blockIdx.y;
+  const int n = S.n, nb = n_blocks(n);
   const int tid = threadIdx.x, grp = tid / kTPR, c8 = (tid % kTPR) * 8;
   const int a = 64 * u, e = min(a + 64, n);
-  const __nv_bfloat16* base = src + ((int64_t)map.row_head[hx] * n) * D;
+  const __nv_bfloat16* base = src + ((int64_t)H * S.tok0 + (int64_t)map.row_head[hx] * n) * D;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int r = a + grp; r < e; r += kGroups) {
     const uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)r * D + c8));
@@ -70,7 +75,8 @@ __global__ void __launch_bounds__(128) block_pool_kernel(const __nv_bfloat16* sr
     const float r1 = m - __bfloat162float(h);
     const __nv_bfloat16 md = __float2bfloat16_rn(r1);
     const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(md));
-    __nv_bfloat16* o = out + ((int64_t)hx * 3 * nb + u) * D + c;
+    // planes of head hx of this sequence: rows 3 * (n_pool * nb0 + hx * nb) + plane * nb + u
+    __nv_bfloat16* o = out + ((int64_t)3 * ((int64_t)n_pool * S.nb0 + (int64_t)hx * nb) + u) * D + c;
     o[0] = h;
     o[(int64_t)nb * D] = md;
     o[(int64_t)2 * nb * D] = lo;
@@ -104,16 +110,16 @@ struct ScLayout {
 };
 
 struct ScArgs {
-  int nb, T, cs;        // query blocks, row tiles, slots in this launch
-  int slot_base;        // first slot of this launch (for the score rows)
-  float* scores;        // packed triangles of every slot
+  int n_bs, n_kv;       // query slots and pooled KV heads per sequence
+  float* scores;        // packed triangles of every slot (sequence-major)
   int* err;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kScThreads, 1)
     block_scores_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                        const __grid_constant__ HeadMap kv_of_slot, const ScArgs A) {
+                        const __grid_constant__ HeadMap kv_of_slot, const ScArgs A,
+                        const __grid_constant__ SeqTable ST) {
   using Ly = ScLayout<D>;
   constexpr int kC = D / 64;  // stages per key tile
   extern __shared__ uint8_t smem_raw[];
@@ -126,10 +132,16 @@ __global__ void __launch_bounds__(kScThreads, 1)
   uint64_t* aempty = afull + 2;                // [2]
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + Ly::kMisc);  // [0] TMEM base, [1] abort
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tu = A.T - 1 - (int)(blockIdx.x / A.cs);
-  const int sl = (int)(blockIdx.x % A.cs);
+  // sequence, then row tile (heaviest first) and slot
+  const SeqInfo& S = ST.s[seq_search(ST.count, [&](int x) { return ST.s[x].sc0; }, (int64_t)blockIdx.x)];
+  const int local = (int)blockIdx.x - S.sc0;
+  const int nb = n_blocks(S.n), T = (nb + 127) / 128;
+  const int tu = T - 1 - local / A.n_bs;
+  const int sl = local % A.n_bs;
   const int kvp = kv_of_slot.row_head[sl];
   const int ntile = tu + 1;  // key tiles tv = 0 .. tu
+  // rows of plane p in the [rows, D] views of the pooled means: 3 (n_heads nb0 + head nb) + p nb
+  const int32_t qrow = 3 * (A.n_bs * S.nb0 + sl * nb), krow = 3 * (A.n_kv * S.nb0 + kvp * nb);
   if (warp == 0) {
     tmem_alloc(const_cast<uint32_t*>(&misc[0]), 256);
     tmem_relinquish();
@@ -159,7 +171,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
       mbar_arrive_expect_tx(qfull, 3 * kC * Ly::kChunk);
       for (int p = 0; p < 3; ++p)
         for (int c = 0; c < kC; ++c)
-          tma_load_3d(sm + Ly::kQ + (p * kC + c) * Ly::kChunk, &tq, qfull, 64 * c, 128 * tu, 3 * sl + p);
+          tma_load_3d(sm + Ly::kQ + (p * kC + c) * Ly::kChunk, &tq, qfull, 64 * c, qrow + p * nb + 128 * tu, 0);
       bool ok = true;
       for (int it = 0; it < ntile * kC && ok; ++it) {
         const int st = it % kScStages;
@@ -167,7 +179,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const int tv = it / kC, c = it % kC;
         mbar_arrive_expect_tx(&kfull[st], 3 * Ly::kChunk);
         for (int p = 0; p < 3; ++p)
-          tma_load_3d(sm + Ly::kK + (st * 3 + p) * Ly::kChunk, &tk, &kfull[st], 64 * c, 128 * tv, 3 * kvp + p);
+          tma_load_3d(sm + Ly::kK + (st * 3 + p) * Ly::kChunk, &tk, &kfull[st], 64 * c, krow + p * nb + 128 * tv, 0);
       }
       if (!ok) { misc[1] = 1; set_err(A.err, kErrTimeout); }
     }
@@ -211,7 +223,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lanes 32q ..
     float* st = reinterpret_cast<float*>(sm + Ly::kStage) + (warp - 2) * 32 * 33;
-    const int64_t tri_base = (int64_t)(A.slot_base + sl) * ((int64_t)A.nb * (A.nb + 1) / 2);
+    const int64_t tri_base = (int64_t)A.n_bs * S.tri0 + (int64_t)sl * ((int64_t)nb * (nb + 1) / 2);
     bool ok = true;
     for (int t = 0; t < ntile; ++t) {
       const int buf = t & 1;
@@ -230,7 +242,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
 #pragma unroll 4
         for (int k = 0; k < 32; ++k) {
           const int u = 128 * tu + 32 * q + k;
-          if (u < A.nb && vcol <= u) A.scores[tri_base + (int64_t)u * (u + 1) / 2 + vcol] = st[k * 33 + lane];
+          if (u < nb && vcol <= u) A.scores[tri_base + (int64_t)u * (u + 1) / 2 + vcol] = st[k * 33 + lane];
         }
         __syncwarp();
       }
@@ -309,15 +321,23 @@ __device__ __forceinline__ void topk_row_regs(const float* row, int u, int k1, i
 // One warp per (slot, query block u): J_u = {u} ∪ top_{k-1} of row u.  Rows
 // longer than 2048 candidates use a radix select over a per-warp histogram in
 // dynamic shared memory (kTopkWarps x 2048 ints, given only when nb > 2048).
-__global__ void __launch_bounds__(32 * kTopkWarps, 4) block_topk_kernel(const float* scores, int nb, int topk,
-                                                                      int nslots, int32_t* J, int32_t* cnt) {
+__global__ void __launch_bounds__(32 * kTopkWarps, 4) block_topk_kernel(const float* scores, int n_bs, int topk,
+                                                                      const __grid_constant__ SeqTable ST,
+                                                                      int64_t jobs, int32_t* J, int32_t* cnt_out) {
   extern __shared__ int hist_all[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t job = (int64_t)blockIdx.x * kTopkWarps + warp;
-  if (job >= (int64_t)nslots * nb) return;
-  const int slot = (int)(job / nb), u = (int)(job % nb);
-  const float* row = scores + (int64_t)slot * ((int64_t)nb * (nb + 1) / 2) + (int64_t)u * (u + 1) / 2;
+  const int64_t job_l = (int64_t)blockIdx.x * kTopkWarps + warp;
+  if (job_l >= jobs) return;
+  // sequence (n_bs * blocks jobs each), slot and query block
+  const SeqInfo& S = ST.s[seq_search(ST.count, [&](int x) { return (int64_t)n_bs * ST.s[x].blk0; }, job_l)];
+  const int nb = n_blocks(S.n);
+  const int64_t local = job_l - (int64_t)n_bs * S.blk0;
+  const int slot = (int)(local / nb), u = (int)(local % nb);
+  const float* row = scores + (int64_t)n_bs * S.tri0 + (int64_t)slot * ((int64_t)nb * (nb + 1) / 2) +
+                     (int64_t)u * (u + 1) / 2;
+  const int64_t job = (int64_t)n_bs * S.nb0 + (int64_t)slot * nb + u;  // output row (sequence-major)
   int32_t* out = J + job * topk;
+  int32_t* cnt = cnt_out;
   const int k1 = min(topk - 1, u);  // picks among v < u
   if (u <= 2048 && k1 < u && k1 > 0) {
     if (u <= 512) topk_row_regs<16>(row, u, k1, topk, lane, out, cnt + job);
@@ -407,38 +427,70 @@ __global__ void __launch_bounds__(32 * kTopkWarps, 4) block_topk_kernel(const fl
 }
 
 struct BSPlan {
-  std::vector<int32_t> q_rows, kv_rows, kv_of_slot;
-  int nb, slots, nkv;
-  size_t off_q, off_k, off_s, total;
+  std::vector<int32_t> q_rows, kv_rows, kv_of_slot;  // per sequence: query head per slot, KV heads, KV index per slot
+  int slots = 0, nkv = 0;                           // per sequence
+  std::vector<SeqInfo> seqs;                        // token order
+  std::vector<SeqTable> launches;                   // blk0 / sc0 filled
+  std::vector<int64_t> blocks, ctas;                // per launch: Σ nb, score CTAs
+  int nb_max = 1;
+  int64_t nb_total = 0, tri_total = 0;
+  size_t off_q = 0, off_k = 0, off_s = 0, total = 0;
 };
 
 size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-BSPlan plan_bs(const msa_shape& s, const int32_t* heads, int32_t n_heads) {
+// heads null: the upper bound (one KV head per listed head).
+BSPlan plan_bs(const msa_shape& s, const int32_t* heads, int32_t n_heads, const std::vector<SeqInfo>* seq_list) {
   BSPlan P;
-  P.nb = ceil_div(s.n, 64);
-  P.slots = s.B * n_heads;
+  P.slots = n_heads;
   const int g = s.Hq / s.Hkv;
   if (heads) {
-    std::vector<int> kv_index((size_t)s.B * s.Hkv, -1);
-    for (int b = 0; b < s.B; ++b)
-      for (int x = 0; x < n_heads; ++x) {
-        P.q_rows.push_back(b * s.Hq + heads[x]);
-        const int kv = b * s.Hkv + heads[x] / g;
-        if (kv_index[(size_t)kv] < 0) {
-          kv_index[(size_t)kv] = (int)P.kv_rows.size();
-          P.kv_rows.push_back(kv);
-        }
-        P.kv_of_slot.push_back(kv_index[(size_t)kv]);
+    std::vector<int> kv_index((size_t)s.Hkv, -1);
+    for (int x = 0; x < n_heads; ++x) {
+      P.q_rows.push_back(heads[x]);
+      const int kv = heads[x] / g;
+      if (kv_index[(size_t)kv] < 0) {
+        kv_index[(size_t)kv] = (int)P.kv_rows.size();
+        P.kv_rows.push_back(kv);
       }
+      P.kv_of_slot.push_back(kv_index[(size_t)kv]);
+    }
     P.nkv = (int)P.kv_rows.size();
   } else {
     P.nkv = P.slots;  // upper bound
   }
+  P.seqs = seq_list ? *seq_list : uniform_seqs(s, 0);
+  for (const SeqInfo& x : P.seqs) {
+    const int64_t nb = n_blocks(x.n);
+    P.nb_total += nb;
+    P.tri_total += nb * (nb + 1) / 2;
+    P.nb_max = (int)nb > P.nb_max ? (int)nb : P.nb_max;
+  }
+  std::vector<SeqInfo> live;
+  for (const SeqInfo& x : P.seqs)
+    if (x.n > 0) live.push_back(x);
+  for (size_t b = 0; b < live.size(); b += kMaxSeqs) {
+    SeqTable st;
+    memset(&st, 0, sizeof(st));
+    st.count = (int32_t)(live.size() - b < (size_t)kMaxSeqs ? live.size() - b : (size_t)kMaxSeqs);
+    int64_t blk = 0, sc = 0;
+    for (int x = 0; x < st.count; ++x) {
+      SeqInfo si = live[b + x];
+      si.blk0 = (int32_t)blk;
+      si.sc0 = (int32_t)sc;
+      const int64_t nb = n_blocks(si.n);
+      blk += nb;
+      sc += (int64_t)P.slots * ((nb + 127) / 128);
+      st.s[x] = si;
+    }
+    P.launches.push_back(st);
+    P.blocks.push_back(blk);
+    P.ctas.push_back(sc);
+  }
   size_t off = 0;
-  P.off_q = off; off = al256(off + sizeof(__nv_bfloat16) * 3 * (size_t)P.slots * P.nb * s.d_h);
-  P.off_k = off; off = al256(off + sizeof(__nv_bfloat16) * 3 * (size_t)P.nkv * P.nb * s.d_h);
-  P.off_s = off; off = al256(off + sizeof(float) * (size_t)P.slots * ((size_t)P.nb * (P.nb + 1) / 2));
+  P.off_q = off; off = al256(off + sizeof(__nv_bfloat16) * 3 * (size_t)P.slots * (size_t)P.nb_total * s.d_h);
+  P.off_k = off; off = al256(off + sizeof(__nv_bfloat16) * 3 * (size_t)P.nkv * (size_t)P.nb_total * s.d_h);
+  P.off_s = off; off = al256(off + sizeof(float) * (size_t)P.slots * (size_t)P.tri_total);
   P.total = off + 256;
   return P;
 }
@@ -446,75 +498,76 @@ BSPlan plan_bs(const msa_shape& s, const int32_t* heads, int32_t n_heads) {
 template <int D>
 msa_status run_bs(const msa_shape& s, const void* q, const void* k, const BSPlan& P, int topk, int32_t* J,
                   int32_t* cnt, uint8_t* w, cudaStream_t stream) {
-  __nv_bfloat16* qbar = reinterpret_cast<__nv_bfloat16*>(w + P.off_q);  // [slots, 3, nb, D]
-  __nv_bfloat16* kbar = reinterpret_cast<__nv_bfloat16*>(w + P.off_k);  // [nkv, 3, nb, D]
+  __nv_bfloat16* qbar = reinterpret_cast<__nv_bfloat16*>(w + P.off_q);  // per sequence [slots, 3, nb, D]
+  __nv_bfloat16* kbar = reinterpret_cast<__nv_bfloat16*>(w + P.off_k);  // per sequence [nkv, 3, nb, D]
   float* sc = reinterpret_cast<float*>(w + P.off_s);
-  for (int base = 0; base < P.slots; base += kMaxSlots) {
-    const int cntq = P.slots - base < kMaxSlots ? P.slots - base : kMaxSlots;
-    HeadMap m;
-    memset(&m, 0, sizeof(m));
-    for (int x = 0; x < cntq; ++x) m.row_head[x] = P.q_rows[(size_t)(base + x)];
-    block_pool_kernel<D><<<dim3(P.nb, cntq), 128, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(q), s.n, P.nb,
-                                                                m, qbar + (int64_t)base * 3 * P.nb * D);
-    note_launch();
-    if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+  if (P.slots > kMaxSlots || P.nkv > kMaxSlots) return MSA_ERR_UNSUPPORTED;
+  HeadMap mq, mk, mslot;
+  memset(&mq, 0, sizeof(mq));
+  memset(&mk, 0, sizeof(mk));
+  memset(&mslot, 0, sizeof(mslot));
+  for (int x = 0; x < P.slots; ++x) {
+    mq.row_head[x] = P.q_rows[(size_t)x];
+    mslot.row_head[x] = P.kv_of_slot[(size_t)x];
   }
-  for (int base = 0; base < P.nkv; base += kMaxSlots) {
-    const int cntk = P.nkv - base < kMaxSlots ? P.nkv - base : kMaxSlots;
-    HeadMap m;
-    memset(&m, 0, sizeof(m));
-    for (int x = 0; x < cntk; ++x) m.row_head[x] = P.kv_rows[(size_t)(base + x)];
-    block_pool_kernel<D><<<dim3(P.nb, cntk), 128, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(k), s.n, P.nb,
-                                                                m, kbar + (int64_t)base * 3 * P.nb * D);
-    note_launch();
-    if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
-  }
-  // scores on the tensor cores: pooled planes viewed as [planes, nb, D] with 128-row boxes
-  CUtensorMap tkm;
-  if (!make_bf16_map(&tkm, kbar, (int64_t)3 * P.nkv, P.nb, D, 128)) return MSA_ERR_CUDA;
+  for (int x = 0; x < P.nkv; ++x) mk.row_head[x] = P.kv_rows[(size_t)x];
+  // scores on the tensor cores: pooled planes viewed as [rows, D] with 128-row boxes
+  CUtensorMap tqm, tkm;
+  if (!make_bf16_map(&tqm, qbar, 1, (int64_t)3 * P.slots * P.nb_total, D, 128) ||
+      !make_bf16_map(&tkm, kbar, 1, (int64_t)3 * P.nkv * P.nb_total, D, 128))
+    return MSA_ERR_CUDA;
   auto kern = block_scores_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ScLayout<D>::kAlloc) != cudaSuccess)
     return MSA_ERR_CUDA;
   ScArgs sa;
-  sa.nb = P.nb;
-  sa.T = (P.nb + 127) / 128;
+  sa.n_bs = P.slots;
+  sa.n_kv = P.nkv;
   sa.scores = sc;
   sa.err = device_error_word();
   if (!sa.err) return MSA_ERR_CUDA;
-  for (int base = 0; base < P.slots; base += kMaxSlots) {
-    const int cs = P.slots - base < kMaxSlots ? P.slots - base : kMaxSlots;
-    HeadMap m;
-    memset(&m, 0, sizeof(m));
-    for (int x = 0; x < cs; ++x) m.row_head[x] = P.kv_of_slot[(size_t)(base + x)];
-    CUtensorMap tqm;
-    if (!make_bf16_map(&tqm, qbar + (int64_t)base * 3 * P.nb * D, (int64_t)3 * cs, P.nb, D, 128)) return MSA_ERR_CUDA;
-    sa.cs = cs;
-    sa.slot_base = base;
-    kern<<<(unsigned)(sa.T * cs), kScThreads, ScLayout<D>::kAlloc, stream>>>(tqm, tkm, m, sa);
+  const int hist_bytes = P.nb_max > 2048 ? kTopkWarps * 2048 * (int)sizeof(int) : 0;
+  for (size_t L = 0; L < P.launches.size(); ++L) {
+    const SeqTable& st = P.launches[L];
+    if (P.blocks[L] > 0x7FFFFFFF || P.ctas[L] > 0x7FFFFFFF) return MSA_ERR_UNSUPPORTED;
+    block_pool_kernel<D><<<dim3((unsigned)P.blocks[L], (unsigned)P.slots), 128, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(q), s.Hq, P.slots, st, mq, qbar);
+    note_launch();
+    if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+    block_pool_kernel<D><<<dim3((unsigned)P.blocks[L], (unsigned)P.nkv), 128, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(k), s.Hkv, P.nkv, st, mk, kbar);
+    note_launch();
+    if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+    kern<<<(unsigned)P.ctas[L], kScThreads, ScLayout<D>::kAlloc, stream>>>(tqm, tkm, mslot, sa, st);
+    note_launch();
+    if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+    const int64_t jobs = (int64_t)P.slots * P.blocks[L];
+    block_topk_kernel<<<(unsigned)((jobs + kTopkWarps - 1) / kTopkWarps), 32 * kTopkWarps, hist_bytes, stream>>>(
+        sc, P.slots, topk, st, jobs, J, cnt);
     note_launch();
     if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   }
-  const int64_t jobs = (int64_t)P.slots * P.nb;
-  const int hist_bytes = P.nb > 2048 ? kTopkWarps * 2048 * (int)sizeof(int) : 0;
-  block_topk_kernel<<<(unsigned)((jobs + kTopkWarps - 1) / kTopkWarps), 32 * kTopkWarps, hist_bytes, stream>>>(
-      sc, P.nb, topk, P.slots, J, cnt);
-  note_launch();
-  return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return MSA_OK;
 }
 
 }  // namespace
 
-size_t block_index_ws_bytes(const msa_shape& s, int32_t n_heads) { return plan_bs(s, nullptr, n_heads).total + 256; }
-size_t block_index_ws_bytes_exact(const msa_shape& s, const int32_t* heads, int32_t n_heads) {
-  return plan_bs(s, heads, n_heads).total + 256;
+size_t block_index_ws_bytes(const msa_shape& s, int32_t n_heads, const std::vector<SeqInfo>* seqs) {
+  return plan_bs(s, nullptr, n_heads, seqs).total + 256;
+}
+size_t block_index_ws_bytes_exact(const msa_shape& s, const int32_t* heads, int32_t n_heads,
+                                  const std::vector<SeqInfo>* seqs) {
+  return plan_bs(s, heads, n_heads, seqs).total + 256;
 }
 
 msa_status run_block_index(const msa_shape& s, const void* q, const void* k, const int32_t* heads,
                            int32_t n_heads, int32_t topk, int32_t* block_idx, int32_t* block_cnt, void* ws,
-                           size_t ws_bytes, cudaStream_t stream) {
-  const int nb = ceil_div(s.n, 64);
-  if ((int64_t)nb * (nb + 1) / 2 > ((int64_t)1 << 40)) return MSA_ERR_UNSUPPORTED;
-  BSPlan P = plan_bs(s, heads, n_heads);
+                           size_t ws_bytes, cudaStream_t stream, const std::vector<SeqInfo>* seqs) {
+  BSPlan P = plan_bs(s, heads, n_heads, seqs);
+  for (const SeqInfo& x : P.seqs) {
+    const int64_t nb = n_blocks(x.n);
+    if (nb * (nb + 1) / 2 > ((int64_t)1 << 40)) return MSA_ERR_UNSUPPORTED;
+  }
+  if (!rows_fit(s.Hq, P.seqs) || (int64_t)3 * P.slots * P.nb_total >= ((int64_t)1 << 31)) return MSA_ERR_UNSUPPORTED;
   // the workspace query is the worst case (one KV head per listed head); what
   // this call needs counts the KV heads the listed heads actually read
   if (!ws || ws_bytes < P.total + 256) return MSA_ERR_WORKSPACE_TOO_SMALL;

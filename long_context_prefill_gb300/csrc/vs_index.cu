@@ -49,29 +49,30 @@ struct ProxyWarps {
 };
 constexpr int kKStages = 3;
 
-struct Pack {
-  int32_t kvh;                  // b * Hkv + kv head
+// The Vertical-Slash heads of one KV group (at most kPackMaxHeads of them),
+// the same for every sequence: a pack is one group pack of one sequence.
+struct GroupPack {
+  int32_t g;                    // kv head
   int32_t nh;                   // heads in this pack
-  int32_t slot[kPackMaxHeads];  // output slot per head
-  int32_t qh[kPackMaxHeads];    // b * Hq + query head
+  int32_t x[kPackMaxHeads];     // slot of each head within its sequence
+  int32_t h[kPackMaxHeads];     // query head
 };
-constexpr int kMaxPacks = 96;
+constexpr int kMaxGroupPacks = 64;
 struct PackTable {
-  Pack p[kMaxPacks];
+  int32_t n_gp, pad;
+  GroupPack p[kMaxGroupPacks];
 };
 
 struct ProxyArgs {
-  const void* q;       // bf16 [B*Hq, n, d]
-  int32_t n, d, L, Lp; // proxy rows L, padded to Lp per head
-  int32_t nchunks;     // key chunks per pack
-  int32_t ntiles;      // 128-key tiles over n
-  float c2;            // scale * log2(e)
-  float2* part;        // [packs, nchunks, 256] (max, sum) in log2 units (pass 1 out)
-  float* lse2;         // [packs, 256] (pass 2 in)
-  float* colsum;       // [slots, n] log2 c_j
-  float* rpart;        // [slots, nkb + LB, LB + 1, 32] log2 partial slash sums
-  int32_t nkb;         // 4 * ntiles key blocks of 32
-  int32_t mode;        // proxy convention bits (MSA_PROXY_*)
+  const void* q;        // bf16 rows (row = Hq * tok0 + h * n + i)
+  int32_t d, Lp;        // proxy rows per head L = min(last_q, n), padded to Lp
+  int32_t last_q, Hq, Hkv, n_vs;  // n_vs: Vertical-Slash slots per sequence
+  float c2;             // scale * log2(e)
+  float2* part;         // [CTAs of the launch, 256] (max, sum) in log2 units (pass 1 out)
+  float* lse2;          // [packs of the launch, 256] (pass 2 in)
+  float* colsum;        // sequence-major, n per slot: log2 c_j
+  float* rpart;         // sequence-major, (4 ntiles + LB) x (LB + 1) x 32 per slot: log2 partial slash sums
+  int32_t mode;         // proxy convention bits (MSA_PROXY_*)
   int* err;
 };
 
@@ -102,15 +103,15 @@ struct PLayout {
 // Load the pack's proxy rows into the 128-byte-swizzled Q tile:
 // row r = head * Lp + t holds q at position n - L + t (zero if t >= L).
 template <int D>
-__device__ void load_rows(uint8_t* sQ, const ProxyArgs& A, const Pack& P) {
+__device__ void load_rows(uint8_t* sQ, const ProxyArgs& A, const GroupPack& P, const SeqInfo& S, int L) {
   constexpr int kC16 = D / 8;
-  const int n = A.n;
+  const int n = S.n;
   for (int idx = threadIdx.x; idx < kRows * kC16; idx += blockDim.x) {
     const int r = idx / kC16, c16 = idx % kC16;
     const int hh = r / A.Lp, t = r % A.Lp;
     uint4 val = make_uint4(0, 0, 0, 0);
-    if (hh < P.nh && t < A.L) {
-      const int64_t row = (int64_t)P.qh[hh] * n + (n - A.L + t);
+    if (hh < P.nh && t < L) {
+      const int64_t row = (int64_t)A.Hq * S.tok0 + (int64_t)P.h[hh] * n + (n - L + t);
       val = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(A.q) + row * D * 2) + c16);
     }
     *reinterpret_cast<uint4*>(sQ + (c16 >> 3) * PLayout<D>::kQChunk + sw128_offset(r, c16 & 7)) = val;
@@ -122,7 +123,8 @@ __device__ void load_rows(uint8_t* sQ, const ProxyArgs& A, const Pack& P) {
 // (S^T = K Q^T, lane = key).  LP: rows per head (32, 64 or 128).
 template <int D, int MODE, int LP>
 __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
-    proxy_kernel(const __grid_constant__ CUtensorMap tk, const ProxyArgs A, const __grid_constant__ PackTable PT) {
+    proxy_kernel(const __grid_constant__ CUtensorMap tk, const ProxyArgs A, const __grid_constant__ PackTable PT,
+                 const __grid_constant__ SeqTable ST) {
   using Ly = PLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -137,12 +139,19 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
   uint64_t* sempty = bars + 2 * kKStages + 2;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pack_id = blockIdx.x / A.nchunks, chunk = blockIdx.x % A.nchunks;
-  const Pack& P = PT.p[pack_id];
-  const int n = A.n;
-  const int tiles_per = (A.ntiles + A.nchunks - 1) / A.nchunks;
+  // sequence, group pack and key chunk of this CTA
+  const int ts = seq_search(ST.count, [&](int x) { return ST.s[x].chunk0; }, (int64_t)blockIdx.x);
+  const SeqInfo& SI = ST.s[ts];
+  const int local = (int)blockIdx.x - SI.chunk0;
+  const int gp = local / SI.chunks, chunk = local % SI.chunks;
+  const GroupPack& P = PT.p[gp];
+  const int pack_id = ts * PT.n_gp + gp;
+  const int n = SI.n;
+  const int L = min(A.last_q, n);
+  const int ntiles = n_tiles(n);
+  const int tiles_per = (ntiles + SI.chunks - 1) / SI.chunks;
   const int tile0 = chunk * tiles_per;
-  const int tile1 = min(A.ntiles, tile0 + tiles_per);
+  const int tile1 = min(ntiles, tile0 + tiles_per);
   const int T = max(0, tile1 - tile0);
   const int nrows = P.nh * A.Lp;              // rows holding data (<= 256)
   const int nrt = (nrows + 127) / 128;        // MODE 1: row tiles
@@ -164,7 +173,7 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
     misc[2] = 0;
     fence_mbar_init();
   }
-  load_rows<D>(sQ, A, P);
+  load_rows<D>(sQ, A, P, SI, L);
   if (MODE == 2)
     for (int r = threadIdx.x; r < kRows; r += blockDim.x) sLse[r] = A.lse2[(int64_t)pack_id * kRows + r];
   tc_fence_before();
@@ -173,6 +182,7 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
   const uint32_t tmem = misc[0];
 
   if (warp == PW::kProd) {
+    const int32_t krow0 = A.Hkv * SI.tok0 + P.g * n;  // row of key 0 of this group in the [rows, d] view of k
     if (lane == 0 && T > 0) {
       tma_prefetch_desc(&tk);
       bool ok = true;
@@ -183,7 +193,8 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
         mbar_arrive_expect_tx(&kfull[st], Ly::kKTile);
         uint8_t* dst = sK + st * Ly::kKTile;
         for (int s = 0; s < 2; ++s)
-          for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384 + s * 8192, &tk, &kfull[st], 64 * c, k0 + 64 * s, P.kvh);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(dst + c * 16384 + s * 8192, &tk, &kfull[st], 64 * c, krow0 + k0 + 64 * s, 0);
       }
       if (!ok) { misc[2] = 1; set_err(A.err, kErrTimeout); }
     }
@@ -235,8 +246,8 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
       const int rt = warp >> 2;
       const int r = rt * 128 + (warp & 3) * 32 + lane;
       const int t = r % A.Lp;
-      const bool row_ok = r < nrows && t < A.L;
-      const int i = n - A.L + t;  // query position of this row
+      const bool row_ok = r < nrows && t < L;
+      const int i = n - L + t;  // query position of this row
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < T; ++j) {
         if (misc[2]) { ok = false; break; }
@@ -277,7 +288,7 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
         }
       }
       if (rt * 128 < kRows)
-        A.part[((int64_t)pack_id * A.nchunks + chunk) * kRows + r] = make_float2(row_ok ? m : -INFINITY, row_ok ? l : 0.f);
+        A.part[(int64_t)blockIdx.x * kRows + r] = make_float2(row_ok ? m : -INFINITY, row_ok ? l : 0.f);
     } else {
       // ------------------------------------------------ per-key Ã, column sums, diagonal bins
       // Sums are kept as (max, sum of 2^(x - max)) pairs over log2
@@ -313,7 +324,7 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
             float mx = -INFINITY;
             // every (row, key) of this chunk valid (warp-uniform): all 32 rows are
             // proxy rows and every key lies at or before the chunk's first row
-            const bool chunk_valid = cc * 32 + 31 < A.L && kb0 + 31 <= n - A.L + cc * 32;
+            const bool chunk_valid = cc * 32 + 31 < L && kb0 + 31 <= n - L + cc * 32;
             if (chunk_valid) {
 #pragma unroll
               for (int tp = 0; tp < 32; ++tp) {
@@ -324,7 +335,7 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
 #pragma unroll
               for (int tp = 0; tp < 32; ++tp) {
                 const int t = cc * 32 + tp;
-                const bool valid = t < A.L && key <= n - A.L + t && key < n;
+                const bool valid = t < L && key <= n - L + t && key < n;
                 xv[tp] = valid ? fmaf(__uint_as_float(sraw[tp]), c2, -sLse[r0 + tp]) : -INFINITY;
                 mx = fmaxf(mx, xv[tp]);
               }
@@ -383,15 +394,16 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sempty[sb]);
         const int kb = kb0 >> 5;  // key block index
+        const int nkb = 4 * n_tiles(n);
 #pragma unroll
         for (int x = 0; x < HPH; ++x) {
           const int hh = ch * HPH + x;
           if (hh >= P.nh) continue;
-          const int64_t slot = P.slot[hh];
-          if (key < n) A.colsum[slot * n + key] = col_log[x];
+          const int64_t slot = P.x[hh];
+          if (key < n) A.colsum[(int64_t)A.n_vs * SI.tok0 + slot * n + key] = col_log[x];
+          const int64_t rrow = (int64_t)A.n_vs * SI.kb0 + slot * (nkb + LB) + (kb + LB);
 #pragma unroll
-          for (int m = 0; m <= LB; ++m)
-            A.rpart[((slot * (A.nkb + LB) + (kb - m + LB)) * (LB + 1) + m) * 32 + lane] = bin_log[x][m];
+          for (int m = 0; m <= LB; ++m) A.rpart[((rrow - m) * (LB + 1) + m) * 32 + lane] = bin_log[x][m];
         }
       }
     }
@@ -405,15 +417,18 @@ __global__ void __launch_bounds__(ProxyWarps<MODE, LP>::kThreads, 1)
   }
 }
 
-// lse2 per row = log2-domain log-sum-exp over the chunks' partials.
-__global__ void proxy_lse_kernel(const float2* part, int nchunks, float* lse2) {
+// lse2 per row = log2-domain log-sum-exp over the partials of the pack's CTAs.
+__global__ void proxy_lse_kernel(const float2* part, int n_gp, const __grid_constant__ SeqTable ST, float* lse2) {
   const int pk = blockIdx.x, r = threadIdx.x;
+  const SeqInfo& S = ST.s[pk / n_gp];
+  const int64_t c0 = S.chunk0 + (int64_t)(pk % n_gp) * S.chunks;
+  const int nchunks = S.chunks;
   float m = -INFINITY;
-  for (int c = 0; c < nchunks; ++c) m = fmaxf(m, part[((int64_t)pk * nchunks + c) * kRows + r].x);
+  for (int c = 0; c < nchunks; ++c) m = fmaxf(m, part[(c0 + c) * kRows + r].x);
   float l = 0.f;
   if (m != -INFINITY)
     for (int c = 0; c < nchunks; ++c) {
-      const float2 v = part[((int64_t)pk * nchunks + c) * kRows + r];
+      const float2 v = part[(c0 + c) * kRows + r];
       if (v.x != -INFINITY) l += v.y * exp2f(v.x - m);
     }
   lse2[(int64_t)pk * kRows + r] = (l > 0.f) ? m + log2f(l) : INFINITY;  // +inf -> exp2(s - lse) = 0 for empty rows
@@ -421,35 +436,43 @@ __global__ void proxy_lse_kernel(const float2* part, int nchunks, float* lse2) {
 
 // log2 r_δ = log-sum-exp over the bins (y = n - L - δ) of the key blocks that
 // own them, m = 0..LB in order.
-// One thread per offset d of a slot (slots along the grid's y dimension).
-__global__ void slash_finalize_kernel(const float* rpart, int n, int L, int LB, int nkb, int slots, int mode,
-                                      float* r) {
-  for (int64_t slot = blockIdx.y; slot < slots; slot += gridDim.y)
-  for (int d = blockIdx.x * blockDim.x + threadIdx.x; d < n; d += gridDim.x * blockDim.x) {
-    const int y = n - L - d;
-    const int beta = (y >= 0) ? (y >> 5) : -((31 - y) >> 5);  // floor(y / 32)
-    const int ln = y - 32 * beta;
-    const float* src = rpart + ((slot * (nkb + LB) + (beta + LB)) * (LB + 1)) * 32 + ln;
-    float v[5];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int m = 0; m < 5; ++m) {
-      if (m > LB) break;
-      const int kb = beta + m;
-      v[m] = (kb < 0 || kb >= nkb) ? -INFINITY : __ldg(src + m * 32);
-      mx = fmaxf(mx, v[m]);
-    }
-    float s = 0.f;
-    if (mx != -INFINITY) {
+// One thread per offset d of a slot (slots of the launch along the grid's y
+// dimension, n_vs per sequence).
+__global__ void slash_finalize_kernel(const float* rpart, const __grid_constant__ SeqTable ST, int n_vs, int last_q,
+                                      int LB, int mode, float* r) {
+  const int slots = ST.count * n_vs;
+  for (int sl = blockIdx.y; sl < slots; sl += gridDim.y) {
+    const SeqInfo& S = ST.s[sl / n_vs];
+    const int64_t x = sl % n_vs;
+    const int n = S.n, L = min(last_q, n), nkb = 4 * n_tiles(n);
+    const int64_t rbase = (int64_t)n_vs * S.kb0 + x * (nkb + LB);
+    float* out = r + (int64_t)n_vs * S.tok0 + x * n;
+    for (int d = blockIdx.x * blockDim.x + threadIdx.x; d < n; d += gridDim.x * blockDim.x) {
+      const int y = n - L - d;
+      const int beta = (y >= 0) ? (y >> 5) : -((31 - y) >> 5);  // floor(y / 32)
+      const int ln = y - 32 * beta;
+      const float* src = rpart + ((rbase + beta + LB) * (LB + 1)) * 32 + ln;
+      float v[5];
+      float mx = -INFINITY;
 #pragma unroll
       for (int m = 0; m < 5; ++m) {
         if (m > LB) break;
-        s += v[m] != -INFINITY ? exp2f(v[m] - mx) : 0.f;
+        const int kb = beta + m;
+        v[m] = (kb < 0 || kb >= nkb) ? -INFINITY : __ldg(src + m * 32);
+        mx = fmaxf(mx, v[m]);
       }
+      float s = 0.f;
+      if (mx != -INFINITY) {
+#pragma unroll
+        for (int m = 0; m < 5; ++m) {
+          if (m > LB) break;
+          s += v[m] != -INFINITY ? exp2f(v[m] - mx) : 0.f;
+        }
+      }
+      float lr = s > 0.f ? mx + log2f(s) : -INFINITY;
+      if ((mode & MSA_PROXY_SLASH_MEAN) && lr != -INFINITY) lr -= log2f((float)min(L, n - d));  // legal pairs of offset d
+      out[d] = lr;
     }
-    float lr = s > 0.f ? mx + log2f(s) : -INFINITY;
-    if ((mode & MSA_PROXY_SLASH_MEAN) && lr != -INFINITY) lr -= log2f((float)min(L, n - d));  // legal pairs of offset d
-    r[slot * n + d] = lr;
   }
 }
 
@@ -472,31 +495,38 @@ struct TopkJob {
   int32_t descending;  // write the list in descending index order
 };
 
-// Both score vectors of every slot: block 2*slot selects the verticals from
-// the column sums, block 2*slot+1 the slashes from the slash sums.
+// Both score vectors of every slot of the launch: vector 2*sl selects the
+// verticals from the column sums, 2*sl+1 the slashes from the slash sums
+// (launch slot sl = table entry * n_vs + head rank).
 struct TopkArgs {
   const float* colsum;
   const float* slashsum;
   msa_vs_index out;
-  int32_t vk, sk;
+  int32_t vk, sk, n_vs, pad;
 };
 
-__device__ __forceinline__ TopkJob topk_job(const TopkArgs& a, int n, int vec) {
-  const int slot = vec >> 1;
-  const int words = (n + 31) / 32;
+// The job of vector `vec`; n: the length of its sequence.
+__device__ __forceinline__ TopkJob topk_job(const TopkArgs& a, const SeqTable& st, int vec, int& n) {
+  const int sl = vec >> 1;
+  const SeqInfo& S = st.s[sl / a.n_vs];
+  const int64_t x = sl % a.n_vs;
+  n = S.n;
+  const int64_t slot = (int64_t)S.seq * a.n_vs + x;                     // slot of the output lists
+  const int64_t vbase = (int64_t)a.n_vs * S.tok0 + x * n;              // score vectors
+  const int64_t wbase = (int64_t)a.n_vs * S.word0 + x * n_words(n);    // bitmaps
   TopkJob J;
   if ((vec & 1) == 0) {
-    J.vals = a.colsum + (int64_t)slot * n;
-    J.list = a.out.vertical + (int64_t)slot * a.out.v_cap;
+    J.vals = a.colsum + vbase;
+    J.list = a.out.vertical + slot * a.out.v_cap;
     J.cnt = a.out.vertical_cnt + slot;
-    J.bits = a.out.vertical_bits + (int64_t)slot * words;
+    J.bits = a.out.vertical_bits + wbase;
     J.k = a.vk;
     J.descending = 0;
   } else {
-    J.vals = a.slashsum + (int64_t)slot * n;
-    J.list = a.out.slash + (int64_t)slot * a.out.s_cap;
+    J.vals = a.slashsum + vbase;
+    J.list = a.out.slash + slot * a.out.s_cap;
     J.cnt = a.out.slash_cnt + slot;
-    J.bits = a.out.slash_bits + (int64_t)slot * words;
+    J.bits = a.out.slash_bits + wbase;
     J.k = a.sk;
     J.descending = 1;
   }
@@ -526,11 +556,12 @@ constexpr int kTopkWarps = kTopkThreads / 32;
 static_assert(kBins <= kTopkThreads && kBins % 32 == 0, "one bin per thread");
 
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads, 2)
-    topk_kernel(const TopkArgs args, int n) {
+    topk_kernel(const TopkArgs args, const __grid_constant__ SeqTable ST) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  const TopkJob J = topk_job(args, n, (int)(blockIdx.x / kTopkCluster));
+  int n = 0;
+  const TopkJob J = topk_job(args, ST, (int)(blockIdx.x / kTopkCluster), n);
   __shared__ int whist[kTopkWarps][kBins];  // per-warp histograms of the current pass
   __shared__ int hist[kBins];        // this CTA's histogram of the current pass (read cluster-wide)
   __shared__ int ghist[kBins];       // the cluster's histogram
@@ -725,11 +756,16 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
 
 // Dilated slash coverage: bit z = any offset of D in [n-1-z, n+62-z], z < n+63.
 // One thread per output bit, words assembled with a warp ballot.
-__global__ void slash_cover_kernel(const uint32_t* dbits, int n, int words, int cover_words, int slots,
+__global__ void slash_cover_kernel(const uint32_t* dbits, const __grid_constant__ SeqTable ST, int n_vs,
                                    uint32_t* cover) {
-  const int zt = cover_words * 32;  // a multiple of 32: the ballot below sees whole warps
-  for (int64_t slot = blockIdx.y; slot < slots; slot += gridDim.y) {
-    const uint32_t* D = dbits + slot * words;
+  const int slots = ST.count * n_vs;
+  for (int sl = blockIdx.y; sl < slots; sl += gridDim.y) {
+    const SeqInfo& S = ST.s[sl / n_vs];
+    const int64_t x = sl % n_vs;
+    const int n = S.n, cover_words = n_cover_words(n);
+    const uint32_t* D = dbits + (int64_t)n_vs * S.word0 + x * n_words(n);
+    uint32_t* out = cover + (int64_t)n_vs * S.cword0 + x * cover_words;
+    const int zt = cover_words * 32;  // a multiple of 32: the ballot below sees whole warps
     for (int z = blockIdx.x * blockDim.x + threadIdx.x; z < zt; z += gridDim.x * blockDim.x) {
       bool any = false;
       if (z < n + 63) {
@@ -737,14 +773,14 @@ __global__ void slash_cover_kernel(const uint32_t* dbits, int n, int words, int 
         lo = lo < 0 ? 0 : lo;
         hi = hi > n - 1 ? n - 1 : hi;
         for (int w = lo >> 5; w <= (hi >> 5) && lo <= hi; ++w) {
-          uint32_t x = __ldg(D + w);
-          if (w == (lo >> 5)) x &= 0xFFFFFFFFu << (lo & 31);
-          if (w == (hi >> 5)) x &= 0xFFFFFFFFu >> (31 - (hi & 31));
-          if (x) { any = true; break; }
+          uint32_t v = __ldg(D + w);
+          if (w == (lo >> 5)) v &= 0xFFFFFFFFu << (lo & 31);
+          if (w == (hi >> 5)) v &= 0xFFFFFFFFu >> (31 - (hi & 31));
+          if (v) { any = true; break; }
         }
       }
       const unsigned b = __ballot_sync(0xFFFFFFFFu, any);
-      if ((threadIdx.x & 31) == 0) cover[slot * cover_words + z / 32] = b;
+      if ((threadIdx.x & 31) == 0) out[z / 32] = b;
     }
   }
 }
@@ -807,58 +843,6 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 int padded_rows(int L) { return L <= 32 ? 32 : (L <= 64 ? 64 : 128); }
 
-struct VSPlan {
-  std::vector<Pack> packs;
-  int L, Lp, LB, ntiles, nkb, nchunks1, nchunks2, slots;
-  size_t off_part, off_lse, off_col, off_slash, off_rpart, total;
-};
-
-VSPlan plan_vs(const msa_shape& s, const int32_t* heads, int32_t n_heads, const msa_head_cfg& cfg, int sms) {
-  VSPlan P;
-  P.L = cfg.last_q < s.n ? cfg.last_q : s.n;
-  P.Lp = padded_rows(P.L);
-  P.LB = P.Lp / 32;
-  const int per_pack = kRows / P.Lp < kPackMaxHeads ? kRows / P.Lp : kPackMaxHeads;
-  const int g = s.Hq / s.Hkv;
-  if (heads) {
-    for (int b = 0; b < s.B; ++b)
-      for (int kv = 0; kv < s.Hkv; ++kv) {
-        Pack cur;
-        memset(&cur, 0, sizeof(cur));
-        cur.kvh = b * s.Hkv + kv;
-        for (int x = 0; x < n_heads; ++x) {
-          if (heads[x] / g != kv) continue;
-          cur.slot[cur.nh] = b * n_heads + x;
-          cur.qh[cur.nh] = b * s.Hq + heads[x];
-          if (++cur.nh == per_pack) {
-            P.packs.push_back(cur);
-            cur.nh = 0;
-          }
-        }
-        if (cur.nh) P.packs.push_back(cur);
-      }
-  }
-  P.ntiles = ceil_div(s.n, 128);
-  P.nkb = 4 * P.ntiles;
-  const int np = P.packs.empty() ? 1 : (int)P.packs.size();
-  auto chunks = [&](int target) {
-    int c = ceil_div(target, np);
-    if (c > P.ntiles) c = P.ntiles;
-    return c < 1 ? 1 : c;
-  };
-  P.nchunks1 = chunks(sms);
-  P.nchunks2 = chunks(sms);
-  P.slots = s.B * n_heads;
-  size_t off = 0;
-  P.off_part = off; off = align256(off + sizeof(float2) * (size_t)np * P.nchunks1 * kRows);
-  P.off_lse = off;  off = align256(off + sizeof(float) * (size_t)np * kRows);
-  P.off_col = off;  off = align256(off + sizeof(float) * (size_t)P.slots * s.n);
-  P.off_slash = off; off = align256(off + sizeof(float) * (size_t)P.slots * s.n);
-  P.off_rpart = off; off = align256(off + sizeof(float) * (size_t)P.slots * (P.nkb + P.LB) * (P.LB + 1) * 32);
-  P.total = off + 256;
-  return P;
-}
-
 int sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -866,81 +850,164 @@ int sm_count() {
   return sms;
 }
 
+// One index pass over a list of sequences: the group packs (the same for
+// every sequence), and the launches, each over at most kMaxSeqs sequences
+// with their CTA prefixes; K chunks are sized so that all packs of all
+// sequences together make about one CTA per SM.
+struct VSPlan {
+  PackTable pt;
+  int n_gp = 0, Lp = 0, LB = 0, v_cap = 0, s_cap = 0;
+  std::vector<SeqInfo> seqs;       // token order (kb0 filled)
+  std::vector<SeqTable> launches;  // chunk0 / chunks filled
+  std::vector<int> ctas;           // CTAs per launch
+  int max_ctas = 0, max_packs = 0;
+  int64_t tokens = 0, kbs = 0;
+  size_t off_part = 0, off_lse = 0, off_col = 0, off_slash = 0, off_rpart = 0, total = 0;
+};
+
+// heads null: the worst case for sizing (every head in its own KV group).
+bool plan_vs(const msa_shape& s, const int32_t* heads, int32_t n_heads, const msa_head_cfg& cfg, int sms,
+             const std::vector<SeqInfo>* seq_list, VSPlan& P) {
+  P.seqs = seq_list ? *seq_list : uniform_seqs(s, 0);
+  int n_max = 1;
+  for (const SeqInfo& x : P.seqs) n_max = x.n > n_max ? x.n : n_max;
+  const int L_max = cfg.last_q < n_max ? cfg.last_q : n_max;
+  P.Lp = padded_rows(L_max);
+  P.LB = P.Lp / 32;
+  P.v_cap = cfg.n_vertical < n_max ? cfg.n_vertical : n_max;
+  P.s_cap = cfg.n_slash < n_max ? cfg.n_slash : n_max;
+  for (SeqInfo& x : P.seqs) {
+    x.kb0 = (int32_t)P.kbs;
+    P.kbs += 4 * n_tiles(x.n) + P.LB;
+    P.tokens += x.n;
+  }
+  // group packs
+  memset(&P.pt, 0, sizeof(P.pt));
+  const int per_pack = kRows / P.Lp < kPackMaxHeads ? kRows / P.Lp : kPackMaxHeads;
+  if (heads) {
+    const int g = s.Hq / s.Hkv;
+    for (int kv = 0; kv < s.Hkv; ++kv) {
+      GroupPack cur;
+      memset(&cur, 0, sizeof(cur));
+      cur.g = kv;
+      for (int x = 0; x < n_heads; ++x) {
+        if (heads[x] / g != kv) continue;
+        cur.x[cur.nh] = x;
+        cur.h[cur.nh] = heads[x];
+        if (++cur.nh == per_pack) {
+          if (P.n_gp == kMaxGroupPacks) return false;
+          P.pt.p[P.n_gp++] = cur;
+          cur.nh = 0;
+        }
+      }
+      if (cur.nh) {
+        if (P.n_gp == kMaxGroupPacks) return false;
+        P.pt.p[P.n_gp++] = cur;
+      }
+    }
+  } else {
+    P.n_gp = n_heads;
+  }
+  P.pt.n_gp = P.n_gp;
+  // K chunks: about one CTA per SM over all packs of all sequences
+  int64_t tile_packs = 0;
+  for (const SeqInfo& x : P.seqs) tile_packs += (int64_t)P.n_gp * n_tiles(x.n);
+  const int64_t tpc = tile_packs > sms ? (tile_packs + sms - 1) / sms : 1;
+  std::vector<SeqInfo> live;
+  for (const SeqInfo& x : P.seqs)
+    if (x.n > 0) live.push_back(x);
+  for (size_t b = 0; b < live.size(); b += kMaxSeqs) {
+    SeqTable st;
+    memset(&st, 0, sizeof(st));
+    st.count = (int32_t)(live.size() - b < (size_t)kMaxSeqs ? live.size() - b : (size_t)kMaxSeqs);
+    int64_t ctas = 0;
+    for (int x = 0; x < st.count; ++x) {
+      SeqInfo si = live[b + x];
+      const int64_t nt = n_tiles(si.n);
+      int64_t ch = (nt + tpc - 1) / tpc;
+      ch = ch < 1 ? 1 : (ch > nt ? nt : ch);
+      si.chunks = (int32_t)ch;
+      si.chunk0 = (int32_t)ctas;
+      ctas += (int64_t)P.n_gp * ch;
+      st.s[x] = si;
+    }
+    if (ctas > 0x7FFFFFFF) return false;
+    P.launches.push_back(st);
+    P.ctas.push_back((int)ctas);
+    P.max_ctas = (int)ctas > P.max_ctas ? (int)ctas : P.max_ctas;
+    P.max_packs = st.count * P.n_gp > P.max_packs ? st.count * P.n_gp : P.max_packs;
+  }
+  size_t off = 0;
+  P.off_part = off; off = align256(off + sizeof(float2) * (size_t)(P.max_ctas > 0 ? P.max_ctas : 1) * kRows);
+  P.off_lse = off;  off = align256(off + sizeof(float) * (size_t)(P.max_packs > 0 ? P.max_packs : 1) * kRows);
+  P.off_col = off;  off = align256(off + sizeof(float) * (size_t)n_heads * (size_t)P.tokens);
+  P.off_slash = off; off = align256(off + sizeof(float) * (size_t)n_heads * (size_t)P.tokens);
+  P.off_rpart = off; off = align256(off + sizeof(float) * (size_t)n_heads * (size_t)P.kbs * (P.LB + 1) * 32);
+  P.total = off + 256;
+  return true;
+}
+
 template <int D, int MODE, int LP>
-msa_status launch_proxy(const CUtensorMap& tk, const ProxyArgs& a, const std::vector<Pack>& packs, int nchunks,
+msa_status launch_proxy(const CUtensorMap& tk, const ProxyArgs& a, const PackTable& pt, const SeqTable& st, int ctas,
                         cudaStream_t stream) {
   auto kern = proxy_kernel<D, MODE, LP>;
   const int smem = PLayout<D>::kAlloc;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return MSA_ERR_CUDA;
-  for (size_t base = 0; base < packs.size(); base += kMaxPacks) {
-    PackTable pt;
-    memset(&pt, 0, sizeof(pt));
-    const size_t cnt = packs.size() - base < (size_t)kMaxPacks ? packs.size() - base : (size_t)kMaxPacks;
-    for (size_t x = 0; x < cnt; ++x) pt.p[x] = packs[base + x];
-    ProxyArgs aa = a;
-    aa.part = a.part + base * nchunks * kRows;
-    aa.lse2 = a.lse2 + base * kRows;
-    aa.nchunks = nchunks;
-    kern<<<(unsigned)(cnt * nchunks), ProxyWarps<MODE, LP>::kThreads, smem, stream>>>(tk, aa, pt);
-    note_launch();
-    if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
-  }
-  return MSA_OK;
+  if (ctas <= 0) return MSA_OK;
+  kern<<<(unsigned)ctas, ProxyWarps<MODE, LP>::kThreads, smem, stream>>>(tk, a, pt, st);
+  note_launch();
+  return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 template <int D>
-msa_status launch_scores(int Lp, const CUtensorMap& tk, const ProxyArgs& a, const std::vector<Pack>& packs,
-                         int nchunks, cudaStream_t stream) {
-  if (Lp == 32) return launch_proxy<D, 2, 32>(tk, a, packs, nchunks, stream);
-  if (Lp == 64) return launch_proxy<D, 2, 64>(tk, a, packs, nchunks, stream);
-  return launch_proxy<D, 2, 128>(tk, a, packs, nchunks, stream);
+msa_status launch_scores(int Lp, const CUtensorMap& tk, const ProxyArgs& a, const PackTable& pt, const SeqTable& st,
+                         int ctas, cudaStream_t stream) {
+  if (Lp == 32) return launch_proxy<D, 2, 32>(tk, a, pt, st, ctas, stream);
+  if (Lp == 64) return launch_proxy<D, 2, 64>(tk, a, pt, st, ctas, stream);
+  return launch_proxy<D, 2, 128>(tk, a, pt, st, ctas, stream);
 }
 
 }  // namespace
 
-size_t vs_index_ws_bytes(const msa_shape& s, const msa_head_cfg& cfg, int32_t n_heads) {
-  std::vector<int32_t> heads((size_t)n_heads);
-  for (int x = 0; x < n_heads; ++x) heads[(size_t)x] = x % s.Hq;
-  // pack count is largest when every head sits in its own KV group
-  msa_shape worst = s;
-  VSPlan P = plan_vs(worst, nullptr, n_heads, cfg, 1);
-  const int packs_max = s.B * n_heads;
-  const int sms = sm_count();
-  const int nch = ceil_div(sms, 1) < P.ntiles ? sms : P.ntiles;
-  size_t total = 0;
-  total += align256(sizeof(float2) * (size_t)packs_max * (nch < 1 ? 1 : nch) * kRows);
-  total += align256(sizeof(float) * (size_t)packs_max * kRows);
-  total += align256(sizeof(float) * (size_t)s.B * n_heads * s.n) * 2;
-  total += align256(sizeof(float) * (size_t)s.B * n_heads * (P.nkb + P.LB) * (P.LB + 1) * 32);
-  return total + 1024;
+size_t vs_index_ws_bytes(const msa_shape& s, const msa_head_cfg& cfg, const int32_t* heads, int32_t n_heads,
+                         const std::vector<SeqInfo>* seqs) {
+  VSPlan P;
+  if (!plan_vs(s, heads, n_heads, cfg, sm_count(), seqs, P)) return 0;
+  // without the heads the pack count is the worst case; so is the CTA count
+  // (at most one per SM plus one per pack and sequence)
+  if (!heads) {
+    const size_t n_seq = P.seqs.size() < (size_t)kMaxSeqs ? P.seqs.size() : (size_t)kMaxSeqs;
+    const size_t ctas = (size_t)sm_count() + (size_t)n_heads * n_seq;
+    const size_t extra = align256(sizeof(float2) * ctas * kRows) + align256(sizeof(float) * (size_t)n_heads * n_seq * kRows);
+    return P.total + extra + 1024;
+  }
+  return P.total + 1024;
 }
 
 msa_status run_vs_index(const msa_shape& s, const void* q, const void* k, const int32_t* heads, int32_t n_heads,
                         const msa_head_cfg& cfg, const msa_vs_index& out, void* ws, size_t ws_bytes,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const std::vector<SeqInfo>* seqs) {
   if (cfg.last_q > 128) return MSA_ERR_UNSUPPORTED;
   if (!out.vertical || !out.vertical_cnt || !out.slash || !out.slash_cnt || !out.vertical_bits || !out.slash_bits ||
       !out.slash_cover)
     return MSA_ERR_INVALID_ARG;
-  const int vcap = cfg.n_vertical < s.n ? cfg.n_vertical : s.n;
-  const int scap = cfg.n_slash < s.n ? cfg.n_slash : s.n;
-  if (out.v_cap < vcap || out.s_cap < scap) return MSA_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < vs_index_ws_bytes(s, cfg, n_heads)) return MSA_ERR_WORKSPACE_TOO_SMALL;
-  VSPlan P = plan_vs(s, heads, n_heads, cfg, sm_count());
-  if (P.total > ws_bytes) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  VSPlan P;
+  if (!plan_vs(s, heads, n_heads, cfg, sm_count(), seqs, P)) return MSA_ERR_UNSUPPORTED;
+  if (out.v_cap < P.v_cap || out.s_cap < P.s_cap) return MSA_ERR_INVALID_ARG;
+  if (!ws || P.total + 256 > ws_bytes) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  if (!rows_fit(s.Hq, P.seqs)) return MSA_ERR_UNSUPPORTED;
   uint8_t* w = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~(uintptr_t)255);
-  if (P.total + 256 > ws_bytes) return MSA_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap tk;
-  if (!make_bf16_map(&tk, k, (int64_t)s.B * s.Hkv, s.n, s.d_h, 64)) return MSA_ERR_CUDA;
+  if (!make_bf16_map(&tk, k, 1, (int64_t)s.Hkv * P.tokens, s.d_h, 64)) return MSA_ERR_CUDA;
   ProxyArgs a;
   memset(&a, 0, sizeof(a));
   a.q = q;
-  a.n = s.n;
   a.d = s.d_h;
-  a.L = P.L;
   a.Lp = P.Lp;
-  a.ntiles = P.ntiles;
-  a.nkb = P.nkb;
+  a.last_q = cfg.last_q;
+  a.Hq = s.Hq;
+  a.Hkv = s.Hkv;
+  a.n_vs = n_heads;
   a.mode = cfg.proxy;
   const float scale = s.scale > 0.f ? s.scale : 1.0f / sqrtf((float)s.d_h);
   a.c2 = scale * 1.4426950408889634f;
@@ -951,46 +1018,54 @@ msa_status run_vs_index(const msa_shape& s, const void* q, const void* k, const 
   a.err = device_error_word();
   if (!a.err) return MSA_ERR_CUDA;
   float* slashsum = reinterpret_cast<float*>(w + P.off_slash);
-  msa_status st;
-  // pass 1: row statistics
-  st = s.d_h == 128 ? launch_proxy<128, 1, 64>(tk, a, P.packs, P.nchunks1, stream)
-                    : launch_proxy<64, 1, 64>(tk, a, P.packs, P.nchunks1, stream);
-  if (st != MSA_OK) return st;
-  proxy_lse_kernel<<<(unsigned)P.packs.size(), kRows, 0, stream>>>(a.part, P.nchunks1, a.lse2);
-  note_launch();
-  if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
-  // pass 2: probabilities, column sums and diagonal bins
-  st = s.d_h == 128 ? launch_scores<128>(P.Lp, tk, a, P.packs, P.nchunks2, stream)
-                    : launch_scores<64>(P.Lp, tk, a, P.packs, P.nchunks2, stream);
-  if (st != MSA_OK) return st;
-  {
-    const int bx = (s.n + 255) / 256 < 1024 ? (s.n + 255) / 256 : 1024;
-    const int by = P.slots < 65535 ? P.slots : 65535;
-    slash_finalize_kernel<<<dim3((unsigned)bx, (unsigned)by), 256, 0, stream>>>(a.rpart, s.n, P.L, P.LB, P.nkb, P.slots,
-                                                                               cfg.proxy, slashsum);
+  int n_max = 1;
+  for (const SeqInfo& x : P.seqs) n_max = x.n > n_max ? x.n : n_max;
+  for (size_t L = 0; L < P.launches.size(); ++L) {
+    const SeqTable& st = P.launches[L];
+    const int ctas = P.ctas[L];
+    msa_status r;
+    // pass 1: row statistics
+    r = s.d_h == 128 ? launch_proxy<128, 1, 64>(tk, a, P.pt, st, ctas, stream)
+                     : launch_proxy<64, 1, 64>(tk, a, P.pt, st, ctas, stream);
+    if (r != MSA_OK) return r;
+    proxy_lse_kernel<<<(unsigned)(st.count * P.n_gp), kRows, 0, stream>>>(a.part, P.n_gp, st, a.lse2);
     note_launch();
     if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
-  }
-  // top-k for both score vectors of every slot
-  TopkArgs ta;
-  ta.colsum = a.colsum;
-  ta.slashsum = slashsum;
-  ta.out = out;
-  ta.vk = vcap;
-  ta.sk = scap;
-  topk_kernel<<<(unsigned)(P.slots * 2 * kTopkCluster), kTopkThreads, 0, stream>>>(ta, s.n);
-  note_launch();
-  if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
-  {
-    const int words = ceil_div(s.n, 32);
-    const int cw = ceil_div(s.n + 63, 32);
-    const int bx = (cw * 32 + 255) / 256 < 1024 ? (cw * 32 + 255) / 256 : 1024;
-    const int by = P.slots < 65535 ? P.slots : 65535;
-    slash_cover_kernel<<<dim3((unsigned)bx, (unsigned)by), 256, 0, stream>>>(out.slash_bits, s.n, words, cw, P.slots,
-                                                                            out.slash_cover);
+    // pass 2: probabilities, column sums and diagonal bins
+    r = s.d_h == 128 ? launch_scores<128>(P.Lp, tk, a, P.pt, st, ctas, stream)
+                     : launch_scores<64>(P.Lp, tk, a, P.pt, st, ctas, stream);
+    if (r != MSA_OK) return r;
+    const int slots = st.count * n_heads;
+    {
+      const int bx = (n_max + 255) / 256 < 1024 ? (n_max + 255) / 256 : 1024;
+      const int by = slots < 65535 ? slots : 65535;
+      slash_finalize_kernel<<<dim3((unsigned)bx, (unsigned)by), 256, 0, stream>>>(a.rpart, st, n_heads, cfg.last_q,
+                                                                                 P.LB, cfg.proxy, slashsum);
+      note_launch();
+      if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+    }
+    // top-k for both score vectors of every slot
+    TopkArgs ta;
+    memset(&ta, 0, sizeof(ta));
+    ta.colsum = a.colsum;
+    ta.slashsum = slashsum;
+    ta.out = out;
+    ta.vk = cfg.n_vertical;
+    ta.sk = cfg.n_slash;
+    ta.n_vs = n_heads;
+    topk_kernel<<<(unsigned)(slots * 2 * kTopkCluster), kTopkThreads, 0, stream>>>(ta, st);
     note_launch();
+    if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+    {
+      const int cw = n_cover_words(n_max);
+      const int bx = (cw * 32 + 255) / 256 < 1024 ? (cw * 32 + 255) / 256 : 1024;
+      const int by = slots < 65535 ? slots : 65535;
+      slash_cover_kernel<<<dim3((unsigned)bx, (unsigned)by), 256, 0, stream>>>(out.slash_bits, st, n_heads,
+                                                                              out.slash_cover);
+      note_launch();
+    }
+    if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   }
-  if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
   return MSA_OK;
 }
 

@@ -4,7 +4,8 @@ packed without padding, each with its own online indices and attention
 
 CPU: the host checks of cu_seqlens and the workspace rule (no launch).  GPU:
 every sequence's output, LSE and edge counts equal those of msa_prefill_layer
-run on that sequence alone (bit for bit), and every head of every packed
+run on that sequence alone (bit for bit), the launches of a batch do not grow
+with its number of sequences, and every head of every packed
 sequence matches the fp64 oracle: its online index against the oracle's index
 of that sequence alone, its rows on the packed layout against eq.(2) over the
 device's sets, and its edge count exactly.  Chunked prefill (MInference page
@@ -54,16 +55,19 @@ def test_varlen_rejects_bad_cu_seqlens(lib, cu):
     assert st == msa.MSA_ERR_INVALID_ARG
 
 
-def test_varlen_workspace_is_the_sum_of_the_sequences(lib):
-    """Each sequence owns a region of the workspace (so its indices survive the
-    call): the requirement is the sum of the sequences' layer workspaces,
-    each rounded up to 256 bytes, plus 256 for alignment."""
-    cu = _cu(LENS)
-    arr = (ctypes.c_int32 * len(cu))(*cu)
+def test_varlen_workspace_of_equal_lengths_is_the_uniform_batch(lib):
+    """One plan covers every sequence (sequence-major regions): a varlen batch
+    of equal lengths needs exactly the workspace of the uniform batch, and a
+    longer batch needs more."""
     tarr = msa.table_array(TABLE)
-    want = 256 + sum((lib.msa_layer_workspace(ctypes.byref(msa.Shape(1, HQ, HKV, n, D, 0.0)), tarr) + 255) // 256 * 256
-                     for n in LENS if n)
-    assert lib.msa_layer_varlen_workspace(ctypes.byref(_shape()), tarr, arr, len(LENS)) == want
+    cu = _cu([512, 512, 512])
+    arr = (ctypes.c_int32 * len(cu))(*cu)
+    uni = lib.msa_layer_workspace(ctypes.byref(msa.Shape(3, HQ, HKV, 512, D, 0.0)), tarr)
+    assert uni > 0 and lib.msa_layer_varlen_workspace(ctypes.byref(_shape()), tarr, arr, 3) == uni
+    cu2 = _cu(LENS)
+    arr2 = (ctypes.c_int32 * len(cu2))(*cu2)
+    more = lib.msa_layer_varlen_workspace(ctypes.byref(_shape()), tarr, arr2, len(LENS))
+    assert more > lib.msa_layer_workspace(ctypes.byref(msa.Shape(1, HQ, HKV, max(LENS), D, 0.0)), tarr)
 
 
 def _sequences(device):
@@ -163,18 +167,27 @@ def test_varlen_every_head_against_oracle(cuda_lib):
 @pytest.mark.timeout(900)
 def test_varlen_many_sequences_against_oracle(cuda_lib):
     """72 sequences of mixed lengths (empty, a single row, ragged tails, up to
-    5000 tokens): every head's index against the oracle and 96 seeded rows per
-    head and sequence (rows 0, 63, 64 and n-1 included)."""
+    5000 tokens) in one index pass and one attention launch: every head's
+    index against the oracle and 96 seeded rows per head and sequence (rows 0,
+    63, 64 and n-1 included)."""
     rng = np.random.default_rng(4242)
     lens = [int(x) for x in rng.integers(1, 5000, size=68)] + [0, 1, 64, 129]
     rng.shuffle(lens)
     seqs = [synth.random_qkv(1, HQ, HKV, n, D, seed=7000 + s, device="cuda") if n else None
             for s, n in enumerate(lens)]
+    l0 = cuda_lib.kernel_launches()
     layer, outs, lses, edges = _run_varlen(cuda_lib, seqs, lens, TABLE)
+    launches = cuda_lib.kernel_launches() - l0
     for s, n in enumerate(lens):
         if n:
             check_sequence_against_oracle(layer, s, n, *seqs[s], outs, lses, edges, TABLE,
                                           rows=synth.sample_rows(n, 96, seed=s), what="batch of 72")
+    # one index pass (6 Vertical-Slash + 4 Block-Sparse launches) and one attention launch,
+    # the same as for a batch of two sequences
+    two = [s for s, n in enumerate(lens) if n][:2]
+    l0 = cuda_lib.kernel_launches()
+    _run_varlen(cuda_lib, [seqs[s] for s in two], [lens[s] for s in two], TABLE)
+    assert cuda_lib.kernel_launches() - l0 == launches == 11
 
 
 # ----------------------------------------------------------------- chunked rows
