@@ -575,7 +575,51 @@ def extra_layers(msa, synth, device, stream, names=("ashape128k", "million"), re
         out[nm] = rec
         del r
         torch.cuda.empty_cache()
+    out["varlen_mixed64"] = varlen_batch(msa, synth, device, stream, reps=reps)
     return out
+
+
+def varlen_batch(msa, synth, device, stream, n_seqs=64, lo=1024, hi=16384, seed=77, reps=3):
+    """A varlen batch (cost-model page §2.2): n_seqs sequences with seeded
+    log-uniform lengths in [lo, hi], each the mixed-pattern generator and
+    table, packed back to back; one msa_prefill_layer_varlen call (one index
+    pass and one attention launch over all sequences), timed after a warm-up."""
+    rng = np.random.default_rng(seed)
+    lens = [int(x) for x in np.exp(rng.uniform(np.log(lo), np.log(hi), size=n_seqs))]
+    ws = [synth.make_workload("mixed", device=device, n=n, seed=3000 + i) for i, n in enumerate(lens)]
+    sh = ws[0]["shape"]
+    table = ws[0]["table"]
+    q = msa.pack_varlen([w["q"][0] for w in ws])
+    k = msa.pack_varlen([w["k"][0] for w in ws])
+    v = msa.pack_varlen([w["v"][0] for w in ws])
+    del ws
+    cu = [0] + [int(x) for x in np.cumsum(lens)]
+    layer = msa.VarlenLayer(table, cu, sh["Hq"], sh["Hkv"], sh["d"], device)
+    edges = torch.zeros(n_seqs * sh["Hq"], dtype=torch.int64, device=device)
+    o = layer(q, k, v, edges=edges)
+    torch.cuda.synchronize()
+    flops = 4.0 * float(edges.sum().item()) * sh["d"]
+    l0 = msa.kernel_launches()
+    layer(q, k, v, o=o)
+    launches = msa.kernel_launches() - l0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ts = []
+    for _ in range(reps):
+        a.record(stream)
+        layer(q, k, v, o=o)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    assert msa.poll_device_status() == 0
+    ms = statistics.median(ts)
+    dense = sum(n * (n + 1) / 2 for n in lens) * sh["Hq"]
+    rec = {"sequences": n_seqs, "tokens": cu[-1], "lengths": f"log-uniform in [{lo}, {hi}] (seed {seed})",
+           "heads": sh["Hq"], "kv_heads": sh["Hkv"], "d_h": sh["d"], "table": "mixed (A-shape : VS : BS = 1 : 6 : 1)",
+           "ms_per_batch": round(ms, 4), "effective_tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+           "density": round(float(edges.sum().item()) / dense, 4), "launches_per_batch": int(launches)}
+    del q, k, v, o, layer
+    torch.cuda.empty_cache()
+    return rec
 
 
 def dense_and_cold(runs, msa, per_layer, stream, reps=2):

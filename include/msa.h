@@ -274,13 +274,14 @@ MSA_API msa_status msa_layer_attend_rows(const msa_shape* shape, const void* q, 
  * starting at element H * cu_seqlens[s] * d_h (q, o: H = Hq; k, v: H = Hkv);
  * lse likewise as [Hq, n_s] blocks at Hq * cu_seqlens[s]; edges: [n_seqs, Hq]
  * counters (ADDED to).  shape gives Hq, Hkv, d_h and scale for every sequence
- * (its B and n are ignored).  Every sequence runs as msa_prefill_layer with
- * B = 1 and n = n_s on its own segment, in order on `stream`, in its own
- * region of `ws`: its own online indices, its own attention, no key of another
- * sequence.  Requires ws_bytes >= msa_layer_varlen_workspace(...) (the sum of
- * the sequences' layer workspaces).  Errors: invalid cu_seqlens ->
- * MSA_ERR_INVALID_ARG before anything is launched; otherwise the first
- * failing sequence's status (earlier sequences have been queued). */
+ * (its B and n are ignored).  Every sequence gets its own online indices and
+ * its own attention (no index, window or tile reaches another sequence's
+ * tokens), computed for the whole batch in one index pass and one attention
+ * launch per 128 sequences; the workspace holds every sequence's indices.
+ * Inputs must be finite: a key past a sequence's end that a tile covers is
+ * weighted by exactly zero.  Requires ws_bytes >= msa_layer_varlen_workspace
+ * (...) and Hq * total tokens < 2^31 (else MSA_ERR_UNSUPPORTED).  Errors:
+ * invalid cu_seqlens -> MSA_ERR_INVALID_ARG before anything is launched. */
 MSA_API size_t msa_layer_varlen_workspace(const msa_shape* shape, const msa_head_cfg* table,
                                           const int32_t* cu_seqlens, int32_t n_seqs);
 MSA_API msa_status msa_prefill_layer_varlen(const msa_shape* shape, const int32_t* cu_seqlens, int32_t n_seqs,
