@@ -22,13 +22,23 @@
 //              one sub-item's softmax runs, the tensor core works for the
 //              other, and neither issuer waits for the other's P;
 //   warps 0-7  softmax: warps 4X..4X+3 own sub-item X; thread r is query row r
-//              (TMEM lane r) with all 128 keys of a tile.  Masks (causal,
-//              pattern, sequence end) are applied before the max; O_X is
-//              rescaled in TMEM only when the max grows by more than 2^8; P
+//              (TMEM lane r) with all 128 keys of a tile.  Per-row masks
+//              (causal, A-shape sink and window) are applied before the max; O_X
+//              is rescaled in TMEM only when the max grows by more than 2^8; P
 //              (bf16 pairs) overwrites the first 64 columns of S_X.
+// In Vertical-Slash tiles, the keys that a whole 64-row half does not attend
+// are masked by the tensor core: such a tile gets one more K-step in
+// S_X = Q_X K^T, a one-hot 16-wide row selector per half (Q side, fixed)
+// against a per-key column of 0 or -BIG per half (K side, written by the
+// loader), so masked scores arrive as -BIG (exactly 0 after the exponential)
+// and attended scores unchanged.  (Range tiles mask whole 64-key words in the
+// softmax, where the extra K-step costs more than it saves.)
 // Every (i, j) pair enters the softmax at most once: a key lies in one tile
 // of the item, and masks drop what lies outside N(i) (MInference page §3.2
 // and §5.1 "boundary masks": set to -inf before the max).
+// A launch whose units all share one pattern runs a kernel compiled for that
+// pattern alone (the others' planner, loader and mask code left out); mixed
+// launches run the kernel that holds all three.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -56,7 +66,12 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kIdleNs = 256;          // poll interval of the planner's and loader's waits
+// P columns per TMEM store: small stores keep few packed values live next to
+// the 128 scores, which is what keeps the softmax free of register spills
+constexpr int kPChunk = 4;
 constexpr bool kTurnLock = true;            // sub-items take turns on each SMSP's MUFU
+constexpr uint16_t kBf16NegBig = 0xFF7Fu;   // -3.3895e38, the most negative finite bf16
+constexpr float kMaskedBelow = -1e30f;      // a raw score below this is a masked one
 
 
 // kTileRange: two 64-key segments (seg[0], seg[1]); kTileRange16: eight 16-key
@@ -69,9 +84,20 @@ struct TileDesc {
   int32_t kind;         // TileKind (kTileEnd: no more tiles in this item)
   uint8_t rule[2][2];   // A-shape row rule per [sub-item][segment]: bit0 j < sink, bit1 j > i - window
   uint8_t active[2];    // sub-item X attends some key of this tile
-  uint8_t pad[2];
+  uint8_t bias;         // some existing half leaves a key of this tile out: the masking K-step runs
+  uint8_t pad;
   uint32_t mask[4][4];  // per half 2X+h: bit k = key k of the tile may be attended
 };
+
+// A half of an active sub-item that exists and leaves out some key of the
+// tile: that tile's scores need the masking K-step.
+__device__ __forceinline__ uint8_t tile_needs_bias(const TileDesc& d, const int* ex) {
+  uint32_t all = ~0u;
+  for (int hh = 0; hh < 4; ++hh)
+    if (ex[hh] && d.active[hh >> 1])
+      all &= d.mask[hh][0] & d.mask[hh][1] & d.mask[hh][2] & d.mask[hh][3];
+  return all != ~0u ? 1 : 0;
+}
 
 enum {
   kBarQ = 0,
@@ -92,7 +118,10 @@ struct Layout {
   static constexpr int kRing = kQ + 2 * kTile;
   static constexpr int kDesc = kRing + kSlots * kTile;
   static constexpr int kBlk = kDesc + kDescSlots * (int)sizeof(TileDesc);  // Block-Sparse lists
-  static constexpr int kBars = kBlk + 4 * kMaxStagedBlocks * 4;
+  // masking K-step operands (128 rows x 16 bf16, unswizzled core matrices, 4 KB
+  // each): the two sub-items' row selectors, then two key-mask slots
+  static constexpr int kAug = kBlk + 4 * kMaxStagedBlocks * 4;
+  static constexpr int kBars = kAug + 4 * 4096;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 64;  // misc words: [0] TMEM base, [2] abort, [8..11] exponential turns
   // > 113 KB keeps one CTA per SM, so the 512-column TMEM allocation never waits.
@@ -455,13 +484,19 @@ struct VSSeg {
       d.active[0] = act & 1u;
       d.active[1] = (act >> 1) & 1u;
       d.rule[0][0] = d.rule[0][1] = d.rule[1][0] = d.rule[1][1] = 0;
+      d.bias = tile_needs_bias(d, ex);
     }
     return true;
   }
 };
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool kCount>
+// kPat: the unit patterns a launch holds (bit 1 << UnitPattern); a launch of
+// one pattern compiles only that pattern's planner, loader and softmax paths.
+constexpr int kPatA = 1 << kUnitAshape, kPatV = 1 << kUnitVS, kPatB = 1 << kUnitBlock;
+constexpr int kPatAll = kPatA | kPatV | kPatB;
+
+template <int D, bool kCount, int kPat>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ AttnMaps M, const AttnArgs A,
                        const __grid_constant__ UnitTable UT, const __grid_constant__ SeqTable ST) {
@@ -473,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* sblk = reinterpret_cast<int*>(sm + Ly::kBlk);
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + Ly::kMisc);  // [0] tmem, [2] abort
 
+  constexpr bool kHasA = (kPat & kPatA) != 0, kHasV = (kPat & kPatV) != 0, kHasB = (kPat & kPatB) != 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // sequence of this item (entries ordered by their first item), then band, t and unit within it
   const SeqInfo& SI = ST.s[seq_search(ST.count, [&](int x) { return ST.s[x].item0; }, (int64_t)blockIdx.x)];
@@ -484,6 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int band_units = UT.band[band + 1] - UT.band[band];
   const int t = SI.T - 1 - rem / band_units;
   const Unit& U = UT.u[UT.band[band] + rem % band_units];
+  const bool is_vs = kPat == kPatV || (kHasV && U.pattern == kUnitVS);
+  const bool is_block = kPat == kPatB || (kHasB && U.pattern == kUnitBlock);
+  const bool is_ashape = kPat == kPatA || (kHasA && U.pattern == kUnitAshape);
   const int n = SI.n;
   const Geo G = make_geo(U, t, n, n_tiles(n));
   // rows of the [rows, d] views: token i of head h of this sequence is row H * tok0 + h * n + i
@@ -518,6 +557,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < 4; ++q) misc[8 + q] = 0;  // exponential turns (one per SMSP)
     fence_mbar_init();
   }
+  // masking K-step operands: row selectors (row r of sub-item X has 1.0 in
+  // column 2X + r / 64), key-mask slots zeroed (their columns 0-3 are written per tile)
+  if (is_vs)
+  for (int x = threadIdx.x; x < 4 * 128; x += kThreads) {
+    const int op = x >> 7, r = x & 127;
+    uint8_t* row = sm + Ly::kAug + op * 4096 + (r >> 3) * 256 + (r & 7) * 16;
+    uint32_t w[2] = {0u, 0u};
+    if (op < 2) {
+      const int col = 2 * op + (r >> 6);
+      w[col >> 1] = 0x3F80u << (16 * (col & 1));  // bf16 1.0
+    }
+    *reinterpret_cast<uint4*>(row) = make_uint4(w[0], w[1], 0u, 0u);     // columns 0-7
+    *reinterpret_cast<uint4*>(row + 128) = make_uint4(0u, 0u, 0u, 0u);  // columns 8-15
+  }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -536,9 +590,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     AshapeSeg as;
     BlockSeg bs;
     VSSeg vw;
-    if (U.pattern == kUnitAshape) as.init(U, G, n);
-    else if (U.pattern == kUnitBlock) bs.init(U, G, A, SI, lane, sblk);
-    else vw.init(U, G, A, SI);
+    if (is_ashape) as.init(U, G, n);
+    else if (is_block) bs.init(U, G, A, SI, lane, sblk);
+    else if (kHasV) vw.init(U, G, A, SI);
     bool ok = true;
     for (int j = 0;; ++j) {
       if (misc[2]) { ok = false; break; }
@@ -546,13 +600,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_idle(&bars[kBarDEmpty + slot], ((j / kDescSlots) & 1) ^ 1, kIdleNs)) { ok = false; break; }
       TileDesc& d = descs[slot];
       bool more;
-      if (U.pattern == kUnitVS) {
+      if (is_vs) {
         more = vw.emit(lane, n, d);
       } else {
         // lane 0 takes up to two segments of the union
         int sg[2] = {0, 0}, rl[2][2] = {{0, 0}, {0, 0}}, bits[2] = {0, 0};
         int got = 0;
-        if (lane == 0 && U.pattern == kUnitAshape) {
+        if (kHasA && lane == 0 && is_ashape) {
           for (; got < 2; ++got) {
             int s = 0, r2[2] = {0, 0};
             if (!as.next(s, r2)) break;
@@ -561,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             rl[1][got] = r2[1];
             bits[got] = (r2[0] ? 3 : 0) | (r2[1] ? 12 : 0);
           }
-        } else if (lane == 0) {
+        } else if (kHasB && lane == 0) {
           // Block-Sparse: the two blocks of a tile are taken from the same class
           // (kept by sub-item 0 only, by sub-item 1 only, or by both), so that a
           // sub-item skips the tiles it does not attend; a block waits in
@@ -608,6 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             d.rule[X][1] = (uint8_t)rl[X][1];
             d.active[X] = (((bits[0] | bits[1]) >> (2 * X)) & 3) != 0;
           }
+          d.bias = 0;  // range tiles: whole 64-key segments per half, masked by the softmax
         }
       }
       if (!more && lane == 0) d.kind = kTileEnd;
@@ -640,7 +695,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileDesc& d = descs[j % kDescSlots];
       uint8_t* dst = sR + st * Ly::kTile;
       uint64_t* full = &bars[kBarFull + st];
-      if (d.kind == kTileRange) {
+      if (kHasV && !is_v && d.bias) {
+        // key-mask slot j mod 2 (free: the K(j - 2) releases came after its last reads):
+        // row k, column hh = 0 if half hh attends key k, else -BIG; lane l writes rows 4l..4l+3
+        uint8_t* ka = sm + Ly::kAug + (2 + (j & 1)) * 4096;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int k = 4 * lane + q;
+          uint32_t w[2];
+#pragma unroll
+          for (int p2 = 0; p2 < 2; ++p2) {
+            const uint32_t lo = ((d.mask[2 * p2][k >> 5] >> (k & 31)) & 1u) ? 0u : (uint32_t)kBf16NegBig;
+            const uint32_t hi = ((d.mask[2 * p2 + 1][k >> 5] >> (k & 31)) & 1u) ? 0u : (uint32_t)kBf16NegBig;
+            w[p2] = lo | (hi << 16);
+          }
+          *reinterpret_cast<uint4*>(ka + (k >> 3) * 256 + (k & 7) * 16) = make_uint4(w[0], w[1], 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();  // every lane's rows are written before the full barrier's arrival
+      }
+      if (!kHasV || d.kind == kTileRange) {
         if (lane == 0) {
           const CUtensorMap* map = is_v ? &M.v : &M.k;
           mbar_arrive_expect_tx(full, Ly::kTile);
@@ -691,6 +765,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024) + (uint64_t)X * kTileDesc;
     const uint64_t dk = sdesc_sw128(smem_u32(sR), 16, 1024);  // + slot * kTile
     const uint64_t dv = sdesc_sw128(smem_u32(sR), 16384, 1024);
+    const uint64_t dqa = sdesc_plain(smem_u32(sm + Ly::kAug + X * 4096), 128, 256);
+    const uint64_t dka = sdesc_plain(smem_u32(sm + Ly::kAug + 2 * 4096), 128, 256);  // + (j & 1) * 4096
     const uint32_t tS = tmem + kColS + 128 * X, tO = tmem + kColO + 128 * X;
     auto issue_pv = [&]() -> bool {  // O_X += P_X V of tile `pending`, then release that V slot
       const int vidx = 2 * pending + 1, vst = vidx % kSlots;
@@ -716,6 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileDesc& d = descs[j % kDescSlots];
       const bool end = d.kind == kTileEnd;
       const bool act = d.active[X] != 0;
+      const bool bias = kHasV && d.bias != 0;
       desc_release(j);
       if (end) break;
       const int kidx = 2 * j, kst = kidx % kSlots;
@@ -730,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);  // ((kk/4) * 16384 + (kk%4) * 32) >> 4
             mma_bf16_ss(tS, dq + off, k0 + off, id_qk, kk > 0 ? 1u : 0u);
           }
+          if (bias) mma_bf16_ss(tS, dqa, dka + (uint64_t)((j & 1) * (4096 >> 4)), id_qk, 1u);
           mma_commit(&bars[kBarSFull + X]);
         }
         __syncwarp();
@@ -758,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t colS = kColS + 128 * X, colO = kColO + 128 * X;
     const float c2 = A.scale_log2;
     const int g = U.sub[X].sink, wnd = U.sub[X].window;
-    const bool ashape = U.pattern == kUnitAshape;
+    const bool ashape = kHasA && is_ashape;
     float m_used = -INFINITY, l = 0.f;
     unsigned long long count = 0;
     bool ok = true;
@@ -771,7 +849,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kind = d.kind;
       if (kind == kTileEnd) { desc_release(j); break; }
       if (!d.active[X]) { desc_release(j); continue; }
-      // ---- validity words of this row's 128 keys
+      // ---- validity words of this row's 128 keys (the half's key set only
+      // where the tensor core has not masked it)
+      const bool bias = kHasV && d.bias != 0;
       uint64_t vw[2] = {0ull, 0ull};
       if (row_ok) {
         // causal keys of each 64-column half are its first c[s] columns: for
@@ -779,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // over the tile, so the count comes from a 3-step search over the
         // eight segment starts and the partial one
         int c0, c1;
-        if (kind == kTileRange) {
+        if (!kHasV || kind == kTileRange) {
           c0 = i - d.seg[0] + 1;
           c1 = i - d.seg[1] + 1;
         } else if (d.seg_hi + 15 <= i) {
@@ -792,8 +872,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           c0 = 16 * sc + min(max(i - d.seg[sc] + 1, 0), 16);  // sc <= 7 here
           c1 = c0 - 64;
         }
-        vw[0] = (((uint64_t)d.mask[hh][1] << 32) | d.mask[hh][0]) & low_mask64(c0);
-        vw[1] = (((uint64_t)d.mask[hh][3] << 32) | d.mask[hh][2]) & low_mask64(c1);
+        const uint64_t hm0 = ((uint64_t)d.mask[hh][1] << 32) | d.mask[hh][0];
+        const uint64_t hm1 = ((uint64_t)d.mask[hh][3] << 32) | d.mask[hh][2];
+        vw[0] = (bias ? ~0ull : hm0) & low_mask64(c0);
+        vw[1] = (bias ? ~0ull : hm1) & low_mask64(c1);
         if (ashape) {
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
@@ -804,9 +886,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             vw[s] &= keep;
           }
         }
+        if (kCount) count += __popcll(vw[0] & hm0) + __popcll(vw[1] & hm1);
       }
       desc_release(j);
-      if (kCount) count += __popcll(vw[0]) + __popcll(vw[1]);
 
       // ---- S of this tile (its completion also means this sub-item's previous PV is done)
       if (!mbar_wait(&bars[kBarSFull + X], mine & 1)) { ok = false; break; }
@@ -835,7 +917,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 8; ++x) mx[x] = max3f(mx[x], sv[k + x], sv[k + 8 + x]);
 #pragma unroll
       for (int x = 0; x < 8; ++x) mx[x] = fmaxf(mx[x], sv[120 + x]);
-      const float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+      float mt = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+      if (kHasV && mt < kMaskedBelow) mt = -INFINITY;  // every key of the tile masked for this row
       const float m_new = fmaxf(m_used, mt * c2);
       const bool need = m_new > m_used + kRescaleThreshold;
       const bool any = __any_sync(0xFFFFFFFFu, need);
@@ -858,13 +941,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint64_t c2x2 = pk2(c2, c2), negm = pk2(-mref, -mref);
       uint64_t acc[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};
-      // ---- P over the first 64 columns of S, 32 columns at a time
+      // ---- P over the first 64 columns of S, kPChunk columns (2 kPChunk keys) at a time
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+      for (int half = 0; half < 64 / kPChunk; ++half) {
+        uint32_t pk[kPChunk];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int e = 64 * half + 2 * k;
+        for (int k = 0; k < kPChunk; ++k) {
+          const int e = 2 * kPChunk * half + 2 * k;
           const uint64_t x = fma2(pk2(sv[e], sv[e + 1]), c2x2, negm);
           float x0, x1;
           up2(x, x0, x1);
@@ -874,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           up2(p, p0, p1);
           pk[k] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(tmem + lane_base + colS + 32 * half, pk);
+        tmem_st4(tmem + lane_base + colS + kPChunk * half, pk);
       }
       {
         float a0, a1, a2, a3;
@@ -955,10 +1038,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kCount>
+template <int D, bool kCount, int kPat>
 msa_status launch_impl(const AttnMaps& maps, const AttnArgs& a, const UnitTable& ut, const SeqTable& st,
                        int64_t items, cudaStream_t stream) {
-  auto kern = sparse_attn_kernel<D, kCount>;
+  auto kern = sparse_attn_kernel<D, kCount, kPat>;
   const int smem = Layout<D>::kAlloc;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return MSA_ERR_CUDA;
@@ -967,6 +1050,26 @@ msa_status launch_impl(const AttnMaps& maps, const AttnArgs& a, const UnitTable&
   kern<<<(unsigned)items, kThreads, smem, stream>>>(maps, a, ut, st);
   note_launch();
   return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+template <int kPat>
+msa_status launch_d(int d, bool count, const AttnMaps& maps, const AttnArgs& a, const UnitTable& ut,
+                    const SeqTable& st, int64_t items, cudaStream_t stream) {
+  if (d == 128)
+    return count ? launch_impl<128, true, kPat>(maps, a, ut, st, items, stream)
+                 : launch_impl<128, false, kPat>(maps, a, ut, st, items, stream);
+  return count ? launch_impl<64, true, kPat>(maps, a, ut, st, items, stream)
+               : launch_impl<64, false, kPat>(maps, a, ut, st, items, stream);
+}
+
+msa_status launch_pat(int pat, int d, bool count, const AttnMaps& maps, const AttnArgs& a, const UnitTable& ut,
+                      const SeqTable& st, int64_t items, cudaStream_t stream) {
+  switch (pat) {
+    case kPatA: return launch_d<kPatA>(d, count, maps, a, ut, st, items, stream);
+    case kPatV: return launch_d<kPatV>(d, count, maps, a, ut, st, items, stream);
+    case kPatB: return launch_d<kPatB>(d, count, maps, a, ut, st, items, stream);
+    default: return launch_d<kPatAll>(d, count, maps, a, ut, st, items, stream);
+  }
 }
 
 }  // namespace
@@ -992,14 +1095,11 @@ msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Un
     AttnArgs a = args;
     a.n_units = cnt;
     a.n_bands = nb;
-    msa_status st;
+    int pat = 0;
+    for (int x = 0; x < cnt; ++x) pat |= 1 << ut.u[x].pattern;
+    if (pat != kPatA && pat != kPatV && pat != kPatB) pat = kPatAll;
     const bool count = args.edges != nullptr || args.tiles != nullptr;
-    if (args.d == 128)
-      st = count ? launch_impl<128, true>(maps, a, ut, seqs, items, stream)
-                 : launch_impl<128, false>(maps, a, ut, seqs, items, stream);
-    else
-      st = count ? launch_impl<64, true>(maps, a, ut, seqs, items, stream)
-                 : launch_impl<64, false>(maps, a, ut, seqs, items, stream);
+    const msa_status st = launch_pat(pat, args.d, count, maps, a, ut, seqs, items, stream);
     if (st != MSA_OK) return st;
   }
   return MSA_OK;
