@@ -69,7 +69,7 @@ constexpr uint32_t kIdleNs = 256;          // poll interval of the planner's and
 // P columns per TMEM store: small stores keep few packed values live next to
 // the 128 scores, which is what keeps the softmax free of register spills
 constexpr int kPChunk = 4;
-constexpr bool kTurnLock = true;            // sub-items take turns on each SMSP's MUFU
+constexpr bool kTurnLock = true;            // sub-items take turns on each SMSP's softmax section
 constexpr uint16_t kBf16NegBig = 0xFF7Fu;   // -3.3895e38, the most negative finite bf16
 constexpr float kMaskedBelow = -1e30f;      // a raw score below this is a masked one
 
@@ -901,6 +901,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tmem + lane_base + colS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(u + 32 * c));
         tmem_ld_wait();
       }
+      // The softmax sections of the two sub-items' warps on this SMSP (warp q
+      // and warp q + 4) take turns, from the max to the last P store: each runs
+      // at full issue rate while the tensor core works for the other, instead
+      // of both stretching into each other's MMA window.
+      if (kTurnLock) {
+        if (lane == 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (atomicCAS(const_cast<uint32_t*>(&misc[8 + quarter]), 0u, 1u) != 0u)
+            if (global_timer_ns() - t0 > MSA_WAIT_LIMIT_NS) { misc[2] = 1; set_error(A.err, kErrTimeout); break; }
+        }
+        __syncwarp();
+      }
       // ---- mask, row max (tree)
       if ((~vw[0]) | (~vw[1])) {
 #pragma unroll
@@ -928,17 +940,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      // The exponentials of the two sub-items' warps on this SMSP take turns
-      // on its MUFU unit (warp q and warp q + 4 share SMSP q): a held turn
-      // lets this sub-item's P reach the tensor core in half the time.
-      if (kTurnLock) {
-        if (lane == 0) {
-          const uint64_t t0 = global_timer_ns();
-          while (atomicCAS(const_cast<uint32_t*>(&misc[8 + quarter]), 0u, 1u) != 0u)
-            if (global_timer_ns() - t0 > MSA_WAIT_LIMIT_NS) { misc[2] = 1; set_error(A.err, kErrTimeout); break; }
-        }
-        __syncwarp();
-      }
       const uint64_t c2x2 = pk2(c2, c2), negm = pk2(-mref, -mref);
       uint64_t acc[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};
       // ---- P over the first 64 columns of S, kPChunk columns (2 kPChunk keys) at a time
