@@ -684,9 +684,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hh = 0; hh < 4; ++hh)
         if (G.ex[hh])
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sQ + (hh >> 1) * Ly::kTile + c * 16384 + (hh & 1) * 8192, &M.q, &bars[kBarQ], 64 * c,
-                        qrow0 + U.sub[hh >> 1].qh[hh & 1] * n + G.row0[hh], 0);
+            tma_load_3d_hint(sQ + (hh >> 1) * Ly::kTile + c * 16384 + (hh & 1) * 8192, &M.q, &bars[kBarQ], 64 * c,
+                        qrow0 + U.sub[hh >> 1].qh[hh & 1] * n + G.row0[hh], 0, policy_evict_first());
     }
+    // K and V tiles are re-read by the other items of their KV head: keep them in
+    // L2 ahead of Q (read once, evict-first) and O (written with streaming stores)
+    const uint64_t kv_policy = policy_evict_last();
     // K(j) into slot 2j, V(j) into 2j+1 (mod kSlots): the MMA releases them in that order
     auto load = [&](int j, bool is_v) -> bool {
       const int idx = 2 * j + (is_v ? 1 : 0);
@@ -719,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const CUtensorMap* map = is_v ? &M.v : &M.k;
           mbar_arrive_expect_tx(full, Ly::kTile);
           for (int s = 0; s < 2; ++s)
-            for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384 + s * 8192, map, full, 64 * c, krow0 + d.seg[s], 0);
+            for (int c = 0; c < D / 64; ++c) tma_load_3d_hint(dst + c * 16384 + s * 8192, map, full, 64 * c, krow0 + d.seg[s], 0, kv_policy);
         }
       } else {
         // eight 16-key segments (lane 8c + x: segment x, columns 64c..): a run
@@ -731,9 +734,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s0 = d.seg[h4];
           const bool run = d.seg[h4 + 1] == s0 + 16 && d.seg[h4 + 2] == s0 + 32 && d.seg[h4 + 3] == s0 + 48;
           if (!run)
-            tma_load_3d(dst + c * 16384 + x * 2048, is_v ? &M.v16 : &M.k16, full, 64 * c, krow0 + d.seg[x], 0);
+            tma_load_3d_hint(dst + c * 16384 + x * 2048, is_v ? &M.v16 : &M.k16, full, 64 * c, krow0 + d.seg[x], 0, kv_policy);
           else if (x == h4)
-            tma_load_3d(dst + c * 16384 + x * 2048, is_v ? &M.v : &M.k, full, 64 * c, krow0 + s0, 0);
+            tma_load_3d_hint(dst + c * 16384 + x * 2048, is_v ? &M.v : &M.k, full, 64 * c, krow0 + s0, 0, kv_policy);
         }
       }
       return true;
@@ -1016,7 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pkd[x] = pack_bf16x2(__uint_as_float(o[2 * x]) * inv_l, __uint_as_float(o[2 * x + 1]) * inv_l);
         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) dst[x] = make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]);
+        for (int x = 0; x < 4; ++x) __stcs(dst + x, make_uint4(pkd[4 * x], pkd[4 * x + 1], pkd[4 * x + 2], pkd[4 * x + 3]));
       }
     }
     if (row_ok && A.lse)
