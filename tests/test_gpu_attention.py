@@ -206,6 +206,35 @@ def test_extreme_logits(cuda_lib, pattern):
         compare_rows(f32(o[0, h]), f32(lse[0, h]), ro, rl, f"{pattern} extreme h{h}")
 
 
+def test_extreme_logits_vs(cuda_lib):
+    """The same ramped large logits on Vertical-Slash heads. Keys that a whole
+    64-row half leaves out reach the softmax as the most negative finite bf16
+    added to their score (the tensor-core masking step), so attended scores of
+    any sign and size must still give eq.(2) over the physical set."""
+    n, d, Hq, Hkv = 1000, 128, 2, 1
+    q, k, v = synth.random_qkv(1, Hq, Hkv, n, d, seed=92, device="cuda", scale_q=8.0)
+    ramp = torch.linspace(1.0, 4.0, n, device="cuda")[None, None, :, None]
+    k = (k.float() * ramp).to(torch.bfloat16)
+    rng = np.random.default_rng(93)
+    C = [np.sort(rng.choice(n, 30, replace=False)), np.array([0, 999])]
+    D = [np.sort(rng.choice(n, 20, replace=False))[::-1], np.array([400, 3, 0])]
+    index = cuda_lib.VSIndex(Hq, n, 30, 20, "cuda")
+    for h in range(Hq):
+        index.vertical_bits[h] = torch.from_numpy(pack_bits(C[h], n)).cuda()
+        index.slash_bits[h] = torch.from_numpy(pack_bits(D[h], n)).cuda()
+        index.slash_cover[h] = torch.from_numpy(cover_bits(D[h], n)).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(1, Hq, n, device="cuda")
+    cuda_lib.attn_vs(q, k, v, [0, 1], index, o=o, lse=lse)
+    assert cuda_lib.poll_device_status() == 0
+    for h in range(Hq):
+        qn, kn, vn = head_qkv(q, k, v, 0, h, Hq, Hkv)
+        cfg = dict(pattern=oracle.VS, block=64)
+        ro, rl, _ = oracle.head_rows(cfg, qn, kn, vn, np.arange(n), scale_of(d), C=C[h], D=D[h])
+        assert np.nanmax(rl[np.isfinite(rl)]) > 60.0
+        compare_rows(f32(o[0, h]), f32(lse[0, h]), ro, rl, f"vs extreme h{h}")
+
+
 @pytest.mark.parametrize("n,topk", [
     (700, 20),            # k_b above N_b = 11
     (64 * 520 + 17, 521),  # k_b = N_b = 521: the last rows' lists exceed the 512 entries staged in shared memory
