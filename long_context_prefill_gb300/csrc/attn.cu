@@ -123,7 +123,7 @@ struct Layout {
   static constexpr int kAug = kBlk + 4 * kMaxStagedBlocks * 4;
   static constexpr int kBars = kAug + 4 * 4096;
   static constexpr int kMisc = kBars + kNumBars * 8;
-  static constexpr int kTotal = kMisc + 64;  // misc words: [0] TMEM base, [2] abort, [8..11] exponential turns
+  static constexpr int kTotal = kMisc + 64;  // misc words: [0] TMEM base, [2] abort, [8..11] softmax turns
   // > 113 KB keeps one CTA per SM, so the 512-column TMEM allocation never waits.
   static constexpr int kAlloc = (kTotal + 1024) > 120 * 1024 ? (kTotal + 1024) : 120 * 1024;
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
@@ -554,22 +554,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[kBarDEmpty + s], kDescReaders);
     }
     misc[2] = 0;
-    for (int q = 0; q < 4; ++q) misc[8 + q] = 0;  // exponential turns (one per SMSP)
+    for (int q = 0; q < 4; ++q) misc[8 + q] = 0;  // softmax turns (one per SMSP)
     fence_mbar_init();
   }
   // masking K-step operands: row selectors (row r of sub-item X has 1.0 in
   // column 2X + r / 64), key-mask slots zeroed (their columns 0-3 are written per tile)
-  if (is_vs)
-  for (int x = threadIdx.x; x < 4 * 128; x += kThreads) {
-    const int op = x >> 7, r = x & 127;
-    uint8_t* row = sm + Ly::kAug + op * 4096 + (r >> 3) * 256 + (r & 7) * 16;
-    uint32_t w[2] = {0u, 0u};
-    if (op < 2) {
-      const int col = 2 * op + (r >> 6);
-      w[col >> 1] = 0x3F80u << (16 * (col & 1));  // bf16 1.0
+  if (is_vs) {
+    for (int x = threadIdx.x; x < 4 * 128; x += kThreads) {
+      const int op = x >> 7, r = x & 127;
+      uint8_t* row = sm + Ly::kAug + op * 4096 + (r >> 3) * 256 + (r & 7) * 16;
+      uint32_t w[2] = {0u, 0u};
+      if (op < 2) {
+        const int col = 2 * op + (r >> 6);
+        w[col >> 1] = 0x3F80u << (16 * (col & 1));  // bf16 1.0
+      }
+      *reinterpret_cast<uint4*>(row) = make_uint4(w[0], w[1], 0u, 0u);     // columns 0-7
+      *reinterpret_cast<uint4*>(row + 128) = make_uint4(0u, 0u, 0u, 0u);  // columns 8-15
     }
-    *reinterpret_cast<uint4*>(row) = make_uint4(w[0], w[1], 0u, 0u);     // columns 0-7
-    *reinterpret_cast<uint4*>(row + 128) = make_uint4(0u, 0u, 0u, 0u);  // columns 8-15
   }
   fence_proxy_async_smem();
   tc_fence_before();
