@@ -662,43 +662,59 @@ def dense_and_cold(runs, msa, per_layer, stream, reps=2):
 def end_to_end(runs, msa, K, world, device, stream):
     """The same metric through host buffers: every step copies each layer's
     Q/K/V from pinned host memory, runs msa_prefill_layer, and reads its O
-    back.  Uploads and downloads run on two copy streams ordered by events, so
-    a layer's transfers overlap the neighbouring layers' compute (a layer's
-    buffers are reused only after the step before has finished with them)."""
-    host = []
+    back.  Each layer has two device buffer sets used by alternate steps, so
+    the uploads of the next step and the downloads of this one run on two copy
+    streams while the current step computes (a set is rewritten only after the
+    step two back has finished computing from it and its output has reached
+    the host)."""
+    host, dev = [], []
     for r in runs:
         hq = r.w["q"].cpu().pin_memory()
         hk = r.w["k"].cpu().pin_memory()
         hv = r.w["v"].cpu().pin_memory()
         ho = torch.empty(r.o.shape, dtype=r.o.dtype).pin_memory()
         host.append((hq, hk, hv, ho))
+        dev.append([(r.w["q"], r.w["k"], r.w["v"], r.o),
+                    (torch.empty_like(r.w["q"]), torch.empty_like(r.w["k"]), torch.empty_like(r.w["v"]),
+                     torch.empty_like(r.o))])
     up_stream, down_stream = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev = lambda: torch.cuda.Event()  # noqa: E731
-    uploaded = [ev() for _ in runs]   # inputs of layer L are on the device
-    computed = [ev() for _ in runs]   # layer L's attention has finished (its inputs are free)
-    fetched = [ev() for _ in runs]    # layer L's output has reached the host (its output buffer is free)
-    first = [True]
+    uploaded = [[ev(), ev()] for _ in runs]  # [layer][set]: inputs are on the device
+    computed = [[ev(), ev()] for _ in runs]  # the layer's compute from this set has finished
+    fetched = [[ev(), ev()] for _ in runs]   # the layer's output in this set has reached the host
+    count = [0]
+
+    def upload(x):
+        for L, (hq, hk, hv, _) in enumerate(host):
+            q, k, v, _ = dev[L][x % 2]
+            with torch.cuda.stream(up_stream):
+                if x >= 2:
+                    up_stream.wait_event(computed[L][x % 2])
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+                uploaded[L][x % 2].record(up_stream)
+
+    def compute(x):
+        for L, r in enumerate(runs):
+            q, k, v, o = dev[L][x % 2]
+            stream.wait_event(uploaded[L][x % 2])
+            if x >= 2:
+                stream.wait_event(fetched[L][x % 2])
+            r.layer(q, k, v, o=o, stream=stream)
+            computed[L][x % 2].record(stream)
+            with torch.cuda.stream(down_stream):
+                down_stream.wait_event(computed[L][x % 2])
+                host[L][3].copy_(o, non_blocking=True)
+                fetched[L][x % 2].record(down_stream)
 
     def step():
-        for L, (r, (hq, hk, hv, ho)) in enumerate(zip(runs, host)):
-            with torch.cuda.stream(up_stream):
-                if not first[0]:
-                    up_stream.wait_event(computed[L])
-                r.w["q"].copy_(hq, non_blocking=True)
-                r.w["k"].copy_(hk, non_blocking=True)
-                r.w["v"].copy_(hv, non_blocking=True)
-                uploaded[L].record(up_stream)
-        for L, (r, (hq, hk, hv, ho)) in enumerate(zip(runs, host)):
-            stream.wait_event(uploaded[L])
-            if not first[0]:
-                stream.wait_event(fetched[L])
-            r.layer(r.w["q"], r.w["k"], r.w["v"], o=r.o, stream=stream)
-            computed[L].record(stream)
-            with torch.cuda.stream(down_stream):
-                down_stream.wait_event(computed[L])
-                ho.copy_(r.o, non_blocking=True)
-                fetched[L].record(down_stream)
-        first[0] = False
+        x = count[0]
+        if x == 0:
+            upload(0)
+        upload(x + 1)  # the next step's inputs go up while this one computes
+        compute(x)
+        count[0] += 1
 
     step()
     torch.cuda.synchronize()
@@ -707,17 +723,21 @@ def end_to_end(runs, msa, K, world, device, stream):
     a.record(stream)
     for _ in range(K):
         step()
-    for L in range(len(runs)):
-        stream.wait_event(fetched[L])
+    last = (count[0] - 1) % 2
+    for L in range(len(runs)):  # K uploads (steps 2 .. K+1), K computes and K downloads in the timed region
+        stream.wait_event(fetched[L][last])
+        stream.wait_event(uploaded[L][count[0] % 2])
     b.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     ms = max_over_ranks(a.elapsed_time(b), world, device)
     flops = sum(r.flops for r in runs)
+    del dev
     return {"value": round(world * flops * K / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(sum(r.bytes_in for r in runs)),
             "d2h_bytes_per_step": int(sum(r.bytes_out for r in runs)), "ms_per_step": round(ms / K, 4),
-            "overlap": "uploads and downloads on two copy streams, overlapping other layers' compute"}
+            "overlap": "two device buffer sets per layer: the next step's uploads and this step's downloads "
+                       "run on two copy streams during this step's compute"}
 
 
 def reference_arm(args, world, rank, local, names):
