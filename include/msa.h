@@ -201,7 +201,11 @@ MSA_API msa_status msa_attn_dense(const msa_shape* shape, const void* q, const v
  * u = [a, e] (MInference page §2.1 "1x64 verticals, 64x64 slash tiles" and
  * §4.1 "verticals as points, slashes as intervals"):
  *   N(i) = ( ∪_{δ in D_h} [a-δ, e-δ]  ∪  C_h ) ∩ [0, i].
- * index: as written by msa_build_vs_index for the same `heads`. */
+ * index: as written by msa_build_vs_index for the same `heads`.  Keys that a
+ * whole 64-row query block leaves out of a key tile are masked on the tensor
+ * core by adding -3.39e38 to their scores, so the raw scores q.k must stay
+ * below 1e30 in magnitude (true for any finite bf16 inputs of ordinary
+ * range); attended scores are not changed. */
 MSA_API msa_status msa_attn_vs(const msa_shape* shape, const void* q, const void* k, const void* v, const int32_t* heads,
                        int32_t n_heads, int32_t block, const msa_vs_index* index, void* o, float* lse,
                        int64_t* edges, void* stream);
