@@ -102,3 +102,28 @@ def test_attend_stats_counts(cuda_lib):
     assert np.all(t * 64 * 128 >= e) and np.all(t > 0)
     # every query block of a head is processed in at least one tile
     assert np.all(t >= (sh["n"] + 63) // 64)
+
+
+def test_pattern_kernels_agree_with_the_mixed_kernel(cuda_lib):
+    """A launch of one pattern runs a kernel compiled for that pattern alone;
+    a mixed table runs the kernel that holds all three.  On the same heads and
+    the same index the two must produce the same bits (same items, same tiles,
+    same arithmetic; the calls group the heads as the layer does).  A-shape
+    heads are left out: the layer pairs them across heads, a lone call pairs a
+    head's even and odd tiles."""
+    w = synth.make_workload("mixed", device="cuda", n=3000, Hq=8, Hkv=2)
+    q, k, v, table, sh = w["q"], w["k"], w["v"], w["table"], w["shape"]
+    layer = cuda_lib.Layer(table, 1, sh["Hq"], sh["Hkv"], sh["n"], sh["d"], "cuda")
+    o_mix = torch.empty_like(q)
+    layer(q, k, v, o=o_mix)
+    assert cuda_lib.poll_device_status() == 0
+    vs, bidx, bcnt = layer.indices()
+    vs_heads = [h for h, e in enumerate(table) if e["pattern"] == "vs"]
+    bs_heads = [h for h, e in enumerate(table) if e["pattern"] == "block"]
+    assert vs_heads and bs_heads
+    o_one = torch.zeros_like(q)
+    cuda_lib.attn_vs(q, k, v, vs_heads, vs, o=o_one)
+    cuda_lib.attn_block(q, k, v, bs_heads, table[bs_heads[0]]["topk"], bidx, bcnt, o=o_one)
+    assert cuda_lib.poll_device_status() == 0
+    for h in vs_heads + bs_heads:
+        assert torch.equal(o_one[0, h], o_mix[0, h]), f"head {h} ({table[h]['pattern']})"
