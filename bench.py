@@ -286,9 +286,10 @@ def oracle_sample(runs, target_s=20.0, seed=5):
 
 
 def attention_traffic(names, n_override):
-    """DRAM bytes per attention launch from the committed ncu capture
-    (profiles/sparse_attn_kernel_traffic.json), if the kernel sources still
-    hash to the captured ones and the workloads are the captured full sizes."""
+    """DRAM bytes of each layer's attention launches from the committed ncu
+    capture (profiles/sparse_attn_kernel_traffic.json), if the kernel sources
+    still hash to the captured ones and the workloads are the captured full
+    sizes."""
     import hashlib
     here = os.path.dirname(os.path.abspath(__file__))
     try:
@@ -298,9 +299,9 @@ def attention_traffic(names, n_override):
             h.update(open(os.path.join(here, f), "rb").read())
     except (OSError, KeyError, ValueError):
         return None, None
-    if h.hexdigest() != rec["source_sha256"] or n_override or any(nm not in rec["bytes_per_launch"] for nm in names):
+    if h.hexdigest() != rec["source_sha256"] or n_override or any(nm not in rec["bytes_per_layer"] for nm in names):
         return None, None
-    per = {nm: rec["bytes_per_launch"][nm] for nm in names}
+    per = {nm: rec["bytes_per_layer"][nm] for nm in names}
     return int(sum(per.values())), per
 
 
@@ -499,9 +500,9 @@ def main():
     traffic, traffic_per = attention_traffic([r.name for r in runs], args.n)
     roofline = {"bound": "tensor", "kernel": "sparse_attn_kernel", "achieved": round(achieved, 2), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                "traffic_note": "DRAM bytes (read + write) of the attention launches of one step, one per layer, from "
+                "traffic_note": "DRAM bytes (read + write) of the attention launches of one step (one per pattern of each layer), from "
                                 "the committed ncu capture; null once the kernel source differs from the captured one",
-                "traffic_per_launch": traffic_per,
+                "traffic_per_layer": traffic_per,
                 "peak_source": (f"{pk_src} bf16 " + ("sustained (the clock record shows sw_power_cap)" if capped else
                                                      "burst (no power cap in the clock record of the timed region)")),
                 "frac_of_burst": round(achieved / burst, 4), "frac_of_sustained": round(achieved / sustained, 4),
@@ -583,7 +584,7 @@ def varlen_batch(msa, synth, device, stream, n_seqs=64, lo=1024, hi=16384, seed=
     """A varlen batch (cost-model page §2.2): n_seqs sequences with seeded
     log-uniform lengths in [lo, hi], each the mixed-pattern generator and
     table, packed back to back; one msa_prefill_layer_varlen call (one index
-    pass and one attention launch over all sequences), timed after a warm-up."""
+    pass and one attention launch per pattern over all sequences), timed after a warm-up."""
     rng = np.random.default_rng(seed)
     lens = [int(x) for x in np.exp(rng.uniform(np.log(lo), np.log(hi), size=n_seqs))]
     ws = [synth.make_workload("mixed", device=device, n=n, seed=3000 + i) for i, n in enumerate(lens)]

@@ -225,9 +225,13 @@ MSA_API msa_status msa_attn_block(const msa_shape* shape, const void* q, const v
 /* One layer's sparse prefill attention dispatched per head from the table
  * (MInference page §5.1 "head dispatch": each head reads its pattern, VS and
  * BS heads build their index online, then every head's sparse kernel runs).
- * table: host array of Hq entries.  All indices are built in `ws` and the
- * three patterns run in one attention launch ordered longest-work-first, with
- * no host synchronisation between index and attention. */
+ * table: host array of Hq entries.  All indices are built in `ws`; then each
+ * pattern's heads run in one attention launch of a kernel compiled for that
+ * pattern, ordered longest-work-first.  When the table holds several
+ * patterns, the Vertical-Slash launch runs on `stream` and the others on two
+ * library-owned side streams forked from `stream` and joined back into it,
+ * so the kernels share the SMs and later work on `stream` sees all of them.
+ * No host synchronisation between index and attention. */
 MSA_API msa_status msa_prefill_layer(const msa_shape* shape, const void* q, const void* k, const void* v,
                              const msa_head_cfg* table, void* o, float* lse, int64_t* edges, void* ws,
                              size_t ws_bytes, void* stream);
@@ -306,7 +310,7 @@ MSA_API msa_status msa_layer_varlen_indices(const msa_shape* shape, const msa_he
 /* The two halves of msa_prefill_layer, in order (the time decomposition
  * T = T_index + T_sparse of the MInference page eq.(13)): msa_layer_index
  * builds every Vertical-Slash and Block-Sparse index of the table into `ws`;
- * msa_layer_attend then runs the one attention launch that reads them.
+ * msa_layer_attend then runs the attention launches that read them.
  * msa_prefill_layer(...) == msa_layer_index(...) followed by
  * msa_layer_attend(...) with the same workspace and stream. */
 MSA_API msa_status msa_layer_index(const msa_shape* shape, const void* q, const void* k, const msa_head_cfg* table,

@@ -36,12 +36,15 @@
 // Every (i, j) pair enters the softmax at most once: a key lies in one tile
 // of the item, and masks drop what lies outside N(i) (MInference page §3.2
 // and §5.1 "boundary masks": set to -inf before the max).
-// A launch whose units all share one pattern runs a kernel compiled for that
-// pattern alone (the others' planner, loader and mask code left out); mixed
-// launches run the kernel that holds all three.
+// Every launch runs a kernel compiled for one pattern (the others' planner,
+// loader and mask code left out); a layer with several patterns launches each
+// pattern in its own kernel on forked streams (launch_attention).  The kernel
+// that holds all three is the fallback when the side streams cannot be made.
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -1079,8 +1082,11 @@ msa_status launch_pat(int pat, int d, bool count, const AttnMaps& maps, const At
 
 }  // namespace
 
-msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Unit* units, int n_units,
-                            SeqTable& seqs, cudaStream_t stream) {
+namespace {
+
+// Units of one launch stream (chunks of kMaxUnits, each one kernel launch).
+msa_status launch_units(const AttnMaps& maps, const AttnArgs& args, const Unit* units, int n_units, SeqTable& seqs,
+                        cudaStream_t stream) {
   for (int base = 0; base < n_units; base += kMaxUnits) {
     UnitTable ut;
     const int cnt = n_units - base < kMaxUnits ? n_units - base : kMaxUnits;
@@ -1108,6 +1114,63 @@ msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Un
     if (st != MSA_OK) return st;
   }
   return MSA_OK;
+}
+
+// Two side streams and three events per device, made once: a launch that
+// holds several patterns forks onto them.
+struct ForkSet {
+  cudaStream_t side[2];
+  cudaEvent_t ev[3];
+  bool ok;
+};
+
+ForkSet* fork_set() {
+  static std::mutex mu;
+  static ForkSet sets[64];
+  static bool made[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!made[dev]) {
+    ForkSet& f = sets[dev];
+    f.ok = true;
+    for (int x = 0; x < 2; ++x) f.ok = f.ok && cudaStreamCreateWithFlags(&f.side[x], cudaStreamNonBlocking) == cudaSuccess;
+    for (int x = 0; x < 3; ++x) f.ok = f.ok && cudaEventCreateWithFlags(&f.ev[x], cudaEventDisableTiming) == cudaSuccess;
+    made[dev] = true;
+  }
+  return sets[dev].ok ? &sets[dev] : nullptr;
+}
+
+}  // namespace
+
+// A launch whose units hold several patterns runs each pattern's units in the
+// kernel compiled for that pattern alone, Vertical-Slash on `stream` and the
+// others on two side streams forked from it and joined back: the kernels then
+// share the SMs, each CTA running only its own pattern's code.
+msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Unit* units, int n_units,
+                            SeqTable& seqs, cudaStream_t stream) {
+  std::vector<Unit> by[3];
+  for (int x = 0; x < n_units; ++x) by[units[x].pattern].push_back(units[x]);
+  const int kinds = (by[0].empty() ? 0 : 1) + (by[1].empty() ? 0 : 1) + (by[2].empty() ? 0 : 1);
+  ForkSet* f = kinds > 1 ? fork_set() : nullptr;
+  if (!f) return launch_units(maps, args, units, n_units, seqs, stream);
+  if (cudaEventRecord(f->ev[0], stream) != cudaSuccess) return MSA_ERR_CUDA;
+  const int order[3] = {kUnitVS, kUnitBlock, kUnitAshape};
+  cudaStream_t on[3] = {stream, f->side[0], f->side[1]};
+  msa_status st = MSA_OK;
+  for (int x = 0; x < 3; ++x) {
+    const std::vector<Unit>& u = by[order[x]];
+    if (u.empty()) continue;
+    if (x > 0 && cudaStreamWaitEvent(on[x], f->ev[0], 0) != cudaSuccess) return MSA_ERR_CUDA;
+    const msa_status r = launch_units(maps, args, u.data(), (int)u.size(), seqs, on[x]);
+    if (r != MSA_OK && st == MSA_OK) st = r;
+  }
+  for (int x = 1; x < 3; ++x) {
+    if (by[order[x]].empty()) continue;
+    if (cudaEventRecord(f->ev[x], on[x]) != cudaSuccess || cudaStreamWaitEvent(stream, f->ev[x], 0) != cudaSuccess)
+      return MSA_ERR_CUDA;
+  }
+  return st;
 }
 
 }  // namespace msa

@@ -355,7 +355,7 @@ msa_status msa_prefill_layer_varlen(const msa_shape* shape, const int32_t* cu_se
   LayerPlan W;
   if ((st = layer_prepare(&s, q, k, v, o, lse, edges, table, ws, ws_bytes, W, &seqs)) != MSA_OK) return st;
   cudaStream_t strm = (cudaStream_t)stream;
-  // one index pass and one attention launch over every sequence
+  // one index pass and one attention launch per pattern over every sequence
   if ((st = layer_index(s, q, k, W, strm)) != MSA_OK) return st;
   return layer_attend(s, q, k, v, table, o, lse, edges, W, strm);
 }
