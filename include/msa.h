@@ -225,7 +225,9 @@ MSA_API msa_status msa_attn_block(const msa_shape* shape, const void* q, const v
 /* One layer's sparse prefill attention dispatched per head from the table
  * (MInference page §5.1 "head dispatch": each head reads its pattern, VS and
  * BS heads build their index online, then every head's sparse kernel runs).
- * table: host array of Hq entries.  All indices are built in `ws`; then each
+ * table: host array of Hq entries.  All indices are built in `ws` (with both
+ * kinds present, the Block-Sparse index on a side stream beside the
+ * Vertical-Slash one, joined back into `stream`); then each
  * pattern's heads run in one attention launch of a kernel compiled for that
  * pattern, ordered longest-work-first.  When the table holds several
  * patterns, the Vertical-Slash launch runs on `stream` and the others on two

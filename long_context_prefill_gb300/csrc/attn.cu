@@ -1116,23 +1116,17 @@ msa_status launch_units(const AttnMaps& maps, const AttnArgs& args, const Unit* 
   return MSA_OK;
 }
 
-// Two side streams and three events per device, made once: a launch that
-// holds several patterns forks onto them.
-struct ForkSet {
-  cudaStream_t side[2];
-  cudaEvent_t ev[3];
-  bool ok;
-};
+}  // namespace
 
-ForkSet* fork_set() {
+SideStreams* side_streams() {
   static std::mutex mu;
-  static ForkSet sets[64];
+  static SideStreams sets[64];
   static bool made[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
   if (!made[dev]) {
-    ForkSet& f = sets[dev];
+    SideStreams& f = sets[dev];
     f.ok = true;
     for (int x = 0; x < 2; ++x) f.ok = f.ok && cudaStreamCreateWithFlags(&f.side[x], cudaStreamNonBlocking) == cudaSuccess;
     for (int x = 0; x < 3; ++x) f.ok = f.ok && cudaEventCreateWithFlags(&f.ev[x], cudaEventDisableTiming) == cudaSuccess;
@@ -1140,8 +1134,6 @@ ForkSet* fork_set() {
   }
   return sets[dev].ok ? &sets[dev] : nullptr;
 }
-
-}  // namespace
 
 // A launch whose units hold several patterns runs each pattern's units in the
 // kernel compiled for that pattern alone, Vertical-Slash on `stream` and the
@@ -1152,7 +1144,7 @@ msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Un
   std::vector<Unit> by[3];
   for (int x = 0; x < n_units; ++x) by[units[x].pattern].push_back(units[x]);
   const int kinds = (by[0].empty() ? 0 : 1) + (by[1].empty() ? 0 : 1) + (by[2].empty() ? 0 : 1);
-  ForkSet* f = kinds > 1 ? fork_set() : nullptr;
+  SideStreams* f = kinds > 1 ? side_streams() : nullptr;
   if (!f) return launch_units(maps, args, units, n_units, seqs, stream);
   if (cudaEventRecord(f->ev[0], stream) != cudaSuccess) return MSA_ERR_CUDA;
   const int order[3] = {kUnitVS, kUnitBlock, kUnitAshape};

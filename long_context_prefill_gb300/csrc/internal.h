@@ -141,6 +141,16 @@ struct AttnMaps {
 
 // Launch the attention engine over n_units units per sequence of the table
 // (each sequence's T items per unit; fills item0 and T of every entry).
+// Two non-blocking side streams and three events per device, made on first
+// use (null when they cannot be made): work that may run beside the caller's
+// stream forks onto them from an event and joins back with another.
+struct SideStreams {
+  cudaStream_t side[2];
+  cudaEvent_t ev[3];
+  bool ok;
+};
+SideStreams* side_streams();
+
 msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Unit* units, int n_units,
                             SeqTable& seqs, cudaStream_t stream);
 

@@ -213,15 +213,25 @@ static msa_status layer_prepare(const msa_shape* shape, const void* q, const voi
 static msa_status layer_index(const msa_shape& s, const void* q, const void* k, const LayerPlan& W,
                               cudaStream_t strm) {
   msa_status st = MSA_OK;
-  if (!W.vs_heads.empty()) {
-    st = run_vs_index(s, q, k, W.vs_heads.data(), (int32_t)W.vs_heads.size(), W.vs_cfg, W.vs, W.vs_ws,
-                      W.vs_ws_bytes, strm, &W.seqs);
-    if (st != MSA_OK) return st;
+  // both kinds of index: the Block-Sparse one runs on a side stream beside the
+  // Vertical-Slash one (separate workspaces; both only read Q and K) and joins back
+  SideStreams* f = (!W.vs_heads.empty() && !W.bs_heads.empty()) ? side_streams() : nullptr;
+  cudaStream_t bs_strm = strm;
+  if (f) {
+    if (cudaEventRecord(f->ev[0], strm) != cudaSuccess || cudaStreamWaitEvent(f->side[0], f->ev[0], 0) != cudaSuccess)
+      return MSA_ERR_CUDA;
+    bs_strm = f->side[0];
   }
   if (!W.bs_heads.empty())
     st = run_block_index(s, q, k, W.bs_heads.data(), (int32_t)W.bs_heads.size(), W.bs_cfg.topk, W.bs_idx, W.bs_cnt,
-                         W.bs_ws, W.bs_ws_bytes, strm, &W.seqs);
-  return st;
+                         W.bs_ws, W.bs_ws_bytes, bs_strm, &W.seqs);
+  msa_status vs_st = MSA_OK;
+  if (!W.vs_heads.empty())
+    vs_st = run_vs_index(s, q, k, W.vs_heads.data(), (int32_t)W.vs_heads.size(), W.vs_cfg, W.vs, W.vs_ws,
+                         W.vs_ws_bytes, strm, &W.seqs);
+  if (f && (cudaEventRecord(f->ev[1], bs_strm) != cudaSuccess || cudaStreamWaitEvent(strm, f->ev[1], 0) != cudaSuccess))
+    return MSA_ERR_CUDA;
+  return st != MSA_OK ? st : vs_st;
 }
 
 static msa_status layer_attend(const msa_shape& s, const void* q, const void* k, const void* v,
