@@ -1146,6 +1146,7 @@ msa_status launch_attention(const AttnMaps& maps, const AttnArgs& args, const Un
   const int kinds = (by[0].empty() ? 0 : 1) + (by[1].empty() ? 0 : 1) + (by[2].empty() ? 0 : 1);
   SideStreams* f = kinds > 1 ? side_streams() : nullptr;
   if (!f) return launch_units(maps, args, units, n_units, seqs, stream);
+  std::lock_guard<std::mutex> hold(f->mu);
   if (cudaEventRecord(f->ev[0], stream) != cudaSuccess) return MSA_ERR_CUDA;
   const int order[3] = {kUnitVS, kUnitBlock, kUnitAshape};
   cudaStream_t on[3] = {stream, f->side[0], f->side[1]};

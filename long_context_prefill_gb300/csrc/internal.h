@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <vector>
 
 #include "../../include/msa.h"
@@ -143,11 +144,14 @@ struct AttnMaps {
 // (each sequence's T items per unit; fills item0 and T of every entry).
 // Two non-blocking side streams and three events per device, made on first
 // use (null when they cannot be made): work that may run beside the caller's
-// stream forks onto them from an event and joins back with another.
+// stream forks onto them from an event and joins back with another.  A caller
+// holds `mu` while it records, waits and enqueues, so that calls from several
+// host threads do not interleave their forks on the shared events.
 struct SideStreams {
   cudaStream_t side[2];
   cudaEvent_t ev[3];
   bool ok;
+  std::mutex mu;
 };
 SideStreams* side_streams();
 

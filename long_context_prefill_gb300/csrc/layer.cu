@@ -217,7 +217,9 @@ static msa_status layer_index(const msa_shape& s, const void* q, const void* k, 
   // Vertical-Slash one (separate workspaces; both only read Q and K) and joins back
   SideStreams* f = (!W.vs_heads.empty() && !W.bs_heads.empty()) ? side_streams() : nullptr;
   cudaStream_t bs_strm = strm;
+  std::unique_lock<std::mutex> hold;
   if (f) {
+    hold = std::unique_lock<std::mutex>(f->mu);
     if (cudaEventRecord(f->ev[0], strm) != cudaSuccess || cudaStreamWaitEvent(f->side[0], f->ev[0], 0) != cudaSuccess)
       return MSA_ERR_CUDA;
     bs_strm = f->side[0];
